@@ -1,0 +1,237 @@
+"""CPU oracle for the rotated-Adam matrix-optimizer step (float64, numpy).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this module.  It shares no code with the CUDA path
+(no kernels, headers, helpers or tables); the two meet only in the seeded input
+generator, which holds none of the method's arithmetic.
+
+Sources (page titles as published):
+* Canzona page ("Canzona" matrix-optimizer framework, aitangshan.cn), section
+  3.2.2 "微组调度算法": global LPT sort by compute cost, then greedy grouping
+  with rollback, a min-heap load simulation and a byte cap per micro-group
+  (section 6.1 / the 3.2.2 tip give 512 MB as a typical cap).
+* "分布式训练中的流水线并行与梯度陈旧性优化", section 2.1 (the per-coordinate
+  Adam update m/(sqrt(v)+eps), no bias correction) and section 2.2 (momentum
+  kept as an m x n matrix; power iteration plus QR every K iterations; the
+  two-sided rotation U^T W V).
+* "大模型分布式优化：通信、内存、计算三层解耦实战", section 2.1 (second moment
+  v_t = beta2 v_{t-1} + (1 - beta2) g_t^2).
+
+Readings taken where the pages are silent or garbled (each is listed with its
+reason in the design notes of this repository):
+* the power iteration is taken to a full basis, one subspace-iteration step per
+  refresh: U <- QR(M M^T U), V <- QR(M^T M V), starting from U = I, V = I;
+* QR is Householder with beta = -sgn(x1)*||x|| (sgn(0) = +1), stopped at the
+  numerical rank (||x|| <= rank_rtol * max_j ||a_j||), Q = H_1 ... H_r I, and the
+  first r columns of Q multiplied by sgn(R_kk) so R's diagonal is positive;
+* the rotated update W <- W - lr * U D V^T, D = M~ / (sqrt(v) + eps);
+* v is kept as is across a refresh; no bias correction, no weight decay;
+* an item's bytes are 4*m*n; one GPU is one rank for the heap.
+
+Every function here is a plain restatement of those steps.  No blocking, no
+fusion, no reordering beyond what the definitions allow.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Micro-group planner (Canzona page, section 3.2.2)
+# ---------------------------------------------------------------------------
+
+def item_cost(m: int, n: int) -> int:
+    """Compute-cost proxy of one matrix: m^2 n + m n^2 + m^3 + n^3 (exact int)."""
+    return m * m * n + m * n * n + m ** 3 + n ** 3
+
+
+def item_bytes(m: int, n: int) -> int:
+    """Bytes of one float32 m x n matrix."""
+    return 4 * m * n
+
+
+@dataclasses.dataclass
+class Plan:
+    groups: List[List[int]]       # input indices, in LPT order, per group
+    owners: List[int]             # rank assigned to each input index
+    group_bytes: List[int]        # total bytes per group
+    group_cost: List[int]         # total cost per group
+
+
+def plan(shapes: Sequence[Tuple[int, int]], c_max: int, ranks: int = 1) -> Plan:
+    """Global LPT sort, then greedy grouping with rollback under a byte cap.
+
+    1. Sort all items by cost, descending; equal costs keep input order.
+    2. Walk the sorted list.  Tentatively put the item into the current group:
+       the load simulation gives it to the rank with the smallest accumulated
+       cost in this group (ties: lowest rank id), as a min-heap would.
+    3. If that leaves some rank of the group holding more than c_max bytes and
+       the group already had items, undo the tentative step, close the group,
+       and place the item in a fresh group (where it is alone at first).  An
+       item larger than c_max therefore ends up in a group of its own.
+    """
+    count = len(shapes)
+    cost = [item_cost(m, n) for m, n in shapes]
+    nbytes = [item_bytes(m, n) for m, n in shapes]
+    order = sorted(range(count), key=lambda i: (-cost[i], i))
+
+    groups: List[List[int]] = []
+    owners = [-1] * count
+    current: List[int] = []
+    load = [0] * ranks      # accumulated cost per rank, current group
+    held = [0] * ranks      # accumulated bytes per rank, current group
+
+    for i in order:
+        r = min(range(ranks), key=lambda q: (load[q], q))
+        trial = list(held)
+        trial[r] += nbytes[i]
+        if current and max(trial) > c_max:
+            groups.append(current)          # roll back: close the group
+            current, load, held = [], [0] * ranks, [0] * ranks
+            r = 0
+            trial = list(held)
+            trial[r] += nbytes[i]
+        current.append(i)
+        load[r] += cost[i]
+        held = trial
+        owners[i] = r
+    if current:
+        groups.append(current)
+
+    return Plan(groups=groups, owners=owners,
+                group_bytes=[sum(nbytes[i] for i in g) for g in groups],
+                group_cost=[sum(cost[i] for i in g) for g in groups])
+
+
+# ---------------------------------------------------------------------------
+# Householder QR with positive R diagonal and numerical-rank stop
+# ---------------------------------------------------------------------------
+
+def hqr_plus(A: np.ndarray, rank_rtol: float) -> Tuple[np.ndarray, int, np.ndarray]:
+    """Q factor of a square matrix by Householder reflections.
+
+    tau = rank_rtol * max_j ||a_j||.  For k = 0, 1, ...: x = (H_{k-1}..H_0 A)[k:, k];
+    stop when ||x|| <= tau (r = k).  Otherwise beta_k = -sgn(x_0) ||x|| with
+    sgn(0) = +1, w = x - beta_k e_0, H_k = I - 2 w w^T / (w^T w) on rows k...
+    Q = H_0 H_1 ... H_{r-1} I (accumulated backwards), then column k of Q for
+    k < r is multiplied by sgn(beta_k), which makes R's diagonal positive.
+    Columns r.. are left as the reflectors make them.
+
+    Returns (Q, r, beta[0:r]).
+    """
+    A = np.array(A, dtype=np.float64, copy=True)
+    p, q = A.shape
+    assert p == q, "square input expected"
+    tau = rank_rtol * max(float(np.linalg.norm(A[:, j])) for j in range(q)) if q else 0.0
+
+    reflectors: List[Tuple[int, np.ndarray]] = []
+    betas: List[float] = []
+    for k in range(q):
+        x = A[k:, k]
+        nx = float(np.linalg.norm(x))
+        if nx <= tau:
+            break
+        beta = -nx if x[0] >= 0.0 else nx
+        w = x.copy()
+        w[0] -= beta
+        ww = float(w @ w)
+        # apply H_k to the trailing block (columns k.. of rows k..)
+        A[k:, k:] -= np.outer(w, (2.0 / ww) * (w @ A[k:, k:]))
+        reflectors.append((k, w))
+        betas.append(beta)
+    r = len(reflectors)
+
+    # Backward accumulation: Q = H_0 (H_1 (... (H_{r-1} I))).  When H_k is
+    # applied, columns 0..k-1 of the partial product are still the unit vectors
+    # e_j (j < k), whose rows k.. are zero, so only Q[k:, k:] changes.
+    Q = np.eye(p)
+    for k, w in reversed(reflectors):
+        ww = float(w @ w)
+        Q[k:, k:] -= np.outer(w, (2.0 / ww) * (w @ Q[k:, k:]))
+    for k in range(r):
+        if betas[k] < 0.0:
+            Q[:, k] = -Q[:, k]
+    return Q, r, np.array(betas)
+
+
+# ---------------------------------------------------------------------------
+# One optimizer step for one matrix
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class MatrixState:
+    M: np.ndarray   # momentum, m x n, original coordinates
+    v: np.ndarray   # second moment, m x n, rotated coordinates
+    U: np.ndarray   # left basis, m x m
+    V: np.ndarray   # right basis, n x n
+    rank_u: int = -1
+    rank_v: int = -1
+
+
+def init_state(m: int, n: int) -> MatrixState:
+    """M = 0, v = 0, U = I_m, V = I_n."""
+    return MatrixState(M=np.zeros((m, n)), v=np.zeros((m, n)), U=np.eye(m), V=np.eye(n))
+
+
+def refresh_basis(M: np.ndarray, U: np.ndarray, V: np.ndarray, rank_rtol: float):
+    """One subspace-iteration step on each side: U <- QR+(M M^T U), V <- QR+(M^T M V)."""
+    A_U = M @ (M.T @ U)
+    A_V = M.T @ (M @ V)
+    U_new, r_u, _ = hqr_plus(A_U, rank_rtol)
+    V_new, r_v, _ = hqr_plus(A_V, rank_rtol)
+    return U_new, V_new, r_u, r_v
+
+
+def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: float,
+         eps: float, lr: float, refresh: bool, rank_rtol: float) -> np.ndarray:
+    """One rotated-Adam step; updates `st` in place and returns the new W (float64).
+
+    (1) M <- beta1 M + (1 - beta1) G
+    (2) if refresh: U, V <- subspace-iteration step + QR+
+    (3) G~ = U^T G V, M~ = U^T M V, v <- beta2 v + (1 - beta2) G~^2, D = M~ / (sqrt(v) + eps)
+    (4) W <- W - lr U D V^T
+    """
+    G = np.asarray(G, dtype=np.float64)
+    st.M = beta1 * st.M + (1.0 - beta1) * G
+    if refresh:
+        st.U, st.V, st.rank_u, st.rank_v = refresh_basis(st.M, st.U, st.V, rank_rtol)
+    Gt = (st.U.T @ G) @ st.V
+    Mt = (st.U.T @ st.M) @ st.V
+    st.v = beta2 * st.v + (1.0 - beta2) * (Gt * Gt)
+    D = Mt / (np.sqrt(st.v) + eps)
+    return np.asarray(W, dtype=np.float64) - lr * ((st.U @ D) @ st.V.T)
+
+
+# ---------------------------------------------------------------------------
+# A whole run of a workload (matrices are independent, so any subset can run)
+# ---------------------------------------------------------------------------
+
+def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
+        first_step: int = 1) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
+    """Run `steps` steps (default: the workload's) for the chosen matrices.
+
+    `wl` is a workload object exposing shapes, hyper, refresh(t), w0(i) and
+    grad(i, t).  Returns {i: (W, state)} with W in float64.
+    """
+    items = list(range(wl.count)) if items is None else list(items)
+    steps = wl.steps if steps is None else steps
+    h = wl.hyper
+    out = {}
+    for i in items:
+        m, n = wl.shapes[i]
+        W = wl.w0(i).astype(np.float64)
+        st = init_state(m, n)
+        for t in range(first_step, first_step + steps):
+            W = step(W, wl.grad(i, t), st, h.beta1, h.beta2, h.eps, h.lr, wl.refresh(t),
+                     h.rank_rtol)
+        out[i] = (W, st)
+    return out
+
+
+def orthogonality_error(Q: np.ndarray) -> float:
+    """||Q^T Q - I||_F."""
+    return float(np.linalg.norm(Q.T @ Q - np.eye(Q.shape[1])))
