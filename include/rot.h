@@ -1,0 +1,161 @@
+/*
+ * rot.h - C ABI of the GB300 rotated-Adam matrix-optimizer step.
+ *
+ * The library runs one optimizer step over many independent 2-D float32
+ * parameter matrices W (m x n, row-major) on one GPU.  Per matrix it keeps
+ * momentum M (m x n), a second moment v (m x n) and two orthogonal bases
+ * U (m x m) and V (n x n), and performs
+ *
+ *   (1) M <- beta1 M + (1 - beta1) G
+ *   (2) on refresh steps: U <- QR+(M M^T U), V <- QR+(M^T M V)
+ *   (3) G~ = U^T G V, M~ = U^T M V, v <- beta2 v + (1 - beta2) G~^2,
+ *       D = M~ / (sqrt(v) + eps)
+ *   (4) W <- W - lr U D V^T
+ *
+ * Sources: the momentum matrix, "power iteration + QR every K iterations" and
+ * the two-sided rotation U^T W V are section 2.2 of the page
+ * "分布式训练中的流水线并行与梯度陈旧性优化"; the per-coordinate update
+ * m / (sqrt(v) + eps) is section 2.1 of that page; the second-moment update is
+ * section 2.1 of "大模型分布式优化：通信、内存、计算三层解耦实战"; the
+ * micro-group planner (global LPT sort, greedy grouping with rollback, min-heap
+ * load simulation, byte cap) is section 3.2.2 of the Canzona page.
+ * QR+ is Householder QR with R's diagonal made positive, stopped at the
+ * numerical rank (first column whose remaining norm is <= rank_rtol times the
+ * largest column norm of the input) and completed by the reflectors found so
+ * far.  The power iteration is taken to a full basis (one subspace-iteration
+ * step per refresh, starting from U = I, V = I).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Return 0 (ROT_OK) on success or a negative ROT_E* code.  No C++ exception
+ *   crosses this boundary.  rot_strerror() names a code.
+ * - "device pointer" means memory of the current CUDA device; the caller owns
+ *   all device memory (W, G, the state blob and the workspace blob).  The
+ *   library allocates no device memory.  The plan is host memory owned by the
+ *   library between rot_plan_create() and rot_plan_destroy().
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Device work is enqueued on it and the call returns without waiting, except
+ *   where stated.
+ * - Matrix dimensions: 1 <= m, n <= ROT_MAX_DIM.
+ */
+#ifndef ROT_H_
+#define ROT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ROT_OK 0
+#define ROT_EINVAL (-1)      /* bad argument (null pointer, size, plan/state mismatch) */
+#define ROT_ENOMEM (-2)      /* host allocation failed */
+#define ROT_ECUDA (-3)       /* a CUDA call or kernel launch failed */
+#define ROT_ETIMEOUT (-4)    /* a device-side wait gave up (see rot_status) */
+#define ROT_ENONFINITE (-5)  /* non-finite value found (see rot_status) */
+#define ROT_ENOTSUP (-6)     /* GPU is not sm_103 or the feature is not built */
+
+#define ROT_PREC_TF32 1      /* one TF32 tensor-core product per GEMM */
+#define ROT_PREC_3XTF32 3    /* hi*hi + hi*lo + lo*hi TF32 split, ~fp32 accuracy */
+
+#define ROT_MAX_DIM 65536
+
+#define ROT_WHICH_M 0        /* momentum, m x n */
+#define ROT_WHICH_V2 1       /* second moment v, m x n */
+#define ROT_WHICH_U 2        /* left basis U, m x m */
+#define ROT_WHICH_V 3        /* right basis V, n x n */
+
+typedef struct rot_shape {
+  int32_t m; /* rows (output features) */
+  int32_t n; /* columns (input features) */
+} rot_shape;
+
+typedef struct rot_plan rot_plan;
+
+/* Build the micro-group plan (host only, no device work).
+ * Items are sorted by cost m^2 n + m n^2 + m^3 + n^3 descending (ties: input
+ * order), then packed greedily into groups whose bytes (4 m n per item) stay
+ * <= c_max_bytes; an item that does not fit rolls the group back and opens a
+ * new one, and an item larger than c_max_bytes forms a group of its own
+ * (Canzona page, section 3.2.2).  count == 0 gives a plan with no groups.
+ * Errors: ROT_EINVAL for a null `out`, count < 0, shapes == NULL with
+ * count > 0, a dimension outside [1, ROT_MAX_DIM] or c_max_bytes == 0;
+ * ROT_ENOMEM.  On error *out is set to NULL. */
+int rot_plan_create(const rot_shape* shapes, int32_t count, uint64_t c_max_bytes,
+                    rot_plan** out);
+
+/* Same as rot_plan_create with `ranks` simulated ranks in the min-heap load
+ * simulation (each item goes to the rank with the least accumulated cost in
+ * its group, ties to the lowest id; the byte cap applies per rank).  ranks = 1
+ * is rot_plan_create.  Used to check the planner; the step runs on one GPU
+ * whatever `ranks` was.  Errors as rot_plan_create, plus ranks < 1. */
+int rot_plan_create_ex(const rot_shape* shapes, int32_t count, uint64_t c_max_bytes,
+                       int32_t ranks, rot_plan** out);
+
+/* Free a plan (NULL is accepted). */
+void rot_plan_destroy(rot_plan* plan);
+
+/* Number of micro-groups.  Errors: ROT_EINVAL for null arguments. */
+int rot_plan_groups(const rot_plan* plan, int32_t* n_groups);
+
+/* Group g: its items (input indices in LPT order; the pointer is borrowed and
+ * valid until rot_plan_destroy), item count, total bytes and total cost.
+ * Any output pointer may be NULL.  Errors: ROT_EINVAL for g out of range. */
+int rot_plan_group(const rot_plan* plan, int32_t g, const int32_t** items,
+                   int32_t* n_items, uint64_t* bytes, uint64_t* cost);
+
+/* Owner rank of every input index (borrowed array of `count` entries). */
+int rot_plan_owners(const rot_plan* plan, const int32_t** owners);
+
+/* Bytes of the caller-allocated state blob (M, v, U, V of every matrix plus a
+ * status word; persists across steps) and of the workspace blob (temporaries
+ * of one step, sized for the largest micro-group; contents need not persist).
+ * Both blobs must be 256-byte aligned device memory.  Either output may be
+ * NULL. */
+int rot_state_bytes(const rot_plan* plan, uint64_t* state_bytes, uint64_t* work_bytes);
+
+/* Initialise the state: M = 0, v = 0, U = I, V = I, status word cleared.
+ * Errors: ROT_EINVAL (null plan/state), ROT_ECUDA. */
+int rot_state_init(const rot_plan* plan, void* state, void* stream);
+
+/* One optimizer step for every matrix of the plan, micro-group by micro-group.
+ * W, G: host arrays of `count` device pointers, in input order; W[i] (m x n,
+ * row-major, float32) is updated in place, G[i] is read only.  state: the
+ * initialised state blob; work: the workspace blob.  refresh != 0 runs the
+ * basis refresh (2) before the rotated update.  precision: ROT_PREC_TF32 or
+ * ROT_PREC_3XTF32 (the basis refresh always uses 3xTF32).  rank_rtol in
+ * [1e-6, 1): the QR's numerical-rank threshold relative to the largest
+ * column norm.  Non-finite inputs propagate (IEEE).
+ * Errors: ROT_EINVAL (null pointers, unknown precision, rank_rtol out of
+ * range), ROT_ENOTSUP (device is not sm_103), ROT_ECUDA (launch failure).
+ * Device-side problems are reported by rot_status. */
+int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void* state,
+             void* work, float beta1, float beta2, float eps, float lr, int32_t refresh,
+             int32_t precision, float rank_rtol, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word of
+ * `state`: *status = ROT_OK, or ROT_ETIMEOUT if a device-side wait exceeded its
+ * spin limit since the last call.  Returns ROT_ECUDA if the synchronisation
+ * fails. */
+int rot_status(const rot_plan* plan, void* state, int32_t* status, void* stream);
+
+/* Copy one state matrix of input item `item` as float32 row-major into the
+ * device buffer dst (M or v: m x n; U: m x m; V: n x n).  Asynchronous.
+ * Errors: ROT_EINVAL (item or which out of range, null pointers). */
+int rot_state_export(const rot_plan* plan, const void* state, int32_t item, int32_t which,
+                     float* dst, void* stream);
+
+/* Numerical ranks of U's and V's inputs at the last refresh of `item`
+ * (device memory is read after synchronising `stream`; -1 before any
+ * refresh).  Errors: ROT_EINVAL, ROT_ECUDA. */
+int rot_state_ranks(const rot_plan* plan, const void* state, int32_t item, int32_t* rank_u,
+                    int32_t* rank_v, void* stream);
+
+/* Static description of an error code. */
+const char* rot_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROT_H_ */

@@ -1,0 +1,186 @@
+"""Thin ctypes binding of librot.so (include/rot.h).
+
+Argument marshalling only: every step of the optimizer runs in the library's
+CUDA kernels.  Device memory comes from the caller (PyTorch tensors are used
+for it in the tests and the benchmark); pointers are passed as integers.
+The library must have been built (build.build()); there is no other path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import List, Optional, Sequence, Tuple
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "librot.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "rot.h")
+
+ROT_OK = 0
+ROT_EINVAL = -1
+ROT_ENOMEM = -2
+ROT_ECUDA = -3
+ROT_ETIMEOUT = -4
+ROT_ENONFINITE = -5
+ROT_ENOTSUP = -6
+ROT_PREC_TF32 = 1
+ROT_PREC_3XTF32 = 3
+ROT_WHICH_M, ROT_WHICH_V2, ROT_WHICH_U, ROT_WHICH_V = 0, 1, 2, 3
+
+
+class RotError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+class rot_shape(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("n", ctypes.c_int32)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_u64 = ctypes.c_uint64
+_f32 = ctypes.c_float
+
+_SIGS = {
+    "rot_plan_create": (_i32, [ctypes.POINTER(rot_shape), _i32, _u64, ctypes.POINTER(_vp)]),
+    "rot_plan_create_ex": (_i32, [ctypes.POINTER(rot_shape), _i32, _u64, _i32,
+                                  ctypes.POINTER(_vp)]),
+    "rot_plan_destroy": (None, [_vp]),
+    "rot_plan_groups": (_i32, [_vp, ctypes.POINTER(_i32)]),
+    "rot_plan_group": (_i32, [_vp, _i32, ctypes.POINTER(ctypes.POINTER(_i32)),
+                              ctypes.POINTER(_i32), ctypes.POINTER(_u64), ctypes.POINTER(_u64)]),
+    "rot_plan_owners": (_i32, [_vp, ctypes.POINTER(ctypes.POINTER(_i32))]),
+    "rot_state_bytes": (_i32, [_vp, ctypes.POINTER(_u64), ctypes.POINTER(_u64)]),
+    "rot_state_init": (_i32, [_vp, _vp, _vp]),
+    "rot_step": (_i32, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _vp, _f32, _f32,
+                        _f32, _f32, _i32, _i32, _f32, _vp]),
+    "rot_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32), _vp]),
+    "rot_state_export": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp]),
+    "rot_state_ranks": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp]),
+    "rot_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load librot.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "matrix_optimizer_step_rot_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_symbols() -> List[str]:
+    """Names of the functions include/rot.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rot_[a-z0-9_]+)\s*\(", text)))
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().rot_strerror(code).decode()
+    except Exception:
+        return f"error {code}"
+
+
+def _check(code: int, where: str) -> None:
+    if code != ROT_OK:
+        raise RotError(code, where)
+
+
+class Plan:
+    """Owns a rot_plan handle."""
+
+    def __init__(self, shapes: Sequence[Tuple[int, int]], c_max: int, ranks: int = 1):
+        self.shapes = [(int(m), int(n)) for m, n in shapes]
+        arr = (rot_shape * max(1, len(self.shapes)))(*[rot_shape(m, n) for m, n in self.shapes])
+        h = _vp()
+        _check(lib().rot_plan_create_ex(arr, len(self.shapes), int(c_max), int(ranks),
+                                        ctypes.byref(h)), "rot_plan_create_ex")
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.rot_plan_destroy(h)
+            self.handle = None
+
+    @property
+    def count(self) -> int:
+        return len(self.shapes)
+
+    def groups(self) -> List[List[int]]:
+        n = _i32()
+        _check(lib().rot_plan_groups(self.handle, ctypes.byref(n)), "rot_plan_groups")
+        out = []
+        for g in range(n.value):
+            items = ctypes.POINTER(_i32)()
+            k = _i32()
+            _check(lib().rot_plan_group(self.handle, g, ctypes.byref(items), ctypes.byref(k),
+                                        None, None), "rot_plan_group")
+            out.append([items[j] for j in range(k.value)])
+        return out
+
+    def group_totals(self, g: int) -> Tuple[int, int]:
+        b, c = _u64(), _u64()
+        _check(lib().rot_plan_group(self.handle, g, None, None, ctypes.byref(b),
+                                    ctypes.byref(c)), "rot_plan_group")
+        return b.value, c.value
+
+    def owners(self) -> List[int]:
+        o = ctypes.POINTER(_i32)()
+        _check(lib().rot_plan_owners(self.handle, ctypes.byref(o)), "rot_plan_owners")
+        return [o[i] for i in range(self.count)]
+
+    def state_bytes(self) -> Tuple[int, int]:
+        s, w = _u64(), _u64()
+        _check(lib().rot_state_bytes(self.handle, ctypes.byref(s), ctypes.byref(w)),
+               "rot_state_bytes")
+        return s.value, w.value
+
+
+def rot_state_init(plan: Plan, state_ptr: int, stream: int) -> None:
+    _check(lib().rot_state_init(plan.handle, _vp(state_ptr), _vp(stream)), "rot_state_init")
+
+
+def rot_step(plan: Plan, w_ptrs: Sequence[int], g_ptrs: Sequence[int], state_ptr: int,
+             work_ptr: int, beta1: float, beta2: float, eps: float, lr: float, refresh: bool,
+             precision: int, rank_rtol: float, stream: int) -> None:
+    n = max(1, plan.count)
+    W = (_vp * n)(*[_vp(p) for p in w_ptrs])
+    G = (_vp * n)(*[_vp(p) for p in g_ptrs])
+    _check(lib().rot_step(plan.handle, W, G, _vp(state_ptr), _vp(work_ptr), beta1, beta2, eps,
+                          lr, 1 if refresh else 0, precision, rank_rtol, _vp(stream)),
+           "rot_step")
+
+
+def rot_status(plan: Plan, state_ptr: int, stream: int) -> int:
+    st = _i32()
+    _check(lib().rot_status(plan.handle, _vp(state_ptr), ctypes.byref(st), _vp(stream)),
+           "rot_status")
+    return st.value
+
+
+def rot_state_export(plan: Plan, state_ptr: int, item: int, which: int, dst_ptr: int,
+                     stream: int) -> None:
+    _check(lib().rot_state_export(plan.handle, _vp(state_ptr), item, which, _vp(dst_ptr),
+                                  _vp(stream)), "rot_state_export")
+
+
+def rot_state_ranks(plan: Plan, state_ptr: int, item: int, stream: int) -> Tuple[int, int]:
+    ru, rv = _i32(), _i32()
+    _check(lib().rot_state_ranks(plan.handle, _vp(state_ptr), item, ctypes.byref(ru),
+                                 ctypes.byref(rv), _vp(stream)), "rot_state_ranks")
+    return ru.value, rv.value

@@ -1,0 +1,197 @@
+// Element-wise kernels of the step: momentum (+ TF32 split of G), the Adam
+// update in rotated coordinates, transposes, fills and exports.
+//
+// All of them are HBM-bound.  Each launch covers many matrices: blockIdx.y
+// selects the matrix, blockIdx.x strides over its elements; the per-matrix
+// descriptors travel in the kernel's parameter block.
+#include <algorithm>
+#include <cstring>
+
+#include "rot_internal.h"
+#include "split.cuh"
+
+namespace rot {
+namespace {
+
+constexpr int kMaxSegs = 64;
+constexpr int kThreads = 256;
+
+template <class Seg>
+struct SegBatch {
+  int count;
+  Seg seg[kMaxSegs];
+};
+
+inline unsigned grid_x_for(int64_t elems) {
+  int64_t blocks = (elems + kThreads * 4 - 1) / (kThreads * 4);
+  return (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, 4096));
+}
+
+template <class Seg, class Kernel, class... Args>
+int launch_segs(const std::vector<Seg>& segs, Kernel kernel, cudaStream_t stream,
+                Args... args) {
+  for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
+    SegBatch<Seg> b;
+    std::memset(&b, 0, sizeof(b));
+    b.count = (int)std::min<size_t>(kMaxSegs, segs.size() - base);
+    int64_t most = 0;
+    for (int i = 0; i < b.count; ++i) {
+      b.seg[i] = segs[base + i];
+      most = std::max<int64_t>(most, (int64_t)b.seg[i].rows * b.seg[i].cols);
+    }
+    if (most == 0) continue;
+    dim3 grid(grid_x_for(most), b.count);
+    kernel<<<grid, kThreads, 0, stream>>>(b, args...);
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+  }
+  return ROT_OK;
+}
+
+// M <- beta1 M + (1 - beta1) G, with M held as a split; also writes G's split.
+__global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b, float beta1) {
+  const MomentumSeg& s = b.seg[blockIdx.y];
+  const int64_t total = (int64_t)s.rows * s.cols;
+  const float one_minus = 1.0f - beta1;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
+    const int64_t o = (int64_t)r * s.ldm + c;
+    const float g = s.g[e];
+    const float m = beta1 * (s.m_hi[o] + s.m_lo[o]) + one_minus * g;
+    float h, l;
+    split_tf32(m, h, l);
+    s.m_hi[o] = h;
+    s.m_lo[o] = l;
+    split_tf32(g, h, l);
+    s.g_hi[o] = h;
+    s.g_lo[o] = l;
+  }
+}
+
+// v <- beta2 v + (1 - beta2) G~^2 ;  D = M~ / (sqrt(v) + eps)  (D as a split)
+__global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float beta2, float eps) {
+  const AdamSeg& s = b.seg[blockIdx.y];
+  const int64_t total = (int64_t)s.rows * s.cols;
+  const float one_minus = 1.0f - beta2;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
+    const int64_t o = (int64_t)r * s.ld + c;
+    const float g = s.gt[o];
+    const float v = beta2 * s.v[o] + one_minus * (g * g);
+    s.v[o] = v;
+    const float d = s.mt[o] / (sqrtf(v) + eps);
+    float h, l;
+    split_tf32(d, h, l);
+    s.d_hi[o] = h;
+    s.d_lo[o] = l;
+  }
+}
+
+// Tiled transpose through shared memory (32 x 32 tiles, padded against bank
+// conflicts).  blockIdx.y = matrix, blockIdx.x strides over tiles.
+__global__ void transpose_kernel(const __grid_constant__ SegBatch<TransposeSeg> b) {
+  __shared__ float th[32][33];
+  __shared__ float tl[32][33];
+  const TransposeSeg& s = b.seg[blockIdx.y];
+  const int tiles_r = (s.rows + 31) / 32, tiles_c = (s.cols + 31) / 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+    for (int i = ty; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + tx;
+      float x = 0.f, y = 0.f;
+      if (r < s.rows && c < s.cols) {
+        const int64_t o = (int64_t)r * s.ld_src + c;
+        x = s.s_hi[o];
+        y = s.src_is_split ? s.s_lo[o] : 0.f;
+      }
+      th[i][tx] = x;
+      tl[i][tx] = y;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int c = c0 + i, r = r0 + tx;  // output row c, column r
+      if (r < s.rows && c < s.cols) {
+        const float v = th[tx][i] + tl[tx][i];
+        const int64_t o = (int64_t)c * s.ld_dst + r;
+        if (s.dst_is_split) {
+          float h, l;
+          split_tf32(v, h, l);
+          s.d_hi[o] = h;
+          s.d_lo[o] = l;
+        } else {
+          s.d_hi[o] = v;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void fill_kernel(const __grid_constant__ SegBatch<FillSeg> b) {
+  const FillSeg& s = b.seg[blockIdx.y];
+  const int64_t total = (int64_t)s.rows * s.cols;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
+    const int64_t o = (int64_t)r * s.ld + c;
+    s.hi[o] = (s.identity && r == c) ? 1.0f : 0.0f;
+    if (s.lo) s.lo[o] = 0.0f;
+  }
+}
+
+__global__ void combine_kernel(const float* hi, const float* lo, int ld_src, float* dst,
+                               int ld_dst, int rows, int cols) {
+  const int64_t total = (int64_t)rows * cols;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / cols), c = (int)(e - (int64_t)r * cols);
+    const int64_t o = (int64_t)r * ld_src + c;
+    dst[(int64_t)r * ld_dst + c] = lo ? hi[o] + lo[o] : hi[o];
+  }
+}
+
+}  // namespace
+
+int launch_momentum(const std::vector<MomentumSeg>& segs, float beta1, cudaStream_t stream) {
+  return launch_segs(segs, momentum_kernel, stream, beta1);
+}
+
+int launch_adam(const std::vector<AdamSeg>& segs, float beta2, float eps, cudaStream_t stream) {
+  return launch_segs(segs, adam_kernel, stream, beta2, eps);
+}
+
+int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream) {
+  for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
+    SegBatch<TransposeSeg> b;
+    std::memset(&b, 0, sizeof(b));
+    b.count = (int)std::min<size_t>(kMaxSegs, segs.size() - base);
+    int64_t most = 0;
+    for (int i = 0; i < b.count; ++i) {
+      b.seg[i] = segs[base + i];
+      most = std::max<int64_t>(most, (int64_t)((b.seg[i].rows + 31) / 32) *
+                                         ((b.seg[i].cols + 31) / 32));
+    }
+    if (most == 0) continue;
+    dim3 grid((unsigned)std::min<int64_t>(most, 2048), b.count);
+    transpose_kernel<<<grid, 256, 0, stream>>>(b);
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+  }
+  return ROT_OK;
+}
+
+int launch_fill(const std::vector<FillSeg>& segs, cudaStream_t stream) {
+  return launch_segs(segs, fill_kernel, stream);
+}
+
+int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,
+                   int rows, int cols, cudaStream_t stream) {
+  const int64_t total = (int64_t)rows * cols;
+  if (total == 0) return ROT_OK;
+  combine_kernel<<<grid_x_for(total), kThreads, 0, stream>>>(hi, lo, ld_src, dst, ld_dst, rows,
+                                                             cols);
+  return cudaGetLastError() == cudaSuccess ? ROT_OK : ROT_ECUDA;
+}
+
+}  // namespace rot

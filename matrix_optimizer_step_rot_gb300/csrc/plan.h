@@ -1,0 +1,65 @@
+// Plan object behind the opaque rot_plan handle: groups, owners and the byte
+// offsets of every buffer in the caller's state and workspace blobs.
+#pragma once
+
+#include <stdint.h>
+
+#include <vector>
+
+#include "rot.h"
+#include "rot_internal.h"
+
+namespace rot {
+
+// Offsets (bytes from the state blob's base) of one matrix's state.
+struct ItemLayout {
+  int m, n, ldm, ldn;                 // ldm = pad(m), ldn = pad(n)
+  uint64_t m_hi, m_lo;                // momentum split, m x ldn
+  uint64_t v;                         // second moment, m x ldn
+  uint64_t u_hi, u_lo, ut_hi, ut_lo;  // U and U^T splits, m x ldm
+  uint64_t vb_hi, vb_lo, vt_hi, vt_lo;  // V and V^T splits, n x ldn
+};
+
+// Offsets (bytes from the workspace blob's base) of one matrix's temporaries
+// while its micro-group runs.
+struct WorkLayout {
+  // rotation region
+  uint64_t g_hi, g_lo;    // G split (m x ldn); later D split
+  uint64_t sg_hi, sg_lo;  // (G V)^T split (n x ldm); later (D V^T)^T split
+  uint64_t sm_hi, sm_lo;  // (M V)^T split (n x ldm)
+  uint64_t gt, mt;        // G~, M~ float32 (m x ldn)
+  // refresh region
+  uint64_t mT_hi, mT_lo;  // M^T split (n x ldm)
+  int zu_rows, zu_ld;
+  uint64_t zu_hi, zu_lo;  // (M^T U)^T (m x ldn) or M M^T (m x ldm)
+  int zv_rows, zv_ld;
+  uint64_t zv_hi, zv_lo;  // (M V)^T (n x ldm) or M^T M (n x ldn)
+  uint64_t aut, avt;      // A_U^T (m x ldm), A_V^T (n x ldn), float32
+  uint64_t qut, qvt;      // Q^T outputs of the QR, float32
+  uint64_t aux_u, aux_v;  // QR scratch
+};
+
+uint64_t item_cost(int64_t m, int64_t n);
+uint64_t item_bytes(int64_t m, int64_t n);
+
+}  // namespace rot
+
+struct rot_plan {
+  int32_t count = 0;
+  int32_t ranks = 1;
+  uint64_t c_max = 0;
+  std::vector<rot_shape> shapes;
+  std::vector<std::vector<int32_t>> groups;
+  std::vector<uint64_t> group_bytes, group_cost;
+  std::vector<int32_t> owners;
+  // layout
+  uint64_t state_bytes = 0, work_bytes = 0;
+  uint64_t ranks_off = 0;  // int32 pairs (rank_u, rank_v) per item
+  std::vector<rot::ItemLayout> items;
+  std::vector<std::vector<rot::WorkLayout>> work;  // [group][position in group]
+};
+
+namespace rot {
+void build_groups(rot_plan* p);
+void build_layout(rot_plan* p);
+}  // namespace rot

@@ -1,0 +1,351 @@
+// C ABI: state initialisation, the step itself, status and state export.
+//
+// A step runs micro-group by micro-group (the plan's order), all on the
+// caller's stream:
+//   momentum     M <- beta1 M + (1 - beta1) G (and G's TF32 split)
+//   refresh      M^T; Z = M^T U or M M^T, ...; A_U, A_V; batched QR+ -> U, V
+//   rotation     (G V)^T, (M V)^T; G~ = U^T G V, M~ = U^T M V
+//   Adam         v <- beta2 v + (1 - beta2) G~^2; D = M~ / (sqrt(v) + eps)
+//   back         (D V^T)^T; W <- W - lr U (D V^T)
+// Every product is C = A * B^T with both operands K-major, so U, V are kept
+// both as-is and transposed, and the intermediates are written in the layout
+// their consumer reads.
+#include <cstring>
+#include <vector>
+
+#include "plan.h"
+#include "rot_internal.h"
+
+namespace rot {
+
+int gemm_simt(const std::vector<GemmProblem>& probs, int precision, cudaStream_t stream);
+
+int gemm_grouped(const std::vector<GemmProblem>& probs, int precision, int* status,
+                 cudaStream_t stream) {
+  (void)status;
+  return gemm_simt(probs, precision, stream);
+}
+
+namespace {
+
+inline float* F(void* base, uint64_t off) {
+  return reinterpret_cast<float*>(static_cast<char*>(base) + off);
+}
+inline const float* F(const void* base, uint64_t off) {
+  return reinterpret_cast<const float*>(static_cast<const char*>(base) + off);
+}
+
+GemmProblem gp(int M, int N, int K, const float* ah, const float* al, int lda, const float* bh,
+               const float* bl, int ldb, float* ch, float* cl, int ldc, int epi,
+               float alpha = 0.f) {
+  GemmProblem P;
+  P.M = M;
+  P.N = N;
+  P.K = K;
+  P.a_hi = ah;
+  P.a_lo = al;
+  P.lda = lda;
+  P.b_hi = bh;
+  P.b_lo = bl;
+  P.ldb = ldb;
+  P.c_hi = ch;
+  P.c_lo = cl;
+  P.ldc = ldc;
+  P.epi = epi;
+  P.alpha = alpha;
+  return P;
+}
+
+int check_device() {
+  static int cached = 0;  // 1 ok, -1 not supported
+  if (cached == 0) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ROT_ECUDA;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cached = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return cached == 1 ? ROT_OK : ROT_ENOTSUP;
+}
+
+#define ROT_TRY(x)             \
+  do {                         \
+    const int _e = (x);        \
+    if (_e != ROT_OK) return _e; \
+  } while (0)
+
+int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* G, void* state,
+              void* work, float beta1, float beta2, float eps, float lr, int refresh,
+              int precision, float rank_rtol, cudaStream_t s) {
+  const std::vector<int32_t>& items = p->groups[g];
+  const std::vector<WorkLayout>& WL = p->work[g];
+  int* status = static_cast<int*>(state);
+  const size_t n_items = items.size();
+
+  // (1) momentum, and the TF32 split of G
+  {
+    std::vector<MomentumSeg> segs(n_items);
+    for (size_t k = 0; k < n_items; ++k) {
+      const int i = items[k];
+      const ItemLayout& L = p->items[i];
+      if (!W[i] || !G[i]) return ROT_EINVAL;
+      segs[k] = {G[i], F(state, L.m_hi), F(state, L.m_lo), F(work, WL[k].g_hi),
+                 F(work, WL[k].g_lo), L.m, L.n, L.ldn};
+    }
+    ROT_TRY(launch_momentum(segs, beta1, s));
+  }
+
+  // (2) basis refresh
+  if (refresh) {
+    std::vector<TransposeSeg> tr(n_items);
+    for (size_t k = 0; k < n_items; ++k) {
+      const ItemLayout& L = p->items[items[k]];
+      const WorkLayout& x = WL[k];
+      tr[k] = {F(state, L.m_hi), F(state, L.m_lo), L.ldn, F(work, x.mT_hi), F(work, x.mT_lo),
+               L.ldm, L.m, L.n, 1, 1};
+    }
+    ROT_TRY(launch_transpose(tr, s));
+
+    std::vector<GemmProblem> first, second;
+    for (size_t k = 0; k < n_items; ++k) {
+      const ItemLayout& L = p->items[items[k]];
+      const WorkLayout& x = WL[k];
+      const int m = L.m, n = L.n;
+      const float *Mh = F(state, L.m_hi), *Ml = F(state, L.m_lo);
+      const float *MTh = F(work, x.mT_hi), *MTl = F(work, x.mT_lo);
+      float *Zuh = F(work, x.zu_hi), *Zul = F(work, x.zu_lo);
+      float *Zvh = F(work, x.zv_hi), *Zvl = F(work, x.zv_lo);
+      if (n < m) {
+        // Z_U = M^T U (n x m), stored transposed (m x n);  A_U = M Z_U
+        first.push_back(gp(n, m, m, MTh, MTl, L.ldm, F(state, L.ut_hi), F(state, L.ut_lo), L.ldm,
+                           Zuh, Zul, x.zu_ld, kEpiStoreSplitT));
+        second.push_back(gp(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, F(work, x.aut), nullptr,
+                            L.ldm, kEpiStoreF32T));
+      } else {
+        // Gram M M^T (m x m);  A_U = Gram U
+        first.push_back(gp(m, m, n, Mh, Ml, L.ldn, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld,
+                           kEpiStoreSplit));
+        second.push_back(gp(m, m, m, Zuh, Zul, x.zu_ld, F(state, L.ut_hi), F(state, L.ut_lo),
+                            L.ldm, F(work, x.aut), nullptr, L.ldm, kEpiStoreF32T));
+      }
+      if (m < n) {
+        // Z_V = M V (m x n), stored transposed (n x m);  A_V = M^T Z_V
+        first.push_back(gp(m, n, n, Mh, Ml, L.ldn, F(state, L.vt_hi), F(state, L.vt_lo), L.ldn,
+                           Zvh, Zvl, x.zv_ld, kEpiStoreSplitT));
+        second.push_back(gp(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, F(work, x.avt), nullptr,
+                            L.ldn, kEpiStoreF32T));
+      } else {
+        // Gram M^T M (n x n);  A_V = Gram V
+        first.push_back(gp(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
+                           kEpiStoreSplit));
+        second.push_back(gp(n, n, n, Zvh, Zvl, x.zv_ld, F(state, L.vt_hi), F(state, L.vt_lo),
+                            L.ldn, F(work, x.avt), nullptr, L.ldn, kEpiStoreF32T));
+      }
+    }
+    ROT_TRY(gemm_grouped(first, ROT_PREC_3XTF32, status, s));
+    ROT_TRY(gemm_grouped(second, ROT_PREC_3XTF32, status, s));
+
+    std::vector<QrProblem> qp;
+    int32_t* ranks = reinterpret_cast<int32_t*>(static_cast<char*>(state) + p->ranks_off);
+    for (size_t k = 0; k < n_items; ++k) {
+      const int i = items[k];
+      const ItemLayout& L = p->items[i];
+      const WorkLayout& x = WL[k];
+      const int rmax = L.m < L.n ? L.m : L.n;
+      for (int side = 0; side < 2; ++side) {
+        const int pdim = side == 0 ? L.m : L.n;
+        const int ld = side == 0 ? L.ldm : L.ldn;
+        char* aux = static_cast<char*>(work) + (side == 0 ? x.aux_u : x.aux_v);
+        const uint64_t np = (uint64_t)((rmax + kQrPanel - 1) / kQrPanel);
+        QrProblem q;
+        std::memset(&q, 0, sizeof(q));
+        q.at = F(work, side == 0 ? x.aut : x.avt);
+        q.qt = F(work, side == 0 ? x.qut : x.qvt);
+        q.tf = reinterpret_cast<float*>(aux);
+        q.beta = reinterpret_cast<float*>(aux + align256(np * kQrPanel * kQrPanel * 4));
+        q.ctrl = reinterpret_cast<int*>(aux + align256(np * kQrPanel * kQrPanel * 4) +
+                                        align256((uint64_t)rmax * 4 + 4));
+        q.tau = reinterpret_cast<float*>(aux + align256(np * kQrPanel * kQrPanel * 4) +
+                                         align256((uint64_t)rmax * 4 + 4) + align256((np + 2) * 4));
+        q.p = pdim;
+        q.ld = ld;
+        q.rmax = rmax;
+        q.u = side == 0 ? Split{F(state, L.u_hi), F(state, L.u_lo)}
+                        : Split{F(state, L.vb_hi), F(state, L.vb_lo)};
+        q.ut = side == 0 ? Split{F(state, L.ut_hi), F(state, L.ut_lo)}
+                         : Split{F(state, L.vt_hi), F(state, L.vt_lo)};
+        q.ld_out = ld;
+        q.rank_out = ranks + 2 * i + side;
+        qp.push_back(q);
+      }
+    }
+    ROT_TRY(qr_batched(qp, rank_rtol, status, s));
+  }
+
+  // (3) rotation: S_G^T = (G V)^T, S_M^T = (M V)^T ; G~ = U^T S_G, M~ = U^T S_M
+  {
+    std::vector<GemmProblem> a, b;
+    for (size_t k = 0; k < n_items; ++k) {
+      const ItemLayout& L = p->items[items[k]];
+      const WorkLayout& x = WL[k];
+      const int m = L.m, n = L.n;
+      const float *Vth = F(state, L.vt_hi), *Vtl = F(state, L.vt_lo);
+      a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, Vth, Vtl, L.ldn,
+                     F(work, x.sg_hi), F(work, x.sg_lo), L.ldm, kEpiStoreSplitT));
+      a.push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
+                     F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT));
+      const float *Uth = F(state, L.ut_hi), *Utl = F(state, L.ut_lo);
+      b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
+                     F(work, x.gt), nullptr, L.ldn, kEpiStoreF32));
+      b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
+                     F(work, x.mt), nullptr, L.ldn, kEpiStoreF32));
+    }
+    ROT_TRY(gemm_grouped(a, precision, status, s));
+    ROT_TRY(gemm_grouped(b, precision, status, s));
+  }
+
+  // (3') Adam in rotated coordinates; D's split overwrites G's split
+  {
+    std::vector<AdamSeg> segs(n_items);
+    for (size_t k = 0; k < n_items; ++k) {
+      const ItemLayout& L = p->items[items[k]];
+      const WorkLayout& x = WL[k];
+      segs[k] = {F(work, x.gt), F(work, x.mt), F(state, L.v), F(work, x.g_hi), F(work, x.g_lo),
+                 L.m, L.n, L.ldn};
+    }
+    ROT_TRY(launch_adam(segs, beta2, eps, s));
+  }
+
+  // (4) back-rotation: (D V^T)^T into S_G's buffer; W -= lr U (D V^T)
+  {
+    std::vector<GemmProblem> a, b;
+    for (size_t k = 0; k < n_items; ++k) {
+      const int i = items[k];
+      const ItemLayout& L = p->items[i];
+      const WorkLayout& x = WL[k];
+      const int m = L.m, n = L.n;
+      a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, F(state, L.vb_hi),
+                     F(state, L.vb_lo), L.ldn, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
+                     kEpiStoreSplitT));
+      b.push_back(gp(m, n, m, F(state, L.u_hi), F(state, L.u_lo), L.ldm, F(work, x.sg_hi),
+                     F(work, x.sg_lo), L.ldm, W[i], nullptr, n, kEpiApply, lr));
+    }
+    ROT_TRY(gemm_grouped(a, precision, status, s));
+    ROT_TRY(gemm_grouped(b, precision, status, s));
+  }
+  return ROT_OK;
+}
+
+}  // namespace
+}  // namespace rot
+
+using namespace rot;
+
+extern "C" {
+
+int rot_state_init(const rot_plan* plan, void* state, void* stream) {
+  if (!plan || !state) return ROT_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(state) & 255) != 0) return ROT_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(state, 0, 256, s) != cudaSuccess) return ROT_ECUDA;
+  if (cudaMemsetAsync(static_cast<char*>(state) + plan->ranks_off, 0xff,
+                      8ull * (uint64_t)(plan->count > 0 ? plan->count : 1), s) != cudaSuccess)
+    return ROT_ECUDA;
+  std::vector<FillSeg> segs;
+  for (int32_t i = 0; i < plan->count; ++i) {
+    const ItemLayout& L = plan->items[i];
+    segs.push_back({F(state, L.m_hi), F(state, L.m_lo), L.m, L.n, L.ldn, 0});
+    segs.push_back({F(state, L.v), nullptr, L.m, L.n, L.ldn, 0});
+    segs.push_back({F(state, L.u_hi), F(state, L.u_lo), L.m, L.m, L.ldm, 1});
+    segs.push_back({F(state, L.ut_hi), F(state, L.ut_lo), L.m, L.m, L.ldm, 1});
+    segs.push_back({F(state, L.vb_hi), F(state, L.vb_lo), L.n, L.n, L.ldn, 1});
+    segs.push_back({F(state, L.vt_hi), F(state, L.vt_lo), L.n, L.n, L.ldn, 1});
+  }
+  return launch_fill(segs, s);
+}
+
+int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void* state,
+             void* work, float beta1, float beta2, float eps, float lr, int32_t refresh,
+             int32_t precision, float rank_rtol, void* stream) {
+  if (!plan) return ROT_EINVAL;
+  if (plan->count == 0) return ROT_OK;
+  if (!W || !G || !state || !work) return ROT_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(state) & 255) || (reinterpret_cast<uintptr_t>(work) & 255))
+    return ROT_EINVAL;
+  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32) return ROT_EINVAL;
+  if (!(rank_rtol >= 1e-6f && rank_rtol < 1.f)) return ROT_EINVAL;
+  for (int32_t i = 0; i < plan->count; ++i)
+    if (!W[i] || !G[i]) return ROT_EINVAL;
+  const int dev = check_device();
+  if (dev != ROT_OK) return dev;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (size_t g = 0; g < plan->groups.size(); ++g) {
+    const int e = run_group(plan, g, W, G, state, work, beta1, beta2, eps, lr, refresh != 0,
+                            precision, rank_rtol, s);
+    if (e != ROT_OK) return e;
+  }
+  return ROT_OK;
+}
+
+int rot_status(const rot_plan* plan, void* state, int32_t* status, void* stream) {
+  if (!plan || !state || !status) return ROT_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, state, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return ROT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ROT_ECUDA;
+  if (host != 0) {
+    if (cudaMemsetAsync(state, 0, sizeof(int32_t), s) != cudaSuccess) return ROT_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ROT_ECUDA;
+  }
+  *status = host;
+  return ROT_OK;
+}
+
+int rot_state_export(const rot_plan* plan, const void* state, int32_t item, int32_t which,
+                     float* dst, void* stream) {
+  if (!plan || !state || !dst || item < 0 || item >= plan->count) return ROT_EINVAL;
+  const ItemLayout& L = plan->items[item];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (which) {
+    case ROT_WHICH_M:
+      return launch_combine(F(state, L.m_hi), F(state, L.m_lo), L.ldn, dst, L.n, L.m, L.n, s);
+    case ROT_WHICH_V2:
+      return launch_combine(F(state, L.v), nullptr, L.ldn, dst, L.n, L.m, L.n, s);
+    case ROT_WHICH_U:
+      return launch_combine(F(state, L.u_hi), F(state, L.u_lo), L.ldm, dst, L.m, L.m, L.m, s);
+    case ROT_WHICH_V:
+      return launch_combine(F(state, L.vb_hi), F(state, L.vb_lo), L.ldn, dst, L.n, L.n, L.n, s);
+    default:
+      return ROT_EINVAL;
+  }
+}
+
+int rot_state_ranks(const rot_plan* plan, const void* state, int32_t item, int32_t* rank_u,
+                    int32_t* rank_v, void* stream) {
+  if (!plan || !state || !rank_u || !rank_v || item < 0 || item >= plan->count) return ROT_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t r[2];
+  const char* src = static_cast<const char*>(state) + plan->ranks_off + 8ull * item;
+  if (cudaMemcpyAsync(r, src, sizeof(r), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return ROT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ROT_ECUDA;
+  *rank_u = r[0];
+  *rank_v = r[1];
+  return ROT_OK;
+}
+
+const char* rot_strerror(int code) {
+  switch (code) {
+    case ROT_OK: return "ok";
+    case ROT_EINVAL: return "invalid argument";
+    case ROT_ENOMEM: return "host allocation failed";
+    case ROT_ECUDA: return "CUDA error";
+    case ROT_ETIMEOUT: return "device-side wait timed out";
+    case ROT_ENONFINITE: return "non-finite value";
+    case ROT_ENOTSUP: return "device is not sm_103 or feature not built";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,144 @@
+// Internal declarations shared by the CUDA translation units of librot.
+// Not part of the public ABI (include/rot.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "rot.h"
+
+namespace rot {
+
+// ---------------------------------------------------------------------------
+// Layout helpers
+// ---------------------------------------------------------------------------
+
+// Leading dimensions of every buffer the library owns are padded to 32 floats
+// (128 bytes): rows start 128-byte aligned, which tensor-map (TMA) loads need.
+constexpr int kLdAlign = 32;
+inline int64_t pad_ld(int64_t x) { return (x + kLdAlign - 1) / kLdAlign * kLdAlign; }
+inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+// A float32 matrix stored as an exact split x = hi + lo, hi = x rounded to
+// TF32 (10 explicit mantissa bits), lo = x - hi.  Tensor-core operands are
+// always held in this form; the float32 value is hi + lo.
+struct Split {
+  float* hi;
+  float* lo;
+};
+
+// ---------------------------------------------------------------------------
+// Grouped GEMM: C[M x N] = A[M x K] * B^T, with A (M x K) and B (N x K) both
+// row-major with K contiguous ("K-major"), given as splits.
+// ---------------------------------------------------------------------------
+
+enum GemmEpi : int {
+  kEpiStoreSplit = 0,   // C (row-major, ldc) <- split(acc)
+  kEpiStoreSplitT = 1,  // C^T (row-major N x M, ldc) <- split(acc)
+  kEpiStoreF32 = 2,     // C (row-major) <- acc, float32 into c.hi
+  kEpiStoreF32T = 3,    // C^T <- acc, float32 into c.hi
+  kEpiApply = 4,        // C (row-major, float32 in c.hi) -= alpha * acc
+};
+
+struct GemmProblem {
+  int M, N, K;
+  const float* a_hi;
+  const float* a_lo;
+  int lda;
+  const float* b_hi;
+  const float* b_lo;
+  int ldb;
+  float* c_hi;
+  float* c_lo;
+  int ldc;
+  int epi;
+  float alpha;
+};
+
+// Runs every problem of `probs` (any count; launched in chunks).  precision is
+// ROT_PREC_TF32 or ROT_PREC_3XTF32.  status: device status word (may be
+// nullptr) set to ROT_ETIMEOUT if a bounded wait gives up.
+int gemm_grouped(const std::vector<GemmProblem>& probs, int precision, int* status,
+                 cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Element-wise kernels (one entry per matrix)
+// ---------------------------------------------------------------------------
+
+struct MomentumSeg {
+  const float* g;  // caller's gradient, row-major, ld = cols
+  float* m_hi;     // state momentum split, ld = ldm
+  float* m_lo;
+  float* g_hi;     // workspace gradient split, ld = ldm
+  float* g_lo;
+  int rows, cols, ldm;
+};
+int launch_momentum(const std::vector<MomentumSeg>& segs, float beta1, cudaStream_t stream);
+
+struct AdamSeg {
+  const float* gt;  // G~ float32, ld
+  const float* mt;  // M~ float32, ld
+  float* v;         // state second moment, ld
+  float* d_hi;      // D split out, ld
+  float* d_lo;
+  int rows, cols, ld;
+};
+int launch_adam(const std::vector<AdamSeg>& segs, float beta2, float eps, cudaStream_t stream);
+
+// dst (cols x rows, ld_dst) = src^T, where src (rows x cols, ld_src) is a split;
+// dst is written as a split.  src_is_split = 0 reads float32 from src.hi.
+struct TransposeSeg {
+  const float* s_hi;
+  const float* s_lo;
+  int ld_src;
+  float* d_hi;
+  float* d_lo;
+  int ld_dst;
+  int rows, cols;
+  int src_is_split;
+  int dst_is_split;
+};
+int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream);
+
+// Fill a p x p split with the identity (lo = 0), or a rows x cols split with 0.
+struct FillSeg {
+  float* hi;
+  float* lo;
+  int rows, cols, ld;
+  int identity;
+};
+int launch_fill(const std::vector<FillSeg>& segs, cudaStream_t stream);
+
+// dst (rows x cols, ld_dst, float32) = hi + lo (or hi alone when lo == nullptr).
+int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,
+                   int rows, int cols, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Batched blocked Householder QR+ (Q factor only)
+// ---------------------------------------------------------------------------
+
+constexpr int kQrPanel = 32;  // panel width b
+
+struct QrProblem {
+  float* at;    // p x ld: row j holds column j of A; overwritten by reflectors
+  float* qt;    // p x ld: receives Q^T (row j = column j of Q), float32
+  float* tf;    // ceil(rmax/b) * b * b: per-panel triangular factors
+  float* beta;  // rmax: R diagonal before the sign fix
+  int* ctrl;    // [0] rank, [1] stopped flag, [2..] per-panel active counts
+  float* tau;   // numerical-rank threshold
+  int p, ld, rmax;
+  // outputs (state): U (row-major) and U^T as splits, ld_out; and the rank.
+  Split u;
+  Split ut;
+  int ld_out;
+  int* rank_out;
+};
+int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status,
+               cudaStream_t stream);
+
+// Bytes of QR scratch (tf, beta, ctrl, tau) for one problem, 256-aligned.
+uint64_t qr_aux_bytes(int p, int rmax);
+
+}  // namespace rot

@@ -1,0 +1,103 @@
+"""CPU checks of the C-ABI library: it loads, exports every declared symbol,
+and its host planner matches the oracle's plan bit for bit."""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from matrix_optimizer_step_rot_gb300 import binding as B
+from matrix_optimizer_step_rot_gb300 import build, inputs
+from oracle import rot_oracle as orc
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    build.build()
+    B.lib()
+
+
+def test_exports_every_declared_symbol():
+    names = B.header_symbols()
+    assert len(names) >= 12
+    L = B.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+@pytest.mark.parametrize("name", inputs.WORKLOADS)
+def test_plan_bit_exact_against_oracle(name):
+    wl = inputs.workload(name)
+    p = B.Plan(wl.shapes, wl.c_max)
+    o = orc.plan(wl.shapes, wl.c_max)
+    assert p.groups() == o.groups
+    assert p.owners() == o.owners
+    for g in range(len(o.groups)):
+        assert p.group_totals(g) == (o.group_bytes[g], o.group_cost[g])
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_plan_fuzz_against_oracle(seed):
+    r = np.random.default_rng(1000 + seed)
+    count = int(r.integers(0, 60))
+    shapes = [(int(r.integers(1, 300)), int(r.integers(1, 300))) for _ in range(count)]
+    if seed % 5 == 0:  # many ties
+        shapes = [shapes[j % 3] for j in range(count)] if count >= 3 else shapes
+    ranks = int(r.integers(1, 5))
+    c_max = int(r.integers(1, 400000))
+    p = B.Plan(shapes, c_max, ranks=ranks)
+    o = orc.plan(shapes, c_max, ranks=ranks)
+    assert p.groups() == o.groups and p.owners() == o.owners
+
+
+def test_large_dims_cost_is_exact():
+    shapes = [(65536, 65536), (65536, 1), (1, 65536), (12288, 4096)]
+    p = B.Plan(shapes, 1 << 40)
+    o = orc.plan(shapes, 1 << 40)
+    assert p.groups() == o.groups and p.group_totals(0) == (o.group_bytes[0], o.group_cost[0])
+
+
+def test_argument_errors():
+    L = B.lib()
+    h = ctypes.c_void_p()
+    good = (B.rot_shape * 1)(B.rot_shape(4, 4))
+    assert L.rot_plan_create(good, 1, 0, ctypes.byref(h)) == B.ROT_EINVAL       # c_max = 0
+    assert L.rot_plan_create(good, -1, 10, ctypes.byref(h)) == B.ROT_EINVAL
+    assert L.rot_plan_create(None, 1, 10, ctypes.byref(h)) == B.ROT_EINVAL
+    assert L.rot_plan_create(good, 1, 10, None) == B.ROT_EINVAL
+    for bad in [(0, 4), (4, 0), (-3, 4), (65537, 2)]:
+        arr = (B.rot_shape * 1)(B.rot_shape(*bad))
+        assert L.rot_plan_create(arr, 1, 10, ctypes.byref(h)) == B.ROT_EINVAL
+        assert h.value is None
+    assert L.rot_plan_create_ex(good, 1, 10, 0, ctypes.byref(h)) == B.ROT_EINVAL
+    n = ctypes.c_int32()
+    assert L.rot_plan_groups(None, ctypes.byref(n)) == B.ROT_EINVAL
+    p = B.Plan([(4, 4)], 10)
+    assert L.rot_plan_group(p.handle, 5, None, None, None, None) == B.ROT_EINVAL
+    assert L.rot_plan_group(p.handle, -1, None, None, None, None) == B.ROT_EINVAL
+    # the step validates its arguments before touching the device
+    W = (ctypes.c_void_p * 1)(ctypes.c_void_p(256))
+    assert L.rot_step(p.handle, W, W, ctypes.c_void_p(256), ctypes.c_void_p(512), 0.9, 0.999,
+                      1e-8, 1e-3, 0, 2, 1e-3, None) == B.ROT_EINVAL          # precision
+    assert L.rot_step(p.handle, W, W, ctypes.c_void_p(256), ctypes.c_void_p(512), 0.9, 0.999,
+                      1e-8, 1e-3, 0, 3, 0.0, None) == B.ROT_EINVAL           # rank_rtol
+    assert L.rot_step(p.handle, W, W, ctypes.c_void_p(100), ctypes.c_void_p(512), 0.9, 0.999,
+                      1e-8, 1e-3, 0, 3, 1e-3, None) == B.ROT_EINVAL          # alignment
+    assert L.rot_step(p.handle, None, W, ctypes.c_void_p(256), ctypes.c_void_p(512), 0.9,
+                      0.999, 1e-8, 1e-3, 0, 3, 1e-3, None) == B.ROT_EINVAL
+    assert L.rot_state_export(p.handle, ctypes.c_void_p(256), 1, 0, ctypes.c_void_p(256),
+                              None) == B.ROT_EINVAL
+    assert L.rot_state_export(p.handle, ctypes.c_void_p(256), 0, 7, ctypes.c_void_p(256),
+                              None) == B.ROT_EINVAL
+    assert B.strerror(B.ROT_EINVAL) == "invalid argument"
+
+
+def test_empty_plan_and_state_sizes():
+    p = B.Plan([], 100)
+    assert p.groups() == []
+    wl = inputs.workload("tiny")
+    p = B.Plan(wl.shapes, wl.c_max)
+    sb, wb = p.state_bytes()
+    # state: M split, v, U, U^T, V, V^T splits per matrix (padded rows)
+    need = sum(4 * (3 * m * n + 4 * m * m + 4 * n * n) for m, n in wl.shapes)
+    assert sb >= need and sb % 256 == 0 and wb > 0

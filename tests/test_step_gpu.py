@@ -1,0 +1,97 @@
+"""GPU parity of rot_step against the fp64 oracle (tiny and ragged-small
+workloads), through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+from matrix_optimizer_step_rot_gb300 import binding as B
+from matrix_optimizer_step_rot_gb300 import build, inputs
+from matrix_optimizer_step_rot_gb300.optimizer import RotatedAdam
+from oracle import rot_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+TOL_W = {B.ROT_PREC_3XTF32: 1e-4, B.ROT_PREC_TF32: 2e-3}
+TOL_ORTH = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    build.build()
+    B.lib()
+
+
+def run_gpu(wl, precision, steps=None, items=None):
+    h = wl.hyper
+    opt = RotatedAdam(wl.shapes, wl.c_max, "cuda", h.beta1, h.beta2, h.eps, h.lr, h.rank_rtol,
+                      precision)
+    W = [torch.from_numpy(wl.w0(i)).cuda() for i in range(wl.count)]
+    for t in range(1, (steps or wl.steps) + 1):
+        G = [torch.from_numpy(wl.grad(i, t)).cuda() for i in range(wl.count)]
+        opt.step(W, G, wl.refresh(t))
+    torch.cuda.synchronize()
+    assert opt.status() == B.ROT_OK
+    return W, opt
+
+
+def rel(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def orth(Q):
+    Q = Q.astype(np.float64)
+    return float(np.linalg.norm(Q.T @ Q - np.eye(Q.shape[1])))
+
+
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32])
+def test_tiny_parity(precision):
+    wl = inputs.workload("tiny")
+    W, opt = run_gpu(wl, precision)
+    ref = orc.run(wl)
+    for i in range(wl.count):
+        Wo, st = ref[i]
+        e = rel(W[i].cpu().numpy().astype(np.float64), Wo)
+        assert e <= TOL_W[precision], (i, e)
+        U = opt.export(i, B.ROT_WHICH_U).cpu().numpy()
+        V = opt.export(i, B.ROT_WHICH_V).cpu().numpy()
+        assert orth(U) <= TOL_ORTH and orth(V) <= TOL_ORTH
+        assert opt.ranks(i) == (st.rank_u, st.rank_v)
+        if precision == B.ROT_PREC_3XTF32:
+            M = opt.export(i, B.ROT_WHICH_M).cpu().numpy()
+            assert rel(M, st.M) <= 1e-6
+            np.testing.assert_allclose(U, st.U, atol=1e-4)
+            np.testing.assert_allclose(V, st.V, atol=1e-4)
+
+
+def test_plain_adam_steps_match_closed_form():
+    """Before the first refresh (U = V = I) the GPU step is plain Adam."""
+    wl = inputs.workload("tiny")
+    W, opt = run_gpu(wl, B.ROT_PREC_3XTF32, steps=3)
+    h = wl.hyper
+    for i in range(wl.count):
+        w = wl.w0(i).astype(np.float64)
+        m = np.zeros_like(w)
+        v = np.zeros_like(w)
+        for t in range(1, 4):
+            g = wl.grad(i, t).astype(np.float64)
+            m = h.beta1 * m + (1 - h.beta1) * g
+            v = h.beta2 * v + (1 - h.beta2) * g * g
+            w = w - h.lr * m / (np.sqrt(v) + h.eps)
+        assert rel(W[i].cpu().numpy().astype(np.float64), w) <= 1e-6
+
+
+def test_ragged_small_parity():
+    """Shapes that are not multiples of the tile sizes, several groups."""
+    shapes = ((100, 36), (36, 100), (97, 97), (1, 40), (40, 1), (130, 70), (33, 65))
+    wl = inputs.Workload("ragged_small", shapes, tuple(map(str, range(len(shapes)))), 0.02,
+                         1e-3, "t3", 6, 3, 40000, 11)
+    W, opt = run_gpu(wl, B.ROT_PREC_3XTF32)
+    ref = orc.run(wl)
+    for i in range(wl.count):
+        Wo, st = ref[i]
+        e = rel(W[i].cpu().numpy().astype(np.float64), Wo)
+        assert e <= TOL_W[B.ROT_PREC_3XTF32], (i, shapes[i], e)
+        assert opt.ranks(i) == (st.rank_u, st.rank_v), (i, shapes[i])
