@@ -151,6 +151,13 @@ int rot_state_export(const rot_plan* plan, const void* state, int32_t item, int3
 int rot_state_ranks(const rot_plan* plan, const void* state, int32_t item, int32_t* rank_u,
                     int32_t* rank_v, void* stream);
 
+/* Set the upper bound, in nanoseconds, on every device-side wait of later
+ * launches (default 2 000 000 000 = 2 s); returns the previous bound.  A wait
+ * that reaches it abandons its kernel's remaining work, and rot_status()
+ * then reports ROT_ETIMEOUT.  Host-side setting, not thread-safe against
+ * concurrent rot_step calls. */
+uint64_t rot_set_wait_timeout_ns(uint64_t ns);
+
 /* Static description of an error code. */
 const char* rot_strerror(int code);
 

@@ -1,0 +1,37 @@
+/*
+ * rot_testing.h - test entry points of librot: run one internal kernel on
+ * its own so that it can be checked in isolation.  Same conventions as
+ * rot.h (return codes, caller-owned device memory, asynchronous on `stream`).
+ */
+#ifndef ROT_TESTING_H_
+#define ROT_TESTING_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* C = A * B^T on the tensor-core grouped GEMM used by rot_step, for one
+ * problem.  A: M x K, B: N x K, both float32 row-major device buffers with
+ * leading dimensions lda, ldb.  The operands are first split into TF32
+ * hi/lo pairs inside `work` (work_bytes >= rot_test_gemm_work_bytes(M, N,
+ * K)).  epi selects the output: 0 C = split(A B^T) into C (hi) and C + M*ldc
+ * (lo); 1 the same for C^T (N x M, ldc >= M); 2 C = A B^T (float32); 3 C^T
+ * = (A B^T)^T; 4 C -= alpha A B^T.  precision: ROT_PREC_TF32 or
+ * ROT_PREC_3XTF32.  status: device int that receives ROT_ETIMEOUT if a
+ * device-side wait gives up (may be NULL).
+ * Errors: ROT_EINVAL (sizes < 1, null pointers, work too small), ROT_ECUDA. */
+int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
+                  int32_t ldb, float* C, int32_t ldc, int32_t epi, float alpha,
+                  int32_t precision, void* work, uint64_t work_bytes, int32_t* status,
+                  void* stream);
+
+/* Workspace bytes rot_test_gemm needs for these sizes. */
+uint64_t rot_test_gemm_work_bytes(int32_t M, int32_t N, int32_t K);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROT_TESTING_H_ */

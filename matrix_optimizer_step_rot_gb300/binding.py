@@ -15,7 +15,8 @@ from typing import List, Optional, Sequence, Tuple
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "librot.so")
-HEADER = os.path.join(os.path.dirname(PKG), "include", "rot.h")
+INCLUDE = os.path.join(os.path.dirname(PKG), "include")
+HEADERS = [os.path.join(INCLUDE, "rot.h"), os.path.join(INCLUDE, "rot_testing.h")]
 
 ROT_OK = 0
 ROT_EINVAL = -1
@@ -62,6 +63,10 @@ _SIGS = {
     "rot_state_export": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp]),
     "rot_state_ranks": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp]),
     "rot_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "rot_set_wait_timeout_ns": (_u64, [_u64]),
+    "rot_test_gemm": (_i32, [_i32, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _i32,
+                             _vp, _u64, _vp, _vp]),
+    "rot_test_gemm_work_bytes": (_u64, [_i32, _i32, _i32]),
 }
 
 
@@ -82,10 +87,12 @@ def lib() -> ctypes.CDLL:
 
 
 def header_symbols() -> List[str]:
-    """Names of the functions include/rot.h declares."""
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rot_[a-z0-9_]+)\s*\(", text)))
+    """Names of the functions the headers under include/ declare."""
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(rot_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def strerror(code: int) -> str:
@@ -149,6 +156,21 @@ class Plan:
         _check(lib().rot_state_bytes(self.handle, ctypes.byref(s), ctypes.byref(w)),
                "rot_state_bytes")
         return s.value, w.value
+
+
+def rot_set_wait_timeout_ns(ns: int) -> int:
+    return int(lib().rot_set_wait_timeout_ns(int(ns)))
+
+
+def rot_test_gemm(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, epi, alpha, precision, work_ptr,
+                  work_bytes, status_ptr, stream) -> None:
+    _check(lib().rot_test_gemm(M, N, K, _vp(a_ptr), lda, _vp(b_ptr), ldb, _vp(c_ptr), ldc, epi,
+                               alpha, precision, _vp(work_ptr), work_bytes, _vp(status_ptr),
+                               _vp(stream)), "rot_test_gemm")
+
+
+def rot_test_gemm_work_bytes(M, N, K) -> int:
+    return int(lib().rot_test_gemm_work_bytes(M, N, K))
 
 
 def rot_state_init(plan: Plan, state_ptr: int, stream: int) -> None:

@@ -141,6 +141,20 @@ __global__ void fill_kernel(const __grid_constant__ SegBatch<FillSeg> b) {
   }
 }
 
+__global__ void split_kernel(const __grid_constant__ SegBatch<SplitSeg> b) {
+  const SplitSeg& s = b.seg[blockIdx.y];
+  const int64_t total = (int64_t)s.rows * s.cols;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
+    float h, l;
+    split_tf32(s.src[(int64_t)r * s.ld_src + c], h, l);
+    const int64_t o = (int64_t)r * s.ld_dst + c;
+    s.hi[o] = h;
+    s.lo[o] = l;
+  }
+}
+
 __global__ void combine_kernel(const float* hi, const float* lo, int ld_src, float* dst,
                                int ld_dst, int rows, int cols) {
   const int64_t total = (int64_t)rows * cols;
@@ -183,6 +197,10 @@ int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream)
 
 int launch_fill(const std::vector<FillSeg>& segs, cudaStream_t stream) {
   return launch_segs(segs, fill_kernel, stream);
+}
+
+int launch_split(const std::vector<SplitSeg>& segs, cudaStream_t stream) {
+  return launch_segs(segs, split_kernel, stream);
 }
 
 int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,

@@ -1,0 +1,444 @@
+// Grouped GEMM on the sm_103a tensor cores (tcgen05, TMEM accumulators,
+// TMA-fed shared-memory ring), C = A * B^T with A (M x K) and B (N x K) both
+// K-major float32 matrices held as TF32 splits.
+//
+// ROT_PREC_3XTF32 issues three kind::tf32 MMAs per K step (hi*lo, lo*hi,
+// hi*hi) and recovers about float32 accuracy; ROT_PREC_TF32 issues one
+// (hi*hi).  Accumulation is float32 in TMEM either way.
+//
+// Structure: a persistent kernel, one CTA per SM, walks the flattened tile
+// list of every problem in the launch.  Per CTA:
+//   warp 0     one thread issues TMA loads into a STAGES-deep ring
+//   warp 1     allocates TMEM; one thread issues the MMAs of a 128 x BN tile
+//              into one of two TMEM accumulators
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (each warp its 32-lane
+//              quarter), apply the output mode, store to global memory
+// mbarriers link the roles; every wait is bounded in time, and a timeout
+// raises a CTA-wide abort flag, drains in-flight copies and MMAs, frees TMEM
+// and reports ROT_ETIMEOUT through the status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "rot_internal.h"
+#include "split.cuh"
+#include "tc_ptx.cuh"
+
+namespace rot {
+
+uint64_t g_wait_limit_ns = 2000000000ull;  // 2 s; see rot_set_wait_timeout_ns
+
+namespace {
+
+constexpr int BM = 128;  // UMMA M (cta_group::1): one TMEM lane per row
+constexpr int BK = 32;   // 32 float32 = 128 bytes = one swizzle-atom row
+constexpr int kMaxP = 40;
+constexpr int kThreads = 192;
+
+struct TcProblem {
+  CUtensorMap a_hi, a_lo, b_hi, b_lo;
+  int M, N, K;
+  int tiles_n;
+  int tile_start;
+  int epi;
+  int ldc;
+  float alpha;
+  float* c_hi;
+  float* c_lo;
+};
+
+struct TcBatch {
+  TcProblem p[kMaxP];
+  int count;
+  int total_tiles;
+  int* status;
+  unsigned long long limit_ns;
+};
+
+template <int BN, int STAGES, bool SPLIT3>
+struct Cfg {
+  static constexpr int kABytes = BM * BK * 4;
+  static constexpr int kBBytes = BN * BK * 4;
+  static constexpr int kStageBytes = (kABytes + kBBytes) * (SPLIT3 ? 2 : 1);
+  static constexpr int kSmem = STAGES * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kTmemCols = 2 * BN;
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of 2");
+};
+
+__device__ __forceinline__ void decode(const TcBatch& b, int tile, int& pi, int& m0, int& n0) {
+  pi = 0;
+  while (pi + 1 < b.count && tile >= b.p[pi + 1].tile_start) ++pi;
+  const int local = tile - b.p[pi].tile_start;
+  m0 = (local / b.p[pi].tiles_n) * BM;
+  n0 = (local % b.p[pi].tiles_n);
+}
+
+// Waits without regard to the abort flag (used only to drain at exit).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return;
+    if ((it & 63u) == 0u && (ptx::globaltimer_ns() - t0 > limit_ns || it > (1u << 30))) return;
+  }
+}
+
+__device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col0,
+                                            const uint32_t (&r)[32]) {
+  const int M = P.M, N = P.N;
+  const int ncol = min(32, N - col0);
+  switch (P.epi) {
+    case kEpiStoreSplitT:
+    case kEpiStoreF32T: {
+      // column j of C is row j of C^T: the warp's 32 lanes (32 consecutive
+      // rows i) write 32 consecutive floats
+      if (row >= M) return;
+      const bool split = P.epi == kEpiStoreSplitT;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        if (t < ncol) {
+          const float v = __uint_as_float(r[t]);
+          const int64_t o = (int64_t)(col0 + t) * P.ldc + row;
+          if (split) {
+            float h, l;
+            split_tf32(v, h, l);
+            P.c_hi[o] = h;
+            P.c_lo[o] = l;
+          } else {
+            P.c_hi[o] = v;
+          }
+        }
+      }
+      return;
+    }
+    case kEpiStoreSplit:
+    case kEpiStoreF32: {
+      if (row >= M) return;
+      const bool split = P.epi == kEpiStoreSplit;
+      float* hi = P.c_hi + (int64_t)row * P.ldc + col0;
+      float* lo = split ? P.c_lo + (int64_t)row * P.ldc + col0 : nullptr;
+      if (ncol == 32 && (P.ldc & 3) == 0 && ((reinterpret_cast<uintptr_t>(hi) & 15) == 0) &&
+          (!split || (reinterpret_cast<uintptr_t>(lo) & 15) == 0)) {
+#pragma unroll
+        for (int t = 0; t < 32; t += 4) {
+          float4 h4, l4;
+          float* hp = &h4.x;
+          float* lp = &l4.x;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float v = __uint_as_float(r[t + u]);
+            if (split) {
+              split_tf32(v, hp[u], lp[u]);
+            } else {
+              hp[u] = v;
+            }
+          }
+          *reinterpret_cast<float4*>(hi + t) = h4;
+          if (split) *reinterpret_cast<float4*>(lo + t) = l4;
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          if (t < ncol) {
+            const float v = __uint_as_float(r[t]);
+            if (split) {
+              float h, l;
+              split_tf32(v, h, l);
+              hi[t] = h;
+              lo[t] = l;
+            } else {
+              hi[t] = v;
+            }
+          }
+        }
+      }
+      return;
+    }
+    case kEpiApply: {
+      if (row >= M) return;
+      float* w = P.c_hi + (int64_t)row * P.ldc + col0;
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if (t < ncol) w[t] = w[t] - P.alpha * __uint_as_float(r[t]);
+      return;
+    }
+  }
+}
+
+template <int BN, int STAGES, bool SPLIT3>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcBatch b) {
+  using C = Cfg<BN, STAGES, SPLIT3>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t limit = b.limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 4);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    for (int i = 0; i < b.count; ++i) {
+      ptx::tma_prefetch_desc(&b.p[i].a_hi);
+      ptx::tma_prefetch_desc(&b.p[i].b_hi);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed_mask = 0, armed_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
+      int pi, m0, nt;
+      decode(b, tile, pi, m0, nt);
+      const TcProblem& P = b.p[pi];
+      const int n0 = nt * BN;
+      const int kblocks = (P.K + BK - 1) / BK;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + stage * C::kStageBytes;
+        ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        armed_mask |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        const int x = kb * BK;
+        ptx::tma_load_2d(st, &P.a_hi, &full[stage], x, m0);
+        if (SPLIT3) {
+          ptx::tma_load_2d(st + C::kABytes, &P.a_lo, &full[stage], x, m0);
+          ptx::tma_load_2d(st + 2 * C::kABytes, &P.b_hi, &full[stage], x, n0);
+          ptx::tma_load_2d(st + 2 * C::kABytes + C::kBBytes, &P.b_lo, &full[stage], x, n0);
+        } else {
+          ptx::tma_load_2d(st + C::kABytes, &P.b_hi, &full[stage], x, n0);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // wait for this thread's copies still in flight before the CTA exits
+    for (int s = 0; s < STAGES; ++s)
+      if (armed_mask & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u, limit);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issue
+    constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
+      int pi, m0, nt;
+      decode(b, tile, pi, m0, nt);
+      const int kblocks = (b.p[pi].K + BK - 1) / BK;
+      if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, limit)) break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, limit)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t s = ptx::smem_u32(smem + stage * C::kStageBytes);
+        const uint64_t ah = ptx::sw128_kmajor_desc(s);
+        const uint64_t al = ptx::sw128_kmajor_desc(s + C::kABytes);
+        const uint64_t bh = ptx::sw128_kmajor_desc(s + (SPLIT3 ? 2 : 1) * C::kABytes);
+        const uint64_t bl = ptx::sw128_kmajor_desc(s + 2 * C::kABytes + C::kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);  // 8 tf32 = 32 bytes
+          const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+          if (SPLIT3) {
+            ptx::umma_tf32(d_tmem, ah + off, bl + off, idesc, accum);
+            ptx::umma_tf32(d_tmem, al + off, bh + off, idesc, 1u);
+            ptx::umma_tf32(d_tmem, ah + off, bh + off, idesc, 1u);
+          } else {
+            ptx::umma_tf32(d_tmem, ah + off, bh + off, idesc, accum);
+          }
+        }
+        ptx::umma_commit(&empty[stage]);  // frees the stage once these MMAs finish
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      ptx::umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    // every MMA this thread issued has completed before TMEM is freed
+    ptx::umma_commit(drain);
+    mbar_drain(drain, 0, limit);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < b.total_tiles; tile += gridDim.x) {
+      int pi, m0, nt;
+      decode(b, tile, pi, m0, nt);
+      const TcProblem& P = b.p[pi];
+      const int n0 = nt * BN;
+      if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, limit)) break;
+      ptx::tc_fence_after();
+      const int row = m0 + quarter * 32 + lane;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      for (int c = 0; c < BN && n0 + c < P.N; c += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c), r);
+        ptx::tmem_wait_ld();
+        store_chunk(P, row, n0 + c, r);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag && b.status) atomicExch(b.status, ROT_ETIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  if (g_encode) return ROT_OK;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return ROT_ECUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return ROT_OK;
+}
+
+// Row-major rows x K float32 matrix (leading dimension ld), boxes of
+// box_rows x 32 with 128-byte swizzle; out-of-range elements read as 0.
+int encode(CUtensorMap* map, const float* base, int rows, int K, int ld, int box_rows) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld & 3)) return ROT_EINVAL;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ROT_OK : ROT_EINVAL;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int BN, int STAGES, bool SPLIT3>
+int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stream) {
+  using C = Cfg<BN, STAGES, SPLIT3>;
+  auto kernel = gemm_tc_kernel<BN, STAGES, SPLIT3>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+        cudaSuccess)
+      return ROT_ECUDA;
+    attr = true;
+  }
+  if (get_encoder() != ROT_OK) return ROT_ECUDA;
+  thread_local static TcBatch b;  // ~23 KB parameter block: keep off the stack
+  size_t i = 0;
+  while (i < probs.size()) {
+    std::memset(&b, 0, sizeof(b));
+    int total = 0;
+    while (i < probs.size() && b.count < kMaxP) {
+      const GemmProblem& G = probs[i++];
+      if (G.M <= 0 || G.N <= 0) continue;
+      if (G.K <= 0) return ROT_EINVAL;
+      TcProblem& P = b.p[b.count];
+      if (encode(&P.a_hi, G.a_hi, G.M, G.K, G.lda, BM) != ROT_OK ||
+          encode(&P.b_hi, G.b_hi, G.N, G.K, G.ldb, BN) != ROT_OK)
+        return ROT_EINVAL;
+      if (SPLIT3 && (encode(&P.a_lo, G.a_lo, G.M, G.K, G.lda, BM) != ROT_OK ||
+                     encode(&P.b_lo, G.b_lo, G.N, G.K, G.ldb, BN) != ROT_OK))
+        return ROT_EINVAL;
+      P.M = G.M;
+      P.N = G.N;
+      P.K = G.K;
+      P.tiles_n = (G.N + BN - 1) / BN;
+      P.tile_start = total;
+      P.epi = G.epi;
+      P.ldc = G.ldc;
+      P.alpha = G.alpha;
+      P.c_hi = G.c_hi;
+      P.c_lo = G.c_lo;
+      total += ((G.M + BM - 1) / BM) * P.tiles_n;
+      ++b.count;
+    }
+    if (total == 0) continue;
+    b.total_tiles = total;
+    b.status = status;
+    b.limit_ns = g_wait_limit_ns;
+    const int grid = std::min(total, num_sms());
+    kernel<<<grid, kThreads, C::kSmem, stream>>>(b);
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+  }
+  return ROT_OK;
+}
+
+}  // namespace
+
+int gemm_tc(const std::vector<GemmProblem>& probs, int precision, int* status,
+            cudaStream_t stream) {
+  if (precision == ROT_PREC_3XTF32) return launch<256, 2, true>(probs, status, stream);
+  return launch<256, 4, false>(probs, status, stream);
+}
+
+}  // namespace rot

@@ -18,12 +18,12 @@
 
 namespace rot {
 
-int gemm_simt(const std::vector<GemmProblem>& probs, int precision, cudaStream_t stream);
+int gemm_tc(const std::vector<GemmProblem>& probs, int precision, int* status,
+            cudaStream_t stream);
 
 int gemm_grouped(const std::vector<GemmProblem>& probs, int precision, int* status,
                  cudaStream_t stream) {
-  (void)status;
-  return gemm_simt(probs, precision, stream);
+  return gemm_tc(probs, precision, status, stream);
 }
 
 namespace {

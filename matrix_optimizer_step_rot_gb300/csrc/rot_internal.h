@@ -57,6 +57,9 @@ struct GemmProblem {
   float alpha;
 };
 
+// Upper bound on every device-side wait, in nanoseconds.
+extern uint64_t g_wait_limit_ns;
+
 // Runs every problem of `probs` (any count; launched in chunks).  precision is
 // ROT_PREC_TF32 or ROT_PREC_3XTF32.  status: device status word (may be
 // nullptr) set to ROT_ETIMEOUT if a bounded wait gives up.
@@ -110,6 +113,17 @@ struct FillSeg {
   int identity;
 };
 int launch_fill(const std::vector<FillSeg>& segs, cudaStream_t stream);
+
+// hi/lo (rows x cols, ld_dst) = TF32 split of src (float32, ld_src).
+struct SplitSeg {
+  const float* src;
+  int ld_src;
+  float* hi;
+  float* lo;
+  int ld_dst;
+  int rows, cols;
+};
+int launch_split(const std::vector<SplitSeg>& segs, cudaStream_t stream);
 
 // dst (rows x cols, ld_dst, float32) = hi + lo (or hi alone when lo == nullptr).
 int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,

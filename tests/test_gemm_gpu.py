@@ -1,0 +1,84 @@
+"""The tensor-core grouped GEMM in isolation (rot_test_gemm) against a float64
+matmul, for every output mode, ragged sizes and both precisions."""
+
+import pytest
+import torch
+
+from matrix_optimizer_step_rot_gb300 import binding as B
+from matrix_optimizer_step_rot_gb300 import build
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(128, 256, 32), (64, 64, 64), (300, 520, 100), (1, 40, 7), (33, 1, 65),
+          (1000, 1000, 1000), (2048, 256, 4096), (130, 300, 2000)]
+TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3}
+
+
+def tol(precision, K):
+    """Relative Frobenius bound.  The tensor cores accumulate in float32 but
+    truncate each partial sum, an error that grows with the number of K steps
+    (about 2^-24 per step relative to the running sum); 3xTF32 is therefore
+    bounded by a K-proportional term on top of the split's own error."""
+    if precision == B.ROT_PREC_3XTF32:
+        return TOL[precision] + 2.5e-8 * K
+    return TOL[precision]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    build.build()
+    B.lib()
+
+
+def run(M, N, K, epi, precision, alpha=0.5, seed=0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    A = torch.rand(M, K, device="cuda", generator=g) * 2 - 1
+    Bm = torch.rand(N, K, device="cuda", generator=g) * 2 - 1
+    ref = A.double() @ Bm.double().T
+    transposed = epi in (1, 3)
+    rows, ldc = (N, M) if transposed else (M, N)
+    if epi in (0, 1):
+        C = torch.zeros(2 * rows * ldc, device="cuda")
+    else:
+        C = torch.rand(rows * ldc, device="cuda", generator=g)
+    C0 = C.clone()
+    wb = B.rot_test_gemm_work_bytes(M, N, K)
+    work = torch.empty(wb, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.rot_test_gemm(M, N, K, A.data_ptr(), K, Bm.data_ptr(), K, C.data_ptr(), ldc, epi, alpha,
+                    precision, work.data_ptr(), wb, status.data_ptr(),
+                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    if epi in (0, 1):
+        out = (C[:rows * ldc].double() + C[rows * ldc:].double()).view(rows, ldc)
+        # the split is exact: hi has 10 explicit mantissa bits
+        hi = C[:rows * ldc]
+        assert torch.equal(hi.view(torch.int32) & 0x1FFF, torch.zeros_like(hi, dtype=torch.int32))
+    elif epi == 4:
+        out = (C0.double() - C.double()).view(rows, ldc) / alpha
+    else:
+        out = C.double().view(rows, ldc)
+    if transposed:
+        out = out.T
+    return out, ref
+
+
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_store_f32(M, N, K, precision):
+    out, ref = run(M, N, K, 2, precision)
+    err = float((out - ref).norm() / ref.norm())
+    print(f"gemm {M}x{N}x{K} prec {precision}: rel err {err:.3e}")
+    assert err <= tol(precision, K), err
+
+
+@pytest.mark.parametrize("epi", [0, 1, 3, 4])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 100), (64, 64, 64), (1, 40, 7)])
+def test_gemm_output_modes(M, N, K, epi):
+    out, ref = run(M, N, K, epi, B.ROT_PREC_3XTF32)
+    err = (out - ref).norm() / ref.norm()
+    # the apply mode recovers the product from a difference of float32 values
+    assert err <= (1e-5 if epi == 4 else tol(B.ROT_PREC_3XTF32, K)), float(err)
