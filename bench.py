@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of the rotated-Adam matrix-optimizer step on one GB300 per rank.
+
+Workload: the Qwen3-1.7B-shaped full stack (28 blocks x 7 float32 matrices,
+1.41e9 parameters), micro-grouped with C_max = 512 MiB, basis refresh every 5
+steps (t % 5 == 0, t counting from 1 across warm-up and timed steps; the
+default 5 warm-up + 10 timed steps time t = 6..15, two refreshes in ten).
+Synthetic, seeded inputs (W ~ N(0, 0.02), G ~ N(0, 1e-3)) drawn on the device;
+two gradient sets alternate (5.6 GB each, far above the 129 MB L2).
+
+Prints one JSON line (rank 0).  `value` is matrix-steps/s over all ranks.
+--impl reference times the float64 CPU oracle instead (bounded samples).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from matrix_optimizer_step_rot_gb300 import flops as FL  # noqa: E402
+from matrix_optimizer_step_rot_gb300 import inputs  # noqa: E402
+
+METRIC = "rotated-Adam matrix-steps/s and TFLOP/s (% TF32 TC peak), Qwen3-1.7B shapes"
+UNIT = "matrix-steps/s"
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 : BF16 tensor rates
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def workload_config(wl, precision):
+    desc = {
+        "full": f"qwen3-1.7b-shaped full stack: {wl.count} fp32 matrices (28 blocks of "
+                "q 2048x2048, k/v 1024x2048, o 2048x2048, gate/up 6144x2048, down 2048x6144)",
+        "block": "one qwen3-1.7b-shaped block: 7 fp32 matrices",
+        "slice8b": "qwen3-8b-shaped slice: 4 blocks, 28 fp32 matrices",
+        "ragged": "ragged stress: 256 fp32 matrices, m, n in {64..1024}",
+        "tiny": "tiny: 4 fp32 matrices 64x64, 64x128, 128x64, 32x96",
+    }[wl.name]
+    return {
+        "workload": desc,
+        "params": sum(m * n for m, n in wl.shapes),
+        "c_max_bytes": wl.c_max,
+        "refresh_every": wl.refresh_every,
+        "precision": precision,
+        "hyper": {"beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "lr": 1e-3, "rank_rtol": 1e-3},
+        "l2": "inputs larger than L2 (5.6 GB of G per step, 129 MB L2); no flush",
+    }
+
+
+def schedule(wl, first, count):
+    return [wl.refresh(t) for t in range(first, first + count)]
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.tmp = tempfile.NamedTemporaryFile(prefix="clocks", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.close()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[4 + j] == "Active"})
+        power = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the float64 oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, steps, first_step=1, item=1):
+    """Time the oracle on one k_proj matrix (item 1 of block 0) for `steps`
+    steps on the workload's schedule; extrapolate to the whole workload by
+    analytic flops.  Returns (matrix-steps/s of the full workload, seconds,
+    description)."""
+    from oracle import rot_oracle as orc
+
+    h = wl.hyper
+    m, n = wl.shapes[item]
+    W = wl.w0(item).astype("float64")
+    st = orc.init_state(m, n)
+    grads = [wl.grad(item, t) for t in range(first_step, first_step + steps)]
+    # the sample always includes the state a refresh step needs: steps
+    # before first_step are not replayed (M, v start at zero)
+    t0 = time.perf_counter()
+    done_flops = 0.0
+    for j, t in enumerate(range(first_step, first_step + steps)):
+        r = wl.refresh(t)
+        W = orc.step(W, grads[j], st, h.beta1, h.beta2, h.eps, h.lr, r, h.rank_rtol)
+        done_flops += FL.matrix_step_flops(m, n, r)
+    secs = time.perf_counter() - t0
+    per_matrix_step = sum(FL.step_flops(wl.shapes, r) for r in schedule(wl, first_step, steps)) / (
+        wl.count * steps)
+    value = done_flops / secs / per_matrix_step
+    desc = (f"oracle (numpy float64) on one {m}x{n} matrix for {steps} steps "
+            f"(t={first_step}..{first_step + steps - 1}); extrapolated to the {wl.count}-matrix "
+            f"workload by analytic flops ({done_flops / secs / 1e9:.2f} GFLOP/s achieved)")
+    return value, secs, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from matrix_optimizer_step_rot_gb300 import binding as B
+    from matrix_optimizer_step_rot_gb300.optimizer import RotatedAdam
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = inputs.workload(args.workload)
+    h = wl.hyper
+    precision = B.ROT_PREC_3XTF32 if args.precision == "3xtf32" else B.ROT_PREC_TF32
+    opt = RotatedAdam(wl.shapes, wl.c_max, dev, h.beta1, h.beta2, h.eps, h.lr, h.rank_rtol,
+                      precision)
+    gen = torch.Generator(device=dev).manual_seed(1000 * wl.seed + rank)
+    W = [torch.randn(m, n, device=dev, generator=gen) * wl.w_std for m, n in wl.shapes]
+    Gsets = [[torch.randn(m, n, device=dev, generator=gen) * wl.g_std for m, n in wl.shapes]
+             for _ in range(2)]
+    stream = torch.cuda.current_stream(dev)
+
+    t = 0
+
+    def step(G):
+        nonlocal t
+        t += 1
+        opt.step(W, G, wl.refresh(t))
+
+    for _ in range(args.warmup):
+        step(Gsets[t % 2])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+
+    timed_sched = schedule(wl, t + 1, args.steps)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = str(local)
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    B.lib().rot_profile_reset()
+    B.lib().rot_profile_enable(1)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(Gsets[t % 2])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    B.lib().rot_profile_enable(0)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    launches = int(B.lib().rot_launch_count())
+    status = opt.status()
+    if status != B.ROT_OK:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    prof = {}
+    import ctypes
+    names = ["gemm", "elementwise", "qr_panel", "qr_apply", "qr_other"]
+    for c, nm in enumerate(names):
+        n_, tot, mx, work = ctypes.c_uint64(), ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        B.lib().rot_profile_read(c, ctypes.byref(n_), ctypes.byref(tot), ctypes.byref(mx),
+                                 ctypes.byref(work))
+        prof[nm] = {"launches": n_.value, "ms": tot.value, "max_ms": mx.value, "work": work.value}
+
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+
+    # ---- end to end through the public API with host buffers
+    g_host = [g.cpu().pin_memory() for g in Gsets[0]]
+    w_host = [w.cpu().pin_memory() for w in W]
+    g_dev = [torch.empty_like(g) for g in Gsets[0]]
+    h2d = sum(g.numel() * 4 for g in g_host)
+    d2h = sum(w.numel() * 4 for w in w_host)
+    e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(e_steps):
+        for gd, gh in zip(g_dev, g_host):
+            gd.copy_(gh, non_blocking=True)
+        step(g_dev)
+        for wh, wd in zip(w_host, W):
+            wh.copy_(wd, non_blocking=True)
+    x1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = x0.elapsed_time(x1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_sched = schedule(wl, t - e_steps + 1, e_steps)
+
+    if rank == 0:
+        peaks, peak_kind = load_peaks()
+        tf32_sust = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]) * TF32_OVER_BF16
+        tf32_burst = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]) * TF32_OVER_BF16
+        secs = ms / 1000.0
+        units = world * wl.count * args.steps
+        step_flops = sum(FL.step_flops(wl.shapes, r) for r in timed_sched)
+        tflops = world * step_flops / secs / 1e12
+        g = prof["gemm"]
+        gemm_tflops = g["work"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else None
+        ew = prof["elementwise"]
+        ew_gbs = ew["work"] / (ew["ms"] / 1000.0) / 1e9 if ew["ms"] > 0 else None
+        hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+        out = {
+            "metric": METRIC,
+            "value": units / secs,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded torch.randn on device; Qwen3-1.7B shapes, no weights)",
+            "config": workload_config(wl, args.precision),
+            "tflops": tflops,
+            "tflops_frac_of_tf32_peak": tflops / tf32_sust,
+            "refresh_steps_timed": sum(timed_sched),
+            "roofline": {
+                "bound": "tensor",
+                "kernel": "gemm_tc_kernel (tcgen05 kind::tf32, "
+                          + ("3 MMAs per K step)" if args.precision == "3xtf32" else "1 MMA per K step)"),
+                "achieved": gemm_tflops,
+                "peak": tf32_sust,
+                "unit": "TFLOP/s",
+                "frac": gemm_tflops / tf32_sust if gemm_tflops else None,
+                "traffic": None,
+                "peak_source": f"{peak_kind} bf16 sustained x {TF32_OVER_BF16:.4f} (nominal "
+                               "TF32:BF16 dense ratio)",
+                "peak_burst": tf32_burst,
+                "mma_issue_factor": 3 if args.precision == "3xtf32" else 1,
+                "share_of_step": g["ms"] / ms if ms > 0 else None,
+            },
+            "kernels": {
+                nm: {"launches": v["launches"], "ms": v["ms"],
+                     "share": v["ms"] / ms if ms > 0 else None} for nm, v in prof.items()
+            },
+            "elementwise_hbm": {"achieved_gbs": ew_gbs, "peak_gbs": hbm,
+                                "frac": ew_gbs / hbm if ew_gbs else None},
+            "e2e": {"value": world * wl.count * e_steps / (e2e_ms / 1000.0), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e_steps, "refresh_steps": sum(e2e_sched)},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            v, secs_cpu, desc = oracle_sample(wl, 5, first_step=1)
+            out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_cores(),
+                                   "kind": "oracle", "sample": desc, "seconds": secs_cpu}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = inputs.workload(args.workload)
+    from oracle import rot_oracle as orc
+
+    h = wl.hyper
+    item = 1  # k_proj of block 0
+    m, n = wl.shapes[item]
+    W = wl.w0(item).astype("float64")
+    st = orc.init_state(m, n)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        W = orc.step(W, wl.grad(item, t), st, h.beta1, h.beta2, h.eps, h.lr, wl.refresh(t),
+                     h.rank_rtol)
+    grads = [wl.grad(item, t + 1 + j) for j in range(args.steps)]
+    sched = schedule(wl, t + 1, args.steps)
+    t0 = time.perf_counter()
+    done = 0.0
+    for j in range(args.steps):
+        t += 1
+        W = orc.step(W, grads[j], st, h.beta1, h.beta2, h.eps, h.lr, sched[j], h.rank_rtol)
+        done += FL.matrix_step_flops(m, n, sched[j])
+    secs = time.perf_counter() - t0
+    per_ms = sum(FL.step_flops(wl.shapes, r) for r in sched) / (wl.count * args.steps)
+    value = done / secs / per_ms
+    desc = (f"each step: the float64 oracle on one {m}x{n} matrix of the workload "
+            f"(k_proj of block 0), extrapolated to {wl.count} matrices by analytic flops")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs * 1000.0 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": workload_config(wl, "float64 oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full", choices=list(inputs.WORKLOADS))
+    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "tf32"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

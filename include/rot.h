@@ -158,6 +158,33 @@ int rot_state_ranks(const rot_plan* plan, const void* state, int32_t item, int32
  * concurrent rot_step calls. */
 uint64_t rot_set_wait_timeout_ns(uint64_t ns);
 
+/* Instrumentation.  Every kernel launch of the library is counted; while
+ * profiling is enabled, a CUDA event pair is also recorded on the launch
+ * stream around each launch, tagged with its kernel class and algorithmic
+ * work.  Host-side state shared by all plans; thread-safe. */
+#define ROT_PROF_GEMM 0        /* tensor-core GEMM; work = 2 M N K flops per product */
+#define ROT_PROF_ELEMENTWISE 1 /* momentum, Adam, transposes, splits; work = bytes moved */
+#define ROT_PROF_QR_PANEL 2    /* QR panel factorisation; work = 0 (latency bound) */
+#define ROT_PROF_QR_APPLY 3    /* QR block-reflector updates; work = flops (32-wide panels) */
+#define ROT_PROF_QR_OTHER 4    /* QR set-up, column norms, identity, sign fix; work = 0 */
+#define ROT_PROF_CLASSES 5
+
+/* Turn event recording on (on != 0) or off.  Returns ROT_OK. */
+int rot_profile_enable(int32_t on);
+
+/* Drop every record and zero the launch counter.  Returns ROT_OK. */
+int rot_profile_reset(void);
+
+/* Kernel launches since the last reset. */
+uint64_t rot_launch_count(void);
+
+/* Summary of the records of class `cls`: number of launches, total and
+ * largest event-measured duration (ms) and summed work.  Waits for the
+ * recorded events.  Errors: ROT_EINVAL (class out of range, null outputs),
+ * ROT_ECUDA. */
+int rot_profile_read(int32_t cls, uint64_t* launches, double* total_ms, double* max_ms,
+                     double* work);
+
 /* Static description of an error code. */
 const char* rot_strerror(int code);
 

@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "profile.h"
 #include "rot_internal.h"
 #include "split.cuh"
 
@@ -27,20 +28,24 @@ inline unsigned grid_x_for(int64_t elems) {
   return (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, 4096));
 }
 
+// bytes_per_elem: algorithmic bytes each element moves (for instrumentation)
 template <class Seg, class Kernel, class... Args>
-int launch_segs(const std::vector<Seg>& segs, Kernel kernel, cudaStream_t stream,
-                Args... args) {
+int launch_segs(const std::vector<Seg>& segs, double bytes_per_elem, Kernel kernel,
+                cudaStream_t stream, Args... args) {
   for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
     SegBatch<Seg> b;
     std::memset(&b, 0, sizeof(b));
     b.count = (int)std::min<size_t>(kMaxSegs, segs.size() - base);
     int64_t most = 0;
+    double elems = 0.0;
     for (int i = 0; i < b.count; ++i) {
       b.seg[i] = segs[base + i];
       most = std::max<int64_t>(most, (int64_t)b.seg[i].rows * b.seg[i].cols);
+      elems += (double)b.seg[i].rows * b.seg[i].cols;
     }
     if (most == 0) continue;
     dim3 grid(grid_x_for(most), b.count);
+    ProfScope prof(ROT_PROF_ELEMENTWISE, elems * bytes_per_elem, stream);
     kernel<<<grid, kThreads, 0, stream>>>(b, args...);
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
   }
@@ -169,11 +174,13 @@ __global__ void combine_kernel(const float* hi, const float* lo, int ld_src, flo
 }  // namespace
 
 int launch_momentum(const std::vector<MomentumSeg>& segs, float beta1, cudaStream_t stream) {
-  return launch_segs(segs, momentum_kernel, stream, beta1);
+  // read G (4) and M's split (8); write M's split (8) and G's split (8)
+  return launch_segs(segs, 28.0, momentum_kernel, stream, beta1);
 }
 
 int launch_adam(const std::vector<AdamSeg>& segs, float beta2, float eps, cudaStream_t stream) {
-  return launch_segs(segs, adam_kernel, stream, beta2, eps);
+  // read G~, M~, v (12); write v (4) and D's split (8)
+  return launch_segs(segs, 24.0, adam_kernel, stream, beta2, eps);
 }
 
 int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream) {
@@ -182,13 +189,17 @@ int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream)
     std::memset(&b, 0, sizeof(b));
     b.count = (int)std::min<size_t>(kMaxSegs, segs.size() - base);
     int64_t most = 0;
+    double bytes = 0.0;
     for (int i = 0; i < b.count; ++i) {
       b.seg[i] = segs[base + i];
       most = std::max<int64_t>(most, (int64_t)((b.seg[i].rows + 31) / 32) *
                                          ((b.seg[i].cols + 31) / 32));
+      bytes += (double)b.seg[i].rows * b.seg[i].cols *
+               ((b.seg[i].src_is_split ? 8 : 4) + (b.seg[i].dst_is_split ? 8 : 4));
     }
     if (most == 0) continue;
     dim3 grid((unsigned)std::min<int64_t>(most, 2048), b.count);
+    ProfScope prof(ROT_PROF_ELEMENTWISE, bytes, stream);
     transpose_kernel<<<grid, 256, 0, stream>>>(b);
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
   }
@@ -196,17 +207,18 @@ int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream)
 }
 
 int launch_fill(const std::vector<FillSeg>& segs, cudaStream_t stream) {
-  return launch_segs(segs, fill_kernel, stream);
+  return launch_segs(segs, 8.0, fill_kernel, stream);
 }
 
 int launch_split(const std::vector<SplitSeg>& segs, cudaStream_t stream) {
-  return launch_segs(segs, split_kernel, stream);
+  return launch_segs(segs, 12.0, split_kernel, stream);
 }
 
 int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,
                    int rows, int cols, cudaStream_t stream) {
   const int64_t total = (int64_t)rows * cols;
   if (total == 0) return ROT_OK;
+  ProfScope prof(ROT_PROF_ELEMENTWISE, (double)total * (lo ? 12 : 8), stream);
   combine_kernel<<<grid_x_for(total), kThreads, 0, stream>>>(hi, lo, ld_src, dst, ld_dst, rows,
                                                              cols);
   return cudaGetLastError() == cudaSuccess ? ROT_OK : ROT_ECUDA;

@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "profile.h"
 #include "rot_internal.h"
 #include "split.cuh"
 #include "tc_ptx.cuh"
@@ -398,6 +399,7 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
   while (i < probs.size()) {
     std::memset(&b, 0, sizeof(b));
     int total = 0;
+    double flops = 0.0;
     while (i < probs.size() && b.count < kMaxP) {
       const GemmProblem& G = probs[i++];
       if (G.M <= 0 || G.N <= 0) continue;
@@ -420,6 +422,7 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
       P.c_hi = G.c_hi;
       P.c_lo = G.c_lo;
       total += ((G.M + BM - 1) / BM) * P.tiles_n;
+      flops += 2.0 * G.M * (double)G.N * G.K;
       ++b.count;
     }
     if (total == 0) continue;
@@ -427,7 +430,10 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
     b.status = status;
     b.limit_ns = g_wait_limit_ns;
     const int grid = std::min(total, num_sms());
-    kernel<<<grid, kThreads, C::kSmem, stream>>>(b);
+    {
+      ProfScope prof(ROT_PROF_GEMM, flops, stream);
+      kernel<<<grid, kThreads, C::kSmem, stream>>>(b);
+    }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
   }
   return ROT_OK;

@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "profile.h"
 #include "rot_internal.h"
 #include "split.cuh"
 
@@ -389,25 +390,53 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       pmax = std::max(pmax, b.p[i].p);
     }
     const unsigned n = (unsigned)b.count;
-    qr_init_kernel<<<n, 64, 0, stream>>>(b);
-    qr_colnorm_kernel<<<dim3(std::max(1, std::min(64, pmax / 64)), n), 256, 0, stream>>>(b);
+    // algorithmic flops of one block-reflector application to `rows` rows of
+    // length len: z = Y^T x and x -= Y z', 2 * 2 * b flops per element
+    auto apply_flops = [&](int k0, int mode) {
+      double f = 0.0;
+      for (int i = 0; i < b.count; ++i) {
+        const QrProblem& q = b.p[i];
+        if (k0 >= q.rmax) continue;
+        const int rows = mode == 0 ? std::max(0, q.rmax - k0 - B) : q.p - k0;
+        f += 4.0 * B * (double)rows * (q.p - k0);
+      }
+      return f;
+    };
+    {
+      ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
+      qr_init_kernel<<<n, 64, 0, stream>>>(b);
+    }
+    {
+      ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
+      qr_colnorm_kernel<<<dim3(std::max(1, std::min(64, pmax / 64)), n), 256, 0, stream>>>(b);
+    }
     for (int k0 = 0; k0 < rmax; k0 += B) {
-      qr_panel_kernel<<<n, kPanelThreads, 0, stream>>>(b, k0, rank_rtol);
+      {
+        ProfScope prof(ROT_PROF_QR_PANEL, 0.0, stream);
+        qr_panel_kernel<<<n, kPanelThreads, 0, stream>>>(b, k0, rank_rtol);
+      }
       const int rows = std::max(0, rmax - k0 - B);
-      if (rows > 0)
+      if (rows > 0) {
+        ProfScope prof(ROT_PROF_QR_APPLY, apply_flops(k0, 0), stream);
         qr_apply_kernel<<<dim3((rows + kRows - 1) / kRows, n), 256, 0, stream>>>(b, k0, 0);
+      }
     }
     {
       const int64_t most = (int64_t)pmax * pmax;
+      ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
       qr_eye_kernel<<<dim3((unsigned)std::min<int64_t>(4096, (most + 1023) / 1024), n), 256, 0,
                       stream>>>(b);
     }
     for (int k0 = ((rmax - 1) / B) * B; k0 >= 0; k0 -= B) {
       const int rows = pmax - k0;
+      ProfScope prof(ROT_PROF_QR_APPLY, apply_flops(k0, 1), stream);
       qr_apply_kernel<<<dim3((rows + kRows - 1) / kRows, n), 256, 0, stream>>>(b, k0, 1);
     }
     const int tiles = (pmax + 31) / 32;
-    qr_finalize_kernel<<<dim3((unsigned)std::min(tiles * tiles, 4096), n), 256, 0, stream>>>(b);
+    {
+      ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
+      qr_finalize_kernel<<<dim3((unsigned)std::min(tiles * tiles, 4096), n), 256, 0, stream>>>(b);
+    }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
   }
   return ROT_OK;
