@@ -54,6 +54,7 @@ extern "C" {
 #define ROT_ETIMEOUT (-4)    /* a device-side wait gave up (see rot_status) */
 #define ROT_ENONFINITE (-5)  /* non-finite value found (see rot_status) */
 #define ROT_ENOTSUP (-6)     /* GPU is not sm_103 or the feature is not built */
+#define ROT_ETOOLARGE (-7)   /* plan needs more scratch than rot_step_noalloc holds */
 
 #define ROT_PREC_TF32 1      /* one TF32 tensor-core product per GEMM */
 #define ROT_PREC_3XTF32 3    /* hi*hi + hi*lo + lo*hi TF32 split, ~fp32 accuracy */
@@ -132,6 +133,26 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream);
 int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void* state,
              void* work, float beta1, float beta2, float eps, float lr, int32_t refresh,
              int32_t precision, float rank_rtol, void* stream);
+
+/* rot_step without a workspace argument, for callers that cannot allocate
+ * device memory themselves (for example code running inside a host framework
+ * that owns every device allocation, or a fixed-budget embedding that may not
+ * call cudaMalloc).  The paper has no counterpart: it is an addition of this
+ * library.  The step's temporaries live in one static device array of
+ * ROT_NOALLOC_MAX_BYTES that every GPU loading the library holds until the
+ * process exits; the caller still passes W, G and the state blob.  Plans whose
+ * workspace (rot_state_bytes' work_bytes) exceeds that size are rejected with
+ * ROT_ETOOLARGE before any device work.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Nothing is allocated.  All
+ * calls share the one array and leave their temporaries in it: calls whose
+ * device work overlaps (other streams, other host threads) race on it, so
+ * order them on one stream.  Other arguments, results and errors as
+ * rot_step. */
+#define ROT_NOALLOC_MAX_BYTES (64u << 20)
+int rot_step_noalloc(const rot_plan* plan, float* const* W, const float* const* G, void* state,
+                     float beta1, float beta2, float eps, float lr, int32_t refresh,
+                     int32_t precision, float rank_rtol, void* stream);
 
 /* Synchronise `stream`, then read and clear the device status word of
  * `state`: *status = ROT_OK, or ROT_ETIMEOUT if a device-side wait exceeded its

@@ -25,6 +25,8 @@ ROT_ECUDA = -3
 ROT_ETIMEOUT = -4
 ROT_ENONFINITE = -5
 ROT_ENOTSUP = -6
+ROT_ETOOLARGE = -7
+ROT_NOALLOC_MAX_BYTES = 64 << 20
 ROT_PREC_TF32 = 1
 ROT_PREC_3XTF32 = 3
 ROT_WHICH_M, ROT_WHICH_V2, ROT_WHICH_U, ROT_WHICH_V = 0, 1, 2, 3
@@ -64,6 +66,8 @@ _SIGS = {
     "rot_state_ranks": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp]),
     "rot_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "rot_set_wait_timeout_ns": (_u64, [_u64]),
+    "rot_step_noalloc": (_i32, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _f32, _f32,
+                                _f32, _f32, _i32, _i32, _f32, _vp]),
     "rot_test_gemm": (_i32, [_i32, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _i32,
                              _vp, _u64, _vp, _vp]),
     "rot_test_gemm_work_bytes": (_u64, [_i32, _i32, _i32]),
@@ -186,6 +190,18 @@ def rot_step(plan: Plan, w_ptrs: Sequence[int], g_ptrs: Sequence[int], state_ptr
     _check(lib().rot_step(plan.handle, W, G, _vp(state_ptr), _vp(work_ptr), beta1, beta2, eps,
                           lr, 1 if refresh else 0, precision, rank_rtol, _vp(stream)),
            "rot_step")
+
+
+def rot_step_noalloc(plan: Plan, w_ptrs: Sequence[int], g_ptrs: Sequence[int], state_ptr: int,
+                     beta1: float, beta2: float, eps: float, lr: float, refresh: bool,
+                     precision: int, rank_rtol: float, stream: int) -> None:
+    """rot_step with its temporaries in the library's static device array."""
+    n = max(1, plan.count)
+    W = (_vp * n)(*[_vp(p) for p in w_ptrs])
+    G = (_vp * n)(*[_vp(p) for p in g_ptrs])
+    _check(lib().rot_step_noalloc(plan.handle, W, G, _vp(state_ptr), beta1, beta2, eps, lr,
+                                  1 if refresh else 0, precision, rank_rtol, _vp(stream)),
+           "rot_step_noalloc")
 
 
 def rot_status(plan: Plan, state_ptr: int, stream: int) -> int:

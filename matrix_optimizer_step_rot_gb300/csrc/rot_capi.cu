@@ -344,6 +344,7 @@ const char* rot_strerror(int code) {
     case ROT_ETIMEOUT: return "device-side wait timed out";
     case ROT_ENONFINITE: return "non-finite value";
     case ROT_ENOTSUP: return "device is not sm_103 or feature not built";
+    case ROT_ETOOLARGE: return "workspace need exceeds the static no-allocation scratch";
     default: return "unknown error";
   }
 }
