@@ -164,6 +164,40 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
         if (t < ncol) w[t] = w[t] - P.alpha * __uint_as_float(r[t]);
       return;
     }
+    case kEpiApplySplit: {
+      if (row >= M) return;
+      float* hi = P.c_hi + (int64_t)row * P.ldc + col0;
+      float* lo = P.c_lo + (int64_t)row * P.ldc + col0;
+      if (ncol == 32 && (P.ldc & 3) == 0 && ((reinterpret_cast<uintptr_t>(hi) & 15) == 0) &&
+          ((reinterpret_cast<uintptr_t>(lo) & 15) == 0)) {
+#pragma unroll
+        for (int t = 0; t < 32; t += 4) {
+          float4 h4 = *reinterpret_cast<const float4*>(hi + t);
+          float4 l4 = *reinterpret_cast<const float4*>(lo + t);
+          float* hp = &h4.x;
+          float* lp = &l4.x;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float v = (hp[u] + lp[u]) - P.alpha * __uint_as_float(r[t + u]);
+            split_tf32(v, hp[u], lp[u]);
+          }
+          *reinterpret_cast<float4*>(hi + t) = h4;
+          *reinterpret_cast<float4*>(lo + t) = l4;
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          if (t < ncol) {
+            const float v = (hi[t] + lo[t]) - P.alpha * __uint_as_float(r[t]);
+            float h, l;
+            split_tf32(v, h, l);
+            hi[t] = h;
+            lo[t] = l;
+          }
+        }
+      }
+      return;
+    }
   }
 }
 
@@ -339,6 +373,198 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
+// Precise 3xTF32 variant (BN = 128).  The tensor cores truncate every partial
+// sum they add into a TMEM accumulator, an error that grows with K and that
+// cancellation (a - Y T Y^T a with a small result) then magnifies.  Here each
+// K block of 32 is accumulated afresh: hi*hi into one TMEM accumulator and the
+// cross terms hi*lo + lo*hi into another, and the epilogue warps add both to a
+// float32 running sum held in registers (round to nearest), one K block at a
+// time, double-buffered against the MMAs of the next block.
+// TMEM: 2 buffers x (hi*hi, cross) x 128 columns = 512 columns.
+// ---------------------------------------------------------------------------
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_precise_kernel(const __grid_constant__ TcBatch b) {
+  constexpr int BN = 128;
+  using C = Cfg<BN, STAGES, true>;
+  constexpr uint32_t kCols = 512;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t limit = b.limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 4);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, kCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    for (int i = 0; i < b.count; ++i) {
+      ptx::tma_prefetch_desc(&b.p[i].a_hi);
+      ptx::tma_prefetch_desc(&b.p[i].b_hi);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed_mask = 0, armed_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
+      int pi, m0, nt;
+      decode(b, tile, pi, m0, nt);
+      const TcProblem& P = b.p[pi];
+      const int n0 = nt * BN;
+      const int kblocks = (P.K + BK - 1) / BK;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + stage * C::kStageBytes;
+        ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        armed_mask |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        const int x = kb * BK;
+        ptx::tma_load_2d(st, &P.a_hi, &full[stage], x, m0);
+        ptx::tma_load_2d(st + C::kABytes, &P.a_lo, &full[stage], x, m0);
+        ptx::tma_load_2d(st + 2 * C::kABytes, &P.b_hi, &full[stage], x, n0);
+        ptx::tma_load_2d(st + 2 * C::kABytes + C::kBBytes, &P.b_lo, &full[stage], x, n0);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    for (int s = 0; s < STAGES; ++s)
+      if (armed_mask & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u, limit);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issue
+    constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t chunk = 0;  // K blocks issued so far by this CTA
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
+      int pi, m0, nt;
+      decode(b, tile, pi, m0, nt);
+      const int kblocks = (b.p[pi].K + BK - 1) / BK;
+      for (int kb = 0; kb < kblocks; ++kb, ++chunk) {
+        const uint32_t buf = chunk & 1u, use = chunk >> 1;
+        if (!ptx::mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, limit) ||
+            !ptx::mbar_wait(&full[stage], phase, abort_flag, limit)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_big = tmem_base + buf * 256u, d_small = d_big + 128u;
+        const uint32_t s = ptx::smem_u32(smem + stage * C::kStageBytes);
+        const uint64_t ah = ptx::sw128_kmajor_desc(s);
+        const uint64_t al = ptx::sw128_kmajor_desc(s + C::kABytes);
+        const uint64_t bh = ptx::sw128_kmajor_desc(s + 2 * C::kABytes);
+        const uint64_t bl = ptx::sw128_kmajor_desc(s + 2 * C::kABytes + C::kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);
+          const uint32_t accum = kk > 0 ? 1u : 0u;
+          ptx::umma_tf32(d_small, ah + off, bl + off, idesc, accum);
+          ptx::umma_tf32(d_small, al + off, bh + off, idesc, 1u);
+          ptx::umma_tf32(d_big, ah + off, bh + off, idesc, accum);
+        }
+        ptx::umma_commit(&empty[stage]);
+        ptx::umma_commit(&tfull[buf]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    ptx::umma_commit(drain);
+    mbar_drain(drain, 0, limit);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t chunk = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
+      int pi, m0, nt;
+      decode(b, tile, pi, m0, nt);
+      const TcProblem& P = b.p[pi];
+      const int n0 = nt * BN;
+      const int kblocks = (P.K + BK - 1) / BK;
+      float acc[BN];
+#pragma unroll
+      for (int c = 0; c < BN; ++c) acc[c] = 0.f;
+      for (int kb = 0; kb < kblocks; ++kb, ++chunk) {
+        const uint32_t buf = chunk & 1u, use = chunk >> 1;
+        if (!ptx::mbar_wait(&tfull[buf], use & 1u, abort_flag, limit)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t t_big = tmem_base + lane_off + buf * 256u;
+#pragma unroll
+        for (int h = 0; h < 2 * (BN / 32); ++h) {  // hi*hi chunks, then cross-term chunks
+          const int q = h % (BN / 32);
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(t_big + (h < BN / 32 ? 0u : 128u) + q * 32, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) acc[q * 32 + t] += __uint_as_float(r[t]);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
+      }
+      if (!ok) break;
+      const int row = m0 + quarter * 32 + lane;
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        if (n0 + q * 32 < P.N) {
+          uint32_t r[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(acc[q * 32 + t]);
+          store_chunk(P, row, n0 + q * 32, r);
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag && b.status) atomicExch(b.status, ROT_ETIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -382,10 +608,11 @@ int num_sms() {
   return n;
 }
 
-template <int BN, int STAGES, bool SPLIT3>
+template <int BN, int STAGES, bool SPLIT3, bool PRECISE = false>
 int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stream) {
   using C = Cfg<BN, STAGES, SPLIT3>;
-  auto kernel = gemm_tc_kernel<BN, STAGES, SPLIT3>;
+  static_assert(!PRECISE || (BN == 128 && SPLIT3), "precise variant is 3xTF32, BN = 128");
+  auto kernel = PRECISE ? gemm_tc_precise_kernel<STAGES> : gemm_tc_kernel<BN, STAGES, SPLIT3>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
@@ -443,8 +670,16 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
 
 int gemm_tc(const std::vector<GemmProblem>& probs, int precision, int* status,
             cudaStream_t stream) {
-  if (precision == ROT_PREC_3XTF32) return launch<256, 2, true>(probs, status, stream);
-  return launch<256, 4, false>(probs, status, stream);
+  if (precision == kPrecPrecise) return launch<128, 3, true, true>(probs, status, stream);
+  // narrow products (every N <= 128) use 128-wide tiles so no MMA column is wasted
+  bool narrow = true;
+  for (const GemmProblem& P : probs) narrow = narrow && P.N <= 128;
+  if (precision == ROT_PREC_3XTF32) {
+    return narrow ? launch<128, 3, true>(probs, status, stream)
+                  : launch<256, 2, true>(probs, status, stream);
+  }
+  return narrow ? launch<128, 6, false>(probs, status, stream)
+                : launch<256, 4, false>(probs, status, stream);
 }
 
 }  // namespace rot

@@ -166,7 +166,7 @@ void build_layout(rot_plan* p) {
       x.mT_lo = w.floats(L.n, L.ldm);
       // U side: Z_U^T = (M^T U)^T (m x n) when n < m, else Gram M M^T (m x m)
       const bool u_form1 = L.n < L.m;
-      x.zu_rows = u_form1 ? L.m : L.m;
+      x.zu_rows = L.m;
       x.zu_ld = u_form1 ? L.ldn : L.ldm;
       x.zu_hi = w.floats(x.zu_rows, x.zu_ld);
       x.zu_lo = w.floats(x.zu_rows, x.zu_ld);
@@ -176,10 +176,14 @@ void build_layout(rot_plan* p) {
       x.zv_ld = v_form1 ? L.ldm : L.ldn;
       x.zv_hi = w.floats(x.zv_rows, x.zv_ld);
       x.zv_lo = w.floats(x.zv_rows, x.zv_ld);
-      x.aut = w.floats(L.m, L.ldm);
-      x.avt = w.floats(L.n, L.ldn);
-      x.qut = w.floats(L.m, L.ldm);
-      x.qvt = w.floats(L.n, L.ldn);
+      x.aut_hi = w.floats(L.m, L.ldm);
+      x.aut_lo = w.floats(L.m, L.ldm);
+      x.avt_hi = w.floats(L.n, L.ldn);
+      x.avt_lo = w.floats(L.n, L.ldn);
+      x.qut_hi = w.floats(L.m, L.ldm);
+      x.qut_lo = w.floats(L.m, L.ldm);
+      x.qvt_hi = w.floats(L.n, L.ldn);
+      x.qvt_lo = w.floats(L.n, L.ldn);
       const int rmax = std::min(L.m, L.n);
       x.aux_u = w.take(qr_aux_bytes(L.m, rmax));
       x.aux_v = w.take(qr_aux_bytes(L.n, rmax));

@@ -34,8 +34,10 @@ struct WorkLayout {
   uint64_t zu_hi, zu_lo;  // (M^T U)^T (m x ldn) or M M^T (m x ldm)
   int zv_rows, zv_ld;
   uint64_t zv_hi, zv_lo;  // (M V)^T (n x ldm) or M^T M (n x ldn)
-  uint64_t aut, avt;      // A_U^T (m x ldm), A_V^T (n x ldn), float32
-  uint64_t qut, qvt;      // Q^T outputs of the QR, float32
+  uint64_t aut_hi, aut_lo;  // A_U^T split (m x ldm); QR input, then reflectors
+  uint64_t avt_hi, avt_lo;  // A_V^T split (n x ldn)
+  uint64_t qut_hi, qut_lo;  // Q^T accumulators of the QR, splits
+  uint64_t qvt_hi, qvt_lo;
   uint64_t aux_u, aux_v;  // QR scratch
 };
 

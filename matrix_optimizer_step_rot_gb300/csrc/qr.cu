@@ -9,16 +9,25 @@
 // is positive.  The input's rank is at most rmax (= min(m, n) for the bases of
 // an m x n momentum), so only the first rmax columns are ever factored.
 //
-// Storage: the input arrives transposed (row j of `at` = column j of A), so a
-// column and a reflector are contiguous.  Reflector k overwrites row k from
-// element k on (w_0 at the diagonal, the tail of x after it).
+// Storage: the input arrives transposed and split (row j of `at` = column j
+// of A, as hi + lo), so a column and a reflector are contiguous.  Reflector k
+// overwrites row k from element k on (w_0 at the diagonal, the tail of x
+// after it); the R entries the factorisation leaves in front of it are
+// zeroed, so rows of `at` serve directly as the reflector matrix Y^T.
 //
-// Blocking (Golub & Van Loan, "Matrix Computations", section 5.1.7, compact
-// WY): a panel of b = 32 columns is factored by one CTA per matrix; its
-// reflectors form H_{k0}..H_{k0+b-1} = I - Y T Y^T with T upper triangular
-// (T_jj = 2 / w_j^T w_j, T[0:j, j] = -T_jj T[0:j, 0:j] Y[:, 0:j]^T w_j).  The
-// trailing columns then receive a <- (I - Y T^T Y^T) a, and Q is accumulated
-// backwards panel by panel with q <- (I - Y T Y^T) q.
+// Blocking (compact WY: Schreiber & Van Loan, "A storage-efficient WY
+// representation for products of Householder transformations", 1989; Golub &
+// Van Loan, "Matrix Computations", section 5.1.7):
+//   * panels of b = 32 columns are factored by one thread-block cluster per
+//     matrix with the panel resident in distributed shared memory;
+//   * the rest of the panel's 128-column block is updated on CUDA cores with
+//     the panel's 32 x 32 triangular factor;
+//   * each 128-column block's reflectors form H_k..H_{k+127} = I - Y T Y^T;
+//     the columns after the block (up to rmax) receive a <- (I - Y T^T Y^T) a,
+//     and Q is accumulated backwards block by block, q <- (I - Y T Y^T) q, both
+//     as three tensor-core GEMMs (T^T Y^T or T Y^T, then X (Y T), X -= Z Y^T).
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <cstring>
 
@@ -26,10 +35,13 @@
 #include "rot_internal.h"
 #include "split.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace rot {
 namespace {
 
-constexpr int B = kQrPanel;
+constexpr int B = kQrPanel;   // panel width (32)
+constexpr int NB = kQrBlock;  // block width (128)
 constexpr int kMaxQ = 64;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -38,8 +50,8 @@ struct QrBatch {
   QrProblem p[kMaxQ];
 };
 
-// scratch layout inside QrProblem pointers (set on the host): see qr_aux_bytes
 __host__ __device__ inline int npanels(int rmax) { return (rmax + B - 1) / B; }
+__host__ __device__ inline int nblocks(int rmax) { return (rmax + NB - 1) / NB; }
 
 // ---------------------------------------------------------------------------
 // reductions
@@ -49,17 +61,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
-}
-
-// Sum of v over the block, returned to every thread.  `red` has >= 32 floats.
-__device__ float block_sum(float v, float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_sum(v);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = lane < nw ? red[lane] : 0.f;
-  return warp_sum(t);
 }
 
 // 32 values per thread -> lane L of each warp holds the warp's total of v[L]
@@ -77,6 +78,10 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[B]) {
     }
   }
   return v[0];
+}
+
+__device__ __forceinline__ int rank_now(const QrProblem& q) {
+  return q.ctrl[1] ? q.ctrl[0] : q.rmax;
 }
 
 // ---------------------------------------------------------------------------
@@ -97,9 +102,12 @@ __global__ void qr_colnorm_kernel(const __grid_constant__ QrBatch b) {
   const int warps = blockDim.x >> 5;
   float best = 0.f;
   for (int j = blockIdx.x * warps + (threadIdx.x >> 5); j < q.p; j += gridDim.x * warps) {
-    const float* row = q.at + (int64_t)j * q.ld;
+    const int64_t o = (int64_t)j * q.ld;
     float s = 0.f;
-    for (int e = lane; e < q.p; e += 32) s = fmaf(row[e], row[e], s);
+    for (int e = lane; e < q.p; e += 32) {
+      const float x = q.at.hi[o + e] + q.at.lo[o + e];
+      s = fmaf(x, x, s);
+    }
     s = warp_sum(s);
     best = fmaxf(best, sqrtf(s));
   }
@@ -107,145 +115,224 @@ __global__ void qr_colnorm_kernel(const __grid_constant__ QrBatch b) {
 }
 
 // ---------------------------------------------------------------------------
-// panel factorisation: one CTA per matrix, columns k0 .. k0+bw-1
+// panel factorisation: one cluster of `cs` CTAs per matrix, columns
+// k0 .. k0+bw-1; CTA c of the cluster holds elements [k0 + c R, k0 + (c+1) R)
+// of the panel's rows in shared memory.  Per column two cluster-wide sums
+// (||x||^2 with x_0, then the 31 dot products with w) go through distributed
+// shared memory; every CTA adds the partials in the same order, so all of
+// them take the same decisions.
 // ---------------------------------------------------------------------------
 
-constexpr int kPanelThreads = 512;
+constexpr int kPanelThreads = 256;
+constexpr int kMaxCluster = 16;  // 16 needs the non-portable cluster size
 
 __global__ void __launch_bounds__(kPanelThreads)
-    qr_panel_kernel(const __grid_constant__ QrBatch b, int k0, float rtol) {
-  const QrProblem& q = b.p[blockIdx.x];
-  if (k0 >= q.rmax) return;
-  const int panel = k0 / B;
-  if (q.ctrl[1]) {  // stopped in an earlier panel
-    if (threadIdx.x == 0) q.ctrl[2 + panel] = 0;
-    return;
-  }
-  __shared__ float red[B][33];
-  __shared__ float s_red[32];
-  __shared__ float s_dot[B];
-  __shared__ float s_ww[B];
-  __shared__ float s_beta[B];
-  __shared__ float gram[B][B + 1];  // gram[i][j] = w_i . w_j, i < j
+    qr_panel_kernel(const __grid_constant__ QrBatch b, int k0, float rtol, int R) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int cs = (int)cl.num_blocks();
+  const int crank = (int)cl.block_rank();
+  const QrProblem& q = b.p[blockIdx.x / cs];
+  extern __shared__ float panel[];  // [B][R]
+  __shared__ float slot_n[2][kMaxCluster][2];
+  __shared__ float slot_d[2][kMaxCluster][B];
+  __shared__ float red[B][kPanelThreads / 32 + 1];
+  __shared__ float s_red[kPanelThreads / 32];
+  __shared__ float s_ww[B], s_beta[B];
+  __shared__ float gram[B][B + 1];
   __shared__ float tmat[B][B + 1];
+  __shared__ float s_dot[B];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarp = nthr >> 5;
   const int p = q.p, ld = q.ld;
-  float* at = q.at;
+  const int kb0 = (k0 / NB) * NB;  // start of this panel's 128-column block
+  const int panel_id = k0 / B;
+  const bool in_range = k0 < q.rmax;
+  const int bw = in_range ? min(B, q.rmax - k0) : 0;
+  const int e0 = k0 + crank * R, e1 = min(p, e0 + R);
+  float* at_hi = q.at.hi;
+  float* at_lo = q.at.lo;
+
+  if (!in_range) {  // the same for every CTA of the cluster
+    cl.sync();
+    return;
+  }
+  if (q.ctrl[1] != 0) {
+    // stopped in an earlier panel: these rows are identities; clear them so
+    // that the block GEMMs read zeros there
+    for (int j = 0; j < bw; ++j)
+      for (int e = kb0 + crank * nthr + tid; e < p; e += cs * nthr) {
+        const int64_t o = (int64_t)(k0 + j) * ld + e;
+        at_hi[o] = 0.f;
+        at_lo[o] = 0.f;
+      }
+    if (crank == 0 && tid == 0) q.ctrl[2 + panel_id] = 0;
+    cl.sync();
+    return;
+  }
+
+  // load my slice of the panel; clear the R entries in front of it
+  // (elements kb0 .. k0-1 of the panel's rows)
+  for (int i = tid; i < bw * R; i += nthr) {
+    const int j = i / R, e = e0 + i % R;
+    float x = 0.f;
+    if (e < e1) {
+      const int64_t o = (int64_t)(k0 + j) * ld + e;
+      x = at_hi[o] + at_lo[o];
+    }
+    panel[i] = x;
+  }
+  for (int j = 0; j < bw; ++j)
+    for (int e = kb0 + crank * nthr + tid; e < k0; e += cs * nthr) {
+      const int64_t o = (int64_t)(k0 + j) * ld + e;
+      at_hi[o] = 0.f;
+      at_lo[o] = 0.f;
+    }
   const float thr = rtol * q.tau[0];
-  const int bw = min(B, q.rmax - k0);
   int active = bw;
+  cl.sync();
 
   for (int j = 0; j < bw; ++j) {
     const int k = k0 + j;
-    float* xr = at + (int64_t)k * ld;
+    const int par = j & 1;
+    const int lo_e = max(k, e0);
+    float* wr = panel + j * R;
+    // ||x||^2 over my elements, and x_0 if element k is mine
     float s = 0.f;
-    for (int e = k + tid; e < p; e += nthr) s = fmaf(xr[e], xr[e], s);
-    s = block_sum(s, s_red);
-    const float nx = sqrtf(s);
+    for (int e = lo_e + tid; e < e1; e += nthr) s = fmaf(wr[e - e0], wr[e - e0], s);
+    s = warp_sum(s);
+    if (lane == 0) s_red[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < nwarp; ++w) t += s_red[w];
+      const float xk = (k >= e0 && k < e1) ? wr[k - e0] : 0.f;
+      for (int c = 0; c < cs; ++c) {
+        float* dst = cl.map_shared_rank(&slot_n[par][crank][0], c);
+        dst[0] = t;
+        dst[1] = xk;
+      }
+    }
+    cl.sync();
+    float sn = 0.f, x0 = 0.f;
+    for (int c = 0; c < cs; ++c) {
+      sn += slot_n[par][c][0];
+      x0 += slot_n[par][c][1];
+    }
+    const float nx = sqrtf(sn);
     if (nx <= thr) {  // numerical rank reached: H_k .. are identities
       active = j;
       break;
     }
-    const float x0 = xr[k];
     const float beta = x0 >= 0.f ? -nx : nx;
     const float w0 = x0 - beta;
-    const float ww = 2.f * fmaf(fabsf(x0), nx, s);  // ||x - beta e0||^2, no cancellation
-    __syncthreads();  // every thread has read xr[k]
+    const float ww = 2.f * fmaf(fabsf(x0), nx, sn);  // ||x - beta e0||^2, no cancellation
     if (tid == 0) {
-      xr[k] = w0;
+      if (k >= e0 && k < e1) wr[k - e0] = w0;
       s_ww[j] = ww;
       s_beta[j] = beta;
     }
     __syncthreads();
 
-    // dots of w with the other panel rows over elements k..p-1: for c < j the
-    // row holds reflector c (its support starts at k0+c < k), for c > j the
-    // not yet reduced column c.
+    // dots of w with the other panel rows over my elements >= k
     float acc[B];
 #pragma unroll
     for (int c = 0; c < B; ++c) acc[c] = 0.f;
-    for (int e = k + tid; e < p; e += nthr) {
-      const float we = xr[e];
+    for (int e = lo_e + tid; e < e1; e += nthr) {
+      const float we = wr[e - e0];
 #pragma unroll
       for (int c = 0; c < B; ++c)
-        if (c < bw && c != j) acc[c] = fmaf(we, at[(int64_t)(k0 + c) * ld + e], acc[c]);
+        if (c < bw && c != j) acc[c] = fmaf(we, panel[c * R + (e - e0)], acc[c]);
     }
-    const float part = warp_transpose_sum(acc);  // lane c: this warp's sum for c
+    const float part = warp_transpose_sum(acc);
     red[lane][warp] = part;
     __syncthreads();
     if (tid < B) {
       float t = 0.f;
       for (int w = 0; w < nwarp; ++w) t += red[tid][w];
+      for (int c = 0; c < cs; ++c) *cl.map_shared_rank(&slot_d[par][crank][tid], c) = t;
+    }
+    cl.sync();
+    if (tid < B) {
+      float t = 0.f;
+      for (int c = 0; c < cs; ++c) t += slot_d[par][c][tid];
       s_dot[tid] = t;
       if (tid < j) gram[tid][j] = t;
     }
     __syncthreads();
-
-    // apply H_k to the remaining panel columns
-    for (int e = k + tid; e < p; e += nthr) {
-      const float we = xr[e];
-      for (int c = j + 1; c < bw; ++c) {
-        const float coef = 2.f * s_dot[c] / ww;
-        at[(int64_t)(k0 + c) * ld + e] -= coef * we;
-      }
+    // apply H_k to the remaining panel rows (my elements >= k)
+    for (int e = lo_e + tid; e < e1; e += nthr) {
+      const float we = wr[e - e0];
+      for (int c = j + 1; c < bw; ++c) panel[c * R + (e - e0)] -= (2.f * s_dot[c] / ww) * we;
     }
     __syncthreads();
   }
 
-  // T: T_jj = 2 / ww_j ; T[0:j, j] = -T_jj * T[0:j, 0:j] * gram[0:j, j]
-  if (warp == 0) {
-    for (int i = lane; i < B * (B + 1); i += 32) (&tmat[0][0])[i] = 0.f;
-    __syncwarp();
-    for (int j = 0; j < active; ++j) {
-      const float tjj = 2.f / s_ww[j];
-      float t = 0.f;
-      if (lane < j) {
-        for (int l = lane; l < j; ++l) t = fmaf(tmat[lane][l], gram[l][j], t);
+  // zero the R entries inside the panel (elements < k of reflector row k)
+  // and the rows past the rank; write my slice back as a split
+  for (int i = tid; i < bw * R; i += nthr) {
+    const int j = i / R, e = e0 + i % R;
+    if (e >= e1) continue;
+    float x = panel[i];
+    if (j >= active || e < k0 + j) x = 0.f;
+    float h, l;
+    split_tf32(x, h, l);
+    const int64_t o = (int64_t)(k0 + j) * ld + e;
+    at_hi[o] = h;
+    at_lo[o] = l;
+  }
+
+  if (crank == 0) {
+    // panel factor T: T_jj = 2 / ww_j ; T[0:j, j] = -T_jj * T[0:j, 0:j] * gram[0:j, j]
+    if (warp == 0) {
+      for (int i = lane; i < B * (B + 1); i += 32) (&tmat[0][0])[i] = 0.f;
+      __syncwarp();
+      for (int j = 0; j < active; ++j) {
+        const float tjj = 2.f / s_ww[j];
+        float t = 0.f;
+        if (lane < j)
+          for (int l = lane; l < j; ++l) t = fmaf(tmat[lane][l], gram[l][j], t);
+        __syncwarp();
+        if (lane < j) tmat[lane][j] = -tjj * t;
+        if (lane == j) tmat[j][j] = tjj;
+        __syncwarp();
       }
-      __syncwarp();
-      if (lane < j) tmat[lane][j] = -tjj * t;
-      if (lane == j) tmat[j][j] = tjj;
-      __syncwarp();
+    }
+    __syncthreads();
+    float* tf = q.tf + (int64_t)panel_id * B * B;
+    for (int i = tid; i < B * B; i += nthr) tf[i] = tmat[i / B][i % B];
+    if (tid < active) q.beta[k0 + tid] = s_beta[tid];
+    if (tid == 0) {
+      q.ctrl[2 + panel_id] = active;
+      if (active < bw) {
+        q.ctrl[1] = 1;
+        q.ctrl[0] = k0 + active;
+      }
     }
   }
-  __syncthreads();
-  float* tf = q.tf + (int64_t)panel * B * B;
-  for (int i = tid; i < B * B; i += nthr) tf[i] = tmat[i / B][i % B];
-  if (tid < active) q.beta[k0 + tid] = s_beta[tid];
-  if (tid == 0) {
-    q.ctrl[2 + panel] = active;
-    if (active < bw) {
-      q.ctrl[1] = 1;
-      q.ctrl[0] = k0 + active;
-    }
-  }
+  cl.sync();  // no CTA leaves while its shared memory may still be written
 }
 
 // ---------------------------------------------------------------------------
-// apply one panel's block reflector to 32 rows of a row-stored matrix:
-//   mode 0 (factorisation, rows k0+b .. rmax-1 of `at`): a <- a - Y (T^T (Y^T a))
-//   mode 1 (Q formation, rows k0 .. p-1 of `qt`):        q <- q - Y (T (Y^T q))
-// Only elements k0..p-1 of each row are touched.
+// within-block update: rows k0+b .. (block end)-1 of `at` get the panel's
+// reflectors, a <- a - Y (T^T (Y^T a)), elements k0..p-1 (CUDA cores)
 // ---------------------------------------------------------------------------
 
 constexpr int kRows = 32;
 
-__global__ void __launch_bounds__(256)
-    qr_apply_kernel(const __grid_constant__ QrBatch b, int k0, int mode) {
+__global__ void __launch_bounds__(256) qr_panel_apply_kernel(const __grid_constant__ QrBatch b,
+                                                             int k0) {
   const QrProblem& q = b.p[blockIdx.y];
   if (k0 >= q.rmax) return;
   const int panel = k0 / B;
   const int active = q.ctrl[2 + panel];
   if (active == 0) return;
   const int p = q.p, ld = q.ld;
-  const int row_begin = mode == 0 ? k0 + B : k0;
-  const int row_end = mode == 0 ? q.rmax : p;
-  const int r0 = row_begin + blockIdx.x * kRows;
+  const int row_end = min(q.rmax, (k0 / NB) * NB + NB);
+  const int r0 = k0 + B + blockIdx.x * kRows;
   if (r0 >= row_end) return;
-  float* X = mode == 0 ? q.at : q.qt;
-  const float* Y = q.at;  // reflector i: row k0+i, elements >= k0+i
+  float* xh = q.at.hi;
+  float* xl = q.at.lo;
 
   __shared__ float xs[kRows][33];
   __shared__ float ys[B][33];
@@ -256,7 +343,6 @@ __global__ void __launch_bounds__(256)
   const float* tf = q.tf + (int64_t)panel * B * B;
   for (int i = tid; i < B * B; i += 256) tm[i / B][i % B] = tf[i];
 
-  // phase 1: z[r][i] = sum_e X[r][e] Y_i[e]
   const int r = tid >> 3, i4 = (tid & 7) * 4;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int e0 = k0; e0 < p; e0 += 32) {
@@ -264,9 +350,17 @@ __global__ void __launch_bounds__(256)
     for (int t = tid; t < kRows * 32; t += 256) {
       const int rr = t >> 5, ee = t & 31, e = e0 + ee;
       const int row = r0 + rr;
-      xs[rr][ee] = (row < row_end && e < p) ? X[(int64_t)row * ld + e] : 0.f;
-      const int yi = rr;  // reflector index (B == kRows == 32)
-      ys[yi][ee] = (yi < active && e < p && e >= k0 + yi) ? Y[(int64_t)(k0 + yi) * ld + e] : 0.f;
+      float xv = 0.f, yv = 0.f;
+      if (row < row_end && e < p) {
+        const int64_t o = (int64_t)row * ld + e;
+        xv = xh[o] + xl[o];
+      }
+      if (rr < active && e < p && e >= k0 + rr) {
+        const int64_t o = (int64_t)(k0 + rr) * ld + e;
+        yv = xh[o] + xl[o];
+      }
+      xs[rr][ee] = xv;
+      ys[rr][ee] = yv;
     }
     __syncthreads();
 #pragma unroll 8
@@ -279,24 +373,25 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int c = 0; c < 4; ++c) z[r][i4 + c] = acc[c];
   __syncthreads();
-
-  // phase 2: zt = z T (mode 0: rows of T^T z) or z T^T (mode 1: rows of T z)
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int i = i4 + c;
     float t = 0.f;
-    for (int jj = 0; jj < B; ++jj) t = fmaf(z[r][jj], mode == 0 ? tm[jj][i] : tm[i][jj], t);
+    for (int jj = 0; jj < B; ++jj) t = fmaf(z[r][jj], tm[jj][i], t);
     zt[r][i] = t;
   }
   __syncthreads();
-
-  // phase 3: X[r][e] -= sum_i zt[r][i] Y_i[e]
   const int e4 = (tid & 7) * 4;
   for (int e0 = k0; e0 < p; e0 += 32) {
     __syncthreads();
     for (int t = tid; t < B * 32; t += 256) {
       const int yi = t >> 5, ee = t & 31, e = e0 + ee;
-      ys[yi][ee] = (yi < active && e < p && e >= k0 + yi) ? Y[(int64_t)(k0 + yi) * ld + e] : 0.f;
+      float yv = 0.f;
+      if (yi < active && e < p && e >= k0 + yi) {
+        const int64_t o = (int64_t)(k0 + yi) * ld + e;
+        yv = xh[o] + xl[o];
+      }
+      ys[yi][ee] = yv;
     }
     __syncthreads();
     const int row = r0 + r;
@@ -308,7 +403,11 @@ __global__ void __launch_bounds__(256)
           float t = 0.f;
 #pragma unroll 8
           for (int i = 0; i < B; ++i) t = fmaf(zt[r][i], ys[i][e4 + c], t);
-          X[(int64_t)row * ld + e] -= t;
+          const int64_t o = (int64_t)row * ld + e;
+          float h, l;
+          split_tf32((xh[o] + xl[o]) - t, h, l);
+          xh[o] = h;
+          xl[o] = l;
         }
       }
     }
@@ -316,7 +415,53 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
-// Q^T = I, then the sign fix and the split outputs U^T (= Q^T) and U (= Q)
+// block factor T (nb x nb, upper triangular) from the Gram S = Y^T Y of the
+// block's reflectors: T_ii = 2 / S_ii, T[0:i, i] = -T_ii T[0:i, 0:i] S[0:i, i];
+// reflectors past the numerical rank get zero rows and columns.  Writes T and
+// T^T as splits (ld NB).  One CTA per matrix.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(NB) qr_tblock_kernel(const __grid_constant__ QrBatch b,
+                                                       int kb0) {
+  const QrProblem& q = b.p[blockIdx.x];
+  if (kb0 >= q.rmax) return;
+  extern __shared__ float tsm[];  // [NB][NB + 1]
+  const int nb = min(NB, q.rmax - kb0);
+  const int act = max(0, min(nb, rank_now(q) - kb0));
+  const int blk = kb0 / NB;
+  const float* S = q.s;
+  const int tid = threadIdx.x;
+  constexpr int LD = NB + 1;
+  for (int i = tid; i < NB * LD; i += blockDim.x) tsm[i] = 0.f;
+  __syncthreads();
+  for (int i = 0; i < act; ++i) {
+    const float tii = 2.f / S[(int64_t)i * NB + i];
+    float t = 0.f;
+    if (tid < i)
+      for (int l = tid; l < i; ++l) t = fmaf(tsm[tid * LD + l], S[(int64_t)l * NB + i], t);
+    __syncthreads();
+    if (tid < i) tsm[tid * LD + i] = -tii * t;
+    if (tid == i) tsm[i * LD + i] = tii;
+    __syncthreads();
+  }
+  float* th = q.tb.hi + (int64_t)blk * NB * NB;
+  float* tl = q.tb.lo + (int64_t)blk * NB * NB;
+  float* uh = q.tbt.hi + (int64_t)blk * NB * NB;
+  float* ul = q.tbt.lo + (int64_t)blk * NB * NB;
+  for (int i = tid; i < NB * NB; i += blockDim.x) {
+    const int r = i / NB, c = i % NB;
+    float h, l;
+    split_tf32(tsm[r * LD + c], h, l);
+    th[i] = h;
+    tl[i] = l;
+    split_tf32(tsm[c * LD + r], h, l);
+    uh[i] = h;
+    ul[i] = l;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Q^T = I (split), then the sign fix and the split outputs U^T and U
 // ---------------------------------------------------------------------------
 
 __global__ void qr_eye_kernel(const __grid_constant__ QrBatch b) {
@@ -325,14 +470,16 @@ __global__ void qr_eye_kernel(const __grid_constant__ QrBatch b) {
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(e / q.p), c = (int)(e % q.p);
-    q.qt[(int64_t)r * q.ld + c] = r == c ? 1.f : 0.f;
+    const int64_t o = (int64_t)r * q.ld + c;
+    q.qt.hi[o] = r == c ? 1.f : 0.f;
+    q.qt.lo[o] = 0.f;
   }
 }
 
 __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
   __shared__ float tile[32][33];
   const QrProblem& q = b.p[blockIdx.y];
-  const int rank = q.ctrl[1] ? q.ctrl[0] : q.rmax;
+  const int rank = rank_now(q);
   const int tiles = (q.p + 31) / 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   for (int t = blockIdx.x; t < tiles * tiles; t += gridDim.x) {
@@ -341,7 +488,8 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
       const int r = r0 + i, c = c0 + tx;
       float v = 0.f;
       if (r < q.p && c < q.p) {
-        v = q.qt[(int64_t)r * q.ld + c];
+        const int64_t oi = (int64_t)r * q.ld + c;
+        v = q.qt.hi[oi] + q.qt.lo[oi];
         if (r < rank && q.beta[r] < 0.f) v = -v;  // row r of Q^T = column r of Q
         float h, l;
         split_tf32(v, h, l);
@@ -367,18 +515,113 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
   if (blockIdx.x == 0 && threadIdx.x == 0 && q.rank_out) *q.rank_out = rank;
 }
 
+// ---------------------------------------------------------------------------
+// host helpers
+// ---------------------------------------------------------------------------
+
+GemmProblem gp(int M, int N, int K, const float* ah, const float* al, int lda, const float* bh,
+               const float* bl, int ldb, float* ch, float* cl, int ldc, int epi,
+               float alpha = 0.f) {
+  GemmProblem P;
+  P.M = M;
+  P.N = N;
+  P.K = K;
+  P.a_hi = ah;
+  P.a_lo = al;
+  P.lda = lda;
+  P.b_hi = bh;
+  P.b_lo = bl;
+  P.ldb = ldb;
+  P.c_hi = ch;
+  P.c_lo = cl;
+  P.ldc = ldc;
+  P.epi = epi;
+  P.alpha = alpha;
+  return P;
+}
+
+int launch_panel(const QrBatch& b, int k0, float rtol, int cs, int R, cudaStream_t stream) {
+  const size_t smem = sizeof(float) * (size_t)B * R;
+  static size_t configured = 0;
+  if (smem > configured) {
+    if (cudaFuncSetAttribute(qr_panel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(qr_panel_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) != cudaSuccess)
+      return ROT_ECUDA;
+    configured = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(b.count * cs));
+  cfg.blockDim = dim3(kPanelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ProfScope prof(ROT_PROF_QR_PANEL, 0.0, stream);
+  return cudaLaunchKernelEx(&cfg, qr_panel_kernel, b, k0, rtol, R) == cudaSuccess ? ROT_OK
+                                                                                   : ROT_ECUDA;
+}
+
 }  // namespace
 
 uint64_t qr_aux_bytes(int p, int rmax) {
-  (void)p;
-  const uint64_t np = (uint64_t)npanels(rmax);
-  return align256(np * B * B * 4) + align256((uint64_t)rmax * 4 + 4) + align256((np + 2) * 4) +
-         256;
+  const uint64_t np = (uint64_t)npanels(rmax), nbk = (uint64_t)nblocks(rmax);
+  const uint64_t ld = (uint64_t)pad_ld(p);
+  return align256(np * B * B * 4)                   // panel T factors
+         + align256((uint64_t)rmax * 4 + 4)         // beta
+         + align256((np + 2) * 4) + 256             // ctrl, tau
+         + 2 * align256((uint64_t)p * NB * 4)       // yt split
+         + 2 * align256((uint64_t)NB * ld * 4)      // w1t split
+         + 2 * align256((uint64_t)p * NB * 4)       // z split
+         + align256((uint64_t)NB * NB * 4)          // Gram S
+         + 4 * align256(nbk * NB * NB * 4);         // T and T^T splits per block
+}
+
+void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax) {
+  const uint64_t np = (uint64_t)npanels(rmax), nbk = (uint64_t)nblocks(rmax);
+  const uint64_t ld = (uint64_t)pad_ld(p);
+  uint64_t o = 0;
+  auto take = [&](uint64_t bytes) {
+    char* ptr = aux + o;
+    o += align256(bytes);
+    return ptr;
+  };
+  q.tf = reinterpret_cast<float*>(take(np * B * B * 4));
+  q.beta = reinterpret_cast<float*>(take((uint64_t)rmax * 4 + 4));
+  q.ctrl = reinterpret_cast<int*>(take((np + 2) * 4));
+  q.tau = reinterpret_cast<float*>(take(256));
+  q.yt.hi = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
+  q.yt.lo = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
+  q.w1t.hi = reinterpret_cast<float*>(take((uint64_t)NB * ld * 4));
+  q.w1t.lo = reinterpret_cast<float*>(take((uint64_t)NB * ld * 4));
+  q.z.hi = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
+  q.z.lo = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
+  q.s = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
+  q.tb.hi = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
+  q.tb.lo = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
+  q.tbt.hi = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
+  q.tbt.lo = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
 }
 
 int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status,
                cudaStream_t stream) {
-  (void)status;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  static bool tattr = false;
+  if (!tattr) {
+    if (cudaFuncSetAttribute(qr_tblock_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(NB * (NB + 1) * sizeof(float))) != cudaSuccess)
+      return ROT_ECUDA;
+    tattr = true;
+  }
   for (size_t base = 0; base < probs.size(); base += kMaxQ) {
     QrBatch b;
     std::memset(&b, 0, sizeof(b));
@@ -390,18 +633,13 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       pmax = std::max(pmax, b.p[i].p);
     }
     const unsigned n = (unsigned)b.count;
-    // algorithmic flops of one block-reflector application to `rows` rows of
-    // length len: z = Y^T x and x -= Y z', 2 * 2 * b flops per element
-    auto apply_flops = [&](int k0, int mode) {
-      double f = 0.0;
-      for (int i = 0; i < b.count; ++i) {
-        const QrProblem& q = b.p[i];
-        if (k0 >= q.rmax) continue;
-        const int rows = mode == 0 ? std::max(0, q.rmax - k0 - B) : q.p - k0;
-        f += 4.0 * B * (double)rows * (q.p - k0);
-      }
-      return f;
-    };
+    // cluster size: enough CTAs that a panel slice fits in shared memory
+    // (<= 1536 elements x 32 rows = 192 KB), more while free SMs allow it and
+    // each CTA keeps >= 256 elements
+    int cs = std::max(1, (pmax + 1535) / 1536);
+    while (cs < kMaxCluster && (cs + 1) * b.count <= sms && pmax / (cs + 1) >= 256) ++cs;
+    cs = std::min(cs, kMaxCluster);
+    const int R = ((pmax + cs - 1) / cs + 3) / 4 * 4;
     {
       ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
       qr_init_kernel<<<n, 64, 0, stream>>>(b);
@@ -410,27 +648,96 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
       qr_colnorm_kernel<<<dim3(std::max(1, std::min(64, pmax / 64)), n), 256, 0, stream>>>(b);
     }
-    for (int k0 = 0; k0 < rmax; k0 += B) {
-      {
-        ProfScope prof(ROT_PROF_QR_PANEL, 0.0, stream);
-        qr_panel_kernel<<<n, kPanelThreads, 0, stream>>>(b, k0, rank_rtol);
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+
+    // ---- factorisation, block by block
+    for (int kb0 = 0; kb0 < rmax; kb0 += NB) {
+      for (int k0 = kb0; k0 < std::min(rmax, kb0 + NB); k0 += B) {
+        if (launch_panel(b, k0, rank_rtol, cs, R, stream) != ROT_OK) return ROT_ECUDA;
+        const int rows = std::min(rmax, kb0 + NB) - k0 - B;
+        if (rows > 0) {
+          double f = 0.0;
+          for (int i = 0; i < b.count; ++i) {
+            const QrProblem& q = b.p[i];
+            const int re = std::min(q.rmax, kb0 + NB);
+            if (k0 < q.rmax && re > k0 + B) f += 4.0 * B * (double)(re - k0 - B) * (q.p - k0);
+          }
+          ProfScope prof(ROT_PROF_QR_APPLY, f, stream);
+          qr_panel_apply_kernel<<<dim3((rows + kRows - 1) / kRows, n), 256, 0, stream>>>(b, k0);
+        }
       }
-      const int rows = std::max(0, rmax - k0 - B);
-      if (rows > 0) {
-        ProfScope prof(ROT_PROF_QR_APPLY, apply_flops(k0, 0), stream);
-        qr_apply_kernel<<<dim3((rows + kRows - 1) / kRows, n), 256, 0, stream>>>(b, k0, 0);
+      // block factor T from the Gram of the block's reflectors
+      std::vector<GemmProblem> gram;
+      for (int i = 0; i < b.count; ++i) {
+        const QrProblem& q = b.p[i];
+        if (kb0 >= q.rmax) continue;
+        const int nb = std::min(NB, q.rmax - kb0);
+        const int64_t o = (int64_t)kb0 * q.ld + kb0;
+        gram.push_back(gp(nb, nb, q.p - kb0, q.at.hi + o, q.at.lo + o, q.ld, q.at.hi + o,
+                          q.at.lo + o, q.ld, q.s, nullptr, NB, kEpiStoreF32));
+      }
+      if (gemm_grouped(gram, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+      {
+        ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
+        qr_tblock_kernel<<<n, NB, NB * (NB + 1) * sizeof(float), stream>>>(b, kb0);
+      }
+      // trailing columns kb0+NB .. rmax-1: a <- a - Y (T^T (Y^T a))
+      std::vector<TransposeSeg> tr;
+      std::vector<GemmProblem> f1, f2, f3;
+      for (int i = 0; i < b.count; ++i) {
+        const QrProblem& q = b.p[i];
+        const int kend = kb0 + NB;
+        if (kend >= q.rmax) continue;
+        const int nb = NB, L = q.p - kb0, nr = q.rmax - kend;
+        const int blk = kb0 / NB;
+        const int64_t oy = (int64_t)kb0 * q.ld + kb0, ox = (int64_t)kend * q.ld + kb0;
+        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, NB, nb, L, 1, 1});
+        f1.push_back(gp(nb, L, nb, q.tbt.hi + (int64_t)blk * NB * NB,
+                        q.tbt.lo + (int64_t)blk * NB * NB, NB, q.yt.hi, q.yt.lo, NB, q.w1t.hi,
+                        q.w1t.lo, q.ld, kEpiStoreSplit));
+        f2.push_back(gp(nr, nb, L, q.at.hi + ox, q.at.lo + ox, q.ld, q.w1t.hi, q.w1t.lo, q.ld,
+                        q.z.hi, q.z.lo, NB, kEpiStoreSplit));
+        f3.push_back(gp(nr, L, nb, q.z.hi, q.z.lo, NB, q.yt.hi, q.yt.lo, NB, q.at.hi + ox,
+                        q.at.lo + ox, q.ld, kEpiApplySplit, 1.f));
+      }
+      if (!tr.empty()) {
+        if (launch_transpose(tr, stream) != ROT_OK) return ROT_ECUDA;
+        if (gemm_grouped(f1, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+        if (gemm_grouped(f2, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+        if (gemm_grouped(f3, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
       }
     }
+
+    // ---- Q = H_0 ... H_{r-1} I, accumulated backwards block by block
     {
       const int64_t most = (int64_t)pmax * pmax;
       ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
       qr_eye_kernel<<<dim3((unsigned)std::min<int64_t>(4096, (most + 1023) / 1024), n), 256, 0,
                       stream>>>(b);
     }
-    for (int k0 = ((rmax - 1) / B) * B; k0 >= 0; k0 -= B) {
-      const int rows = pmax - k0;
-      ProfScope prof(ROT_PROF_QR_APPLY, apply_flops(k0, 1), stream);
-      qr_apply_kernel<<<dim3((rows + kRows - 1) / kRows, n), 256, 0, stream>>>(b, k0, 1);
+    for (int kb0 = ((rmax - 1) / NB) * NB; kb0 >= 0; kb0 -= NB) {
+      std::vector<TransposeSeg> tr;
+      std::vector<GemmProblem> q1, q2, q3;
+      for (int i = 0; i < b.count; ++i) {
+        const QrProblem& q = b.p[i];
+        if (kb0 >= q.rmax) continue;
+        const int nb = std::min(NB, q.rmax - kb0), L = q.p - kb0;
+        const int blk = kb0 / NB;
+        const int64_t oy = (int64_t)kb0 * q.ld + kb0;
+        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, NB, nb, L, 1, 1});
+        q1.push_back(gp(nb, L, nb, q.tb.hi + (int64_t)blk * NB * NB,
+                        q.tb.lo + (int64_t)blk * NB * NB, NB, q.yt.hi, q.yt.lo, NB, q.w1t.hi,
+                        q.w1t.lo, q.ld, kEpiStoreSplit));
+        q2.push_back(gp(L, nb, L, q.qt.hi + oy, q.qt.lo + oy, q.ld, q.w1t.hi, q.w1t.lo, q.ld,
+                        q.z.hi, q.z.lo, NB, kEpiStoreSplit));
+        q3.push_back(gp(L, L, nb, q.z.hi, q.z.lo, NB, q.yt.hi, q.yt.lo, NB, q.qt.hi + oy,
+                        q.qt.lo + oy, q.ld, kEpiApplySplit, 1.f));
+      }
+      if (tr.empty()) continue;
+      if (launch_transpose(tr, stream) != ROT_OK) return ROT_ECUDA;
+      if (gemm_grouped(q1, ROT_PREC_3XTF32, status, stream) != ROT_OK) return ROT_ECUDA;
+      if (gemm_grouped(q2, ROT_PREC_3XTF32, status, stream) != ROT_OK) return ROT_ECUDA;
+      if (gemm_grouped(q3, ROT_PREC_3XTF32, status, stream) != ROT_OK) return ROT_ECUDA;
     }
     const int tiles = (pmax + 31) / 32;
     {

@@ -115,35 +115,37 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const float *MTh = F(work, x.mT_hi), *MTl = F(work, x.mT_lo);
       float *Zuh = F(work, x.zu_hi), *Zul = F(work, x.zu_lo);
       float *Zvh = F(work, x.zv_hi), *Zvl = F(work, x.zv_lo);
+      float *Auh = F(work, x.aut_hi), *Aul = F(work, x.aut_lo);
+      float *Avh = F(work, x.avt_hi), *Avl = F(work, x.avt_lo);
       if (n < m) {
         // Z_U = M^T U (n x m), stored transposed (m x n);  A_U = M Z_U
         first.push_back(gp(n, m, m, MTh, MTl, L.ldm, F(state, L.ut_hi), F(state, L.ut_lo), L.ldm,
                            Zuh, Zul, x.zu_ld, kEpiStoreSplitT));
-        second.push_back(gp(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, F(work, x.aut), nullptr,
-                            L.ldm, kEpiStoreF32T));
+        second.push_back(gp(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, Auh, Aul, L.ldm,
+                            kEpiStoreSplitT));
       } else {
         // Gram M M^T (m x m);  A_U = Gram U
         first.push_back(gp(m, m, n, Mh, Ml, L.ldn, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld,
                            kEpiStoreSplit));
         second.push_back(gp(m, m, m, Zuh, Zul, x.zu_ld, F(state, L.ut_hi), F(state, L.ut_lo),
-                            L.ldm, F(work, x.aut), nullptr, L.ldm, kEpiStoreF32T));
+                            L.ldm, Auh, Aul, L.ldm, kEpiStoreSplitT));
       }
       if (m < n) {
         // Z_V = M V (m x n), stored transposed (n x m);  A_V = M^T Z_V
         first.push_back(gp(m, n, n, Mh, Ml, L.ldn, F(state, L.vt_hi), F(state, L.vt_lo), L.ldn,
                            Zvh, Zvl, x.zv_ld, kEpiStoreSplitT));
-        second.push_back(gp(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, F(work, x.avt), nullptr,
-                            L.ldn, kEpiStoreF32T));
+        second.push_back(gp(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, Avh, Avl, L.ldn,
+                            kEpiStoreSplitT));
       } else {
         // Gram M^T M (n x n);  A_V = Gram V
         first.push_back(gp(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
                            kEpiStoreSplit));
         second.push_back(gp(n, n, n, Zvh, Zvl, x.zv_ld, F(state, L.vt_hi), F(state, L.vt_lo),
-                            L.ldn, F(work, x.avt), nullptr, L.ldn, kEpiStoreF32T));
+                            L.ldn, Avh, Avl, L.ldn, kEpiStoreSplitT));
       }
     }
-    ROT_TRY(gemm_grouped(first, ROT_PREC_3XTF32, status, s));
-    ROT_TRY(gemm_grouped(second, ROT_PREC_3XTF32, status, s));
+    ROT_TRY(gemm_grouped(first, kPrecPrecise, status, s));
+    ROT_TRY(gemm_grouped(second, kPrecPrecise, status, s));
 
     std::vector<QrProblem> qp;
     int32_t* ranks = reinterpret_cast<int32_t*>(static_cast<char*>(state) + p->ranks_off);
@@ -156,17 +158,13 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         const int pdim = side == 0 ? L.m : L.n;
         const int ld = side == 0 ? L.ldm : L.ldn;
         char* aux = static_cast<char*>(work) + (side == 0 ? x.aux_u : x.aux_v);
-        const uint64_t np = (uint64_t)((rmax + kQrPanel - 1) / kQrPanel);
         QrProblem q;
         std::memset(&q, 0, sizeof(q));
-        q.at = F(work, side == 0 ? x.aut : x.avt);
-        q.qt = F(work, side == 0 ? x.qut : x.qvt);
-        q.tf = reinterpret_cast<float*>(aux);
-        q.beta = reinterpret_cast<float*>(aux + align256(np * kQrPanel * kQrPanel * 4));
-        q.ctrl = reinterpret_cast<int*>(aux + align256(np * kQrPanel * kQrPanel * 4) +
-                                        align256((uint64_t)rmax * 4 + 4));
-        q.tau = reinterpret_cast<float*>(aux + align256(np * kQrPanel * kQrPanel * 4) +
-                                         align256((uint64_t)rmax * 4 + 4) + align256((np + 2) * 4));
+        q.at = side == 0 ? Split{F(work, x.aut_hi), F(work, x.aut_lo)}
+                         : Split{F(work, x.avt_hi), F(work, x.avt_lo)};
+        q.qt = side == 0 ? Split{F(work, x.qut_hi), F(work, x.qut_lo)}
+                         : Split{F(work, x.qvt_hi), F(work, x.qvt_lo)};
+        qr_bind_aux(q, aux, pdim, rmax);
         q.p = pdim;
         q.ld = ld;
         q.rmax = rmax;
@@ -274,8 +272,11 @@ int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void*
     return ROT_EINVAL;
   if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32) return ROT_EINVAL;
   if (!(rank_rtol >= 1e-6f && rank_rtol < 1.f)) return ROT_EINVAL;
-  for (int32_t i = 0; i < plan->count; ++i)
+  for (int32_t i = 0; i < plan->count; ++i) {
     if (!W[i] || !G[i]) return ROT_EINVAL;
+    if (refresh && (plan->shapes[i].m > kQrMaxDim || plan->shapes[i].n > kQrMaxDim))
+      return ROT_ENOTSUP;
+  }
   const int dev = check_device();
   if (dev != ROT_OK) return dev;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -40,6 +40,7 @@ enum GemmEpi : int {
   kEpiStoreF32 = 2,     // C (row-major) <- acc, float32 into c.hi
   kEpiStoreF32T = 3,    // C^T <- acc, float32 into c.hi
   kEpiApply = 4,        // C (row-major, float32 in c.hi) -= alpha * acc
+  kEpiApplySplit = 5,   // C (row-major split) <- split(hi + lo - alpha * acc)
 };
 
 struct GemmProblem {
@@ -56,6 +57,11 @@ struct GemmProblem {
   int epi;
   float alpha;
 };
+
+// Internal precision code (not in the public ABI): 3xTF32 with each K block
+// accumulated afresh and summed in float32 registers, and hi*hi kept apart
+// from the cross terms; for products whose results cancel.
+constexpr int kPrecPrecise = 4;
 
 // Upper bound on every device-side wait, in nanoseconds.
 extern uint64_t g_wait_limit_ns;
@@ -133,15 +139,22 @@ int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int
 // Batched blocked Householder QR+ (Q factor only)
 // ---------------------------------------------------------------------------
 
-constexpr int kQrPanel = 32;  // panel width b
+constexpr int kQrPanel = 32;   // panel width b
+constexpr int kQrBlock = 128;  // block-reflector width
 
 struct QrProblem {
-  float* at;    // p x ld: row j holds column j of A; overwritten by reflectors
-  float* qt;    // p x ld: receives Q^T (row j = column j of Q), float32
-  float* tf;    // ceil(rmax/b) * b * b: per-panel triangular factors
+  Split at;     // p x ld: row j holds column j of A; overwritten by reflectors
+  Split qt;     // p x ld: Q^T accumulates here
+  Split yt;     // p x kQrBlock: the current block's reflectors, transposed
+  Split w1t;    // kQrBlock x ld: (Y T)^T or (Y T^T)^T of the current block
+  Split z;      // p x kQrBlock: X (Y T) of the current block
+  float* s;     // kQrBlock x kQrBlock: Gram Y^T Y of the current block
+  Split tb;     // per block: T (kQrBlock x kQrBlock)
+  Split tbt;    // per block: T^T
+  float* tf;    // per panel: 32 x 32 triangular factor
   float* beta;  // rmax: R diagonal before the sign fix
   int* ctrl;    // [0] rank, [1] stopped flag, [2..] per-panel active counts
-  float* tau;   // numerical-rank threshold
+  float* tau;   // largest column norm of A
   int p, ld, rmax;
   // outputs (state): U (row-major) and U^T as splits, ld_out; and the rank.
   Split u;
@@ -152,7 +165,12 @@ struct QrProblem {
 int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status,
                cudaStream_t stream);
 
-// Bytes of QR scratch (tf, beta, ctrl, tau) for one problem, 256-aligned.
+// Bytes of QR scratch besides `at` and `qt` for one problem (256-aligned
+// pieces), and the binding of those pieces to a problem's pointers.
 uint64_t qr_aux_bytes(int p, int rmax);
+void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax);
+
+// Largest p the QR accepts (panel slices must fit a 16-CTA cluster).
+constexpr int kQrMaxDim = 16 * 1536;
 
 }  // namespace rot

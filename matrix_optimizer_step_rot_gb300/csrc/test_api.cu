@@ -21,8 +21,9 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
                   int32_t precision, void* work, uint64_t work_bytes, int32_t* status,
                   void* stream) {
   if (M < 1 || N < 1 || K < 1 || !A || !B || !C || !work) return ROT_EINVAL;
-  if (lda < K || ldb < K || epi < kEpiStoreSplit || epi > kEpiApply) return ROT_EINVAL;
-  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32) return ROT_EINVAL;
+  if (lda < K || ldb < K || epi < kEpiStoreSplit || epi > kEpiApplySplit) return ROT_EINVAL;
+  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 && precision != kPrecPrecise)
+    return ROT_EINVAL;
   const bool transposed = epi == kEpiStoreSplitT || epi == kEpiStoreF32T;
   if (ldc < (transposed ? M : N)) return ROT_EINVAL;
   if (work_bytes < rot_test_gemm_work_bytes(M, N, K)) return ROT_EINVAL;

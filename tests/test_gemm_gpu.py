@@ -11,7 +11,8 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [(128, 256, 32), (64, 64, 64), (300, 520, 100), (1, 40, 7), (33, 1, 65),
           (1000, 1000, 1000), (2048, 256, 4096), (130, 300, 2000)]
-TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3}
+PRECISE = 4  # the 3xTF32 variant with per-K-block float32 summation
+TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3, PRECISE: 1.5e-6}
 
 
 def tol(precision, K):
@@ -21,7 +22,7 @@ def tol(precision, K):
     bounded by a K-proportional term on top of the split's own error."""
     if precision == B.ROT_PREC_3XTF32:
         return TOL[precision] + 2.5e-8 * K
-    return TOL[precision]
+    return TOL[precision]  # TF32: input rounding dominates; precise: K-independent
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,6 +42,9 @@ def run(M, N, K, epi, precision, alpha=0.5, seed=0):
     rows, ldc = (N, M) if transposed else (M, N)
     if epi in (0, 1):
         C = torch.zeros(2 * rows * ldc, device="cuda")
+    elif epi == 5:
+        C = torch.cat([torch.rand(rows * ldc, device="cuda", generator=g),
+                       torch.zeros(rows * ldc, device="cuda")])
     else:
         C = torch.rand(rows * ldc, device="cuda", generator=g)
     C0 = C.clone()
@@ -59,6 +63,10 @@ def run(M, N, K, epi, precision, alpha=0.5, seed=0):
         assert torch.equal(hi.view(torch.int32) & 0x1FFF, torch.zeros_like(hi, dtype=torch.int32))
     elif epi == 4:
         out = (C0.double() - C.double()).view(rows, ldc) / alpha
+    elif epi == 5:
+        before = C0[:rows * ldc].double() + C0[rows * ldc:].double()
+        after = C[:rows * ldc].double() + C[rows * ldc:].double()
+        out = (before - after).view(rows, ldc) / alpha
     else:
         out = C.double().view(rows, ldc)
     if transposed:
@@ -66,7 +74,7 @@ def run(M, N, K, epi, precision, alpha=0.5, seed=0):
     return out, ref
 
 
-@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32])
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32, PRECISE])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_store_f32(M, N, K, precision):
     out, ref = run(M, N, K, 2, precision)
@@ -75,10 +83,11 @@ def test_gemm_store_f32(M, N, K, precision):
     assert err <= tol(precision, K), err
 
 
-@pytest.mark.parametrize("epi", [0, 1, 3, 4])
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, PRECISE])
+@pytest.mark.parametrize("epi", [0, 1, 3, 4, 5])
 @pytest.mark.parametrize("M,N,K", [(300, 520, 100), (64, 64, 64), (1, 40, 7)])
-def test_gemm_output_modes(M, N, K, epi):
-    out, ref = run(M, N, K, epi, B.ROT_PREC_3XTF32)
+def test_gemm_output_modes(M, N, K, epi, precision):
+    out, ref = run(M, N, K, epi, precision)
     err = (out - ref).norm() / ref.norm()
-    # the apply mode recovers the product from a difference of float32 values
-    assert err <= (1e-5 if epi == 4 else tol(B.ROT_PREC_3XTF32, K)), float(err)
+    # the apply modes recover the product from a difference of float32 values
+    assert err <= (1e-5 if epi in (4, 5) else tol(precision, K)), float(err)

@@ -95,3 +95,21 @@ def test_ragged_small_parity():
         e = rel(W[i].cpu().numpy().astype(np.float64), Wo)
         assert e <= TOL_W[B.ROT_PREC_3XTF32], (i, shapes[i], e)
         assert opt.ranks(i) == (st.rank_u, st.rank_v), (i, shapes[i])
+
+
+def test_medium_multi_block_parity():
+    """QR inputs wider than one 128-column block (several block reflectors,
+    multi-CTA panel clusters), rectangular both ways and square."""
+    shapes = ((520, 300), (300, 520), (384, 384), (1030, 260))
+    wl = inputs.Workload("medium", shapes, tuple(map(str, range(len(shapes)))), 0.02, 1e-3,
+                         "normal", 4, 2, 1 << 30, 21)
+    W, opt = run_gpu(wl, B.ROT_PREC_3XTF32)
+    ref = orc.run(wl)
+    for i in range(wl.count):
+        Wo, st = ref[i]
+        e = rel(W[i].cpu().numpy().astype(np.float64), Wo)
+        assert e <= TOL_W[B.ROT_PREC_3XTF32], (i, shapes[i], e)
+        assert opt.ranks(i) == (st.rank_u, st.rank_v), (i, shapes[i])
+        U = opt.export(i, B.ROT_WHICH_U).cpu().numpy()
+        V = opt.export(i, B.ROT_WHICH_V).cpu().numpy()
+        assert orth(U) <= TOL_ORTH and orth(V) <= TOL_ORTH, (i, orth(U), orth(V))
