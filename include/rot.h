@@ -58,6 +58,9 @@ extern "C" {
 
 #define ROT_PREC_TF32 1      /* one TF32 tensor-core product per GEMM */
 #define ROT_PREC_3XTF32 3    /* hi*hi + hi*lo + lo*hi TF32 split, ~fp32 accuracy */
+#define ROT_PREC_3XTF32_PRECISE 4 /* 3xTF32 with each K block of 32 summed in float32
+                                     registers and hi*hi kept apart from the cross
+                                     terms: float32-level accuracy at any K */
 
 #define ROT_MAX_DIM 65536
 
@@ -123,8 +126,9 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream);
  * W, G: host arrays of `count` device pointers, in input order; W[i] (m x n,
  * row-major, float32) is updated in place, G[i] is read only.  state: the
  * initialised state blob; work: the workspace blob.  refresh != 0 runs the
- * basis refresh (2) before the rotated update.  precision: ROT_PREC_TF32 or
- * ROT_PREC_3XTF32 (the basis refresh always uses 3xTF32).  rank_rtol in
+ * basis refresh (2) before the rotated update.  precision of the rotation
+ * products: ROT_PREC_TF32, ROT_PREC_3XTF32 or ROT_PREC_3XTF32_PRECISE (the
+ * basis refresh always uses ROT_PREC_3XTF32_PRECISE).  rank_rtol in
  * [1e-6, 1): the QR's numerical-rank threshold relative to the largest
  * column norm.  Non-finite inputs propagate (IEEE).
  * Errors: ROT_EINVAL (null pointers, unknown precision, rank_rtol out of

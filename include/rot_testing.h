@@ -19,15 +19,19 @@ extern "C" {
  * K)).  epi selects the output: 0 C = split(A B^T) into C (hi) and C + M*ldc
  * (lo); 1 the same for C^T (N x M, ldc >= M); 2 C = A B^T (float32); 3 C^T
  * = (A B^T)^T; 4 C -= alpha A B^T; 5 C (split) -= alpha A B^T.  precision:
- * ROT_PREC_TF32, ROT_PREC_3XTF32, or 4 for the precise 3xTF32 variant the
- * basis refresh uses (each K block of 32 summed in float32 registers, hi*hi
- * kept apart from the cross terms).  status: device int that receives ROT_ETIMEOUT if a
+ * ROT_PREC_TF32, ROT_PREC_3XTF32 or ROT_PREC_3XTF32_PRECISE (rot.h).  status: device int that receives ROT_ETIMEOUT if a
  * device-side wait gives up (may be NULL).
  * Errors: ROT_EINVAL (sizes < 1, null pointers, work too small), ROT_ECUDA. */
 int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
                   int32_t ldb, float* C, int32_t ldc, int32_t epi, float alpha,
                   int32_t precision, void* work, uint64_t work_bytes, int32_t* status,
                   void* stream);
+
+/* Failure detection check: one thread waits, with the same bounded wait the
+ * GEMM kernels use, on an mbarrier that nothing ever arrives on.  After
+ * limit_ns (<= 10 s) the wait gives up and *status (device int) becomes
+ * ROT_ETIMEOUT; the context stays usable.  Errors: ROT_EINVAL, ROT_ECUDA. */
+int rot_test_wait_timeout(uint64_t limit_ns, int32_t* status, void* stream);
 
 /* Workspace bytes rot_test_gemm needs for these sizes. */
 uint64_t rot_test_gemm_work_bytes(int32_t M, int32_t N, int32_t K);

@@ -29,6 +29,7 @@ ROT_ETOOLARGE = -7
 ROT_NOALLOC_MAX_BYTES = 64 << 20
 ROT_PREC_TF32 = 1
 ROT_PREC_3XTF32 = 3
+ROT_PREC_3XTF32_PRECISE = 4
 ROT_WHICH_M, ROT_WHICH_V2, ROT_WHICH_U, ROT_WHICH_V = 0, 1, 2, 3
 
 
@@ -71,6 +72,7 @@ _SIGS = {
     "rot_test_gemm": (_i32, [_i32, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _i32,
                              _vp, _u64, _vp, _vp]),
     "rot_test_gemm_work_bytes": (_u64, [_i32, _i32, _i32]),
+    "rot_test_wait_timeout": (_i32, [_u64, _vp, _vp]),
 }
 
 

@@ -76,8 +76,11 @@ __device__ __forceinline__ void decode(const TcBatch& b, int tile, int& pi, int&
   n0 = (local % b.p[pi].tiles_n);
 }
 
-// Waits without regard to the abort flag (used only to drain at exit).
+// Waits without regard to the abort flag (used only to drain at exit).  The
+// drain keeps waiting at least 100 ms whatever the wait limit, so that copies
+// and MMAs in flight land before the CTA's shared memory and TMEM are freed.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  limit_ns = limit_ns > 100000000ull ? limit_ns : 100000000ull;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return;
@@ -666,7 +669,29 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
   return ROT_OK;
 }
 
+__global__ void wait_timeout_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on `bar`: the bounded wait must give up
+  if (threadIdx.x == 0) {
+    const bool ok = ptx::mbar_wait(&bar, 0, &abort_flag, limit_ns);
+    if (!ok && abort_flag) atomicExch(status, ROT_ETIMEOUT);
+  }
+}
+
 }  // namespace
+
+int launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream) {
+  ProfScope prof(ROT_PROF_GEMM, 0.0, stream);
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError() == cudaSuccess ? ROT_OK : ROT_ECUDA;
+}
 
 int gemm_tc(const std::vector<GemmProblem>& probs, int precision, int* status,
             cudaStream_t stream) {

@@ -117,10 +117,17 @@ __global__ void qr_colnorm_kernel(const __grid_constant__ QrBatch b) {
 // ---------------------------------------------------------------------------
 // panel factorisation: one cluster of `cs` CTAs per matrix, columns
 // k0 .. k0+bw-1; CTA c of the cluster holds elements [k0 + c R, k0 + (c+1) R)
-// of the panel's rows in shared memory.  Per column two cluster-wide sums
-// (||x||^2 with x_0, then the 31 dot products with w) go through distributed
-// shared memory; every CTA adds the partials in the same order, so all of
-// them take the same decisions.
+// of the panel's rows in shared memory.
+//
+// One pass and one cluster-wide reduction per column: the pass that applies
+// H_j to the later columns also accumulates, for column j+1, the dot products
+// x_{j+1} . a_c with every panel row (c = j+1 gives ||x_{j+1}||^2), and the
+// thread holding element k+1 records the pivot row a_c[k+1].  Since
+// w = x - beta e_k, w . a_c = x . a_c - beta a_c[k] follows from those sums,
+// and so do the Gram entries w_i . w_j of the panel's triangular factor.
+// The 64 partial values of every CTA go to every CTA through distributed
+// shared memory; each adds them in the same order, so all of them take the
+// same decisions.
 // ---------------------------------------------------------------------------
 
 constexpr int kPanelThreads = 256;
@@ -133,14 +140,14 @@ __global__ void __launch_bounds__(kPanelThreads)
   const int crank = (int)cl.block_rank();
   const QrProblem& q = b.p[blockIdx.x / cs];
   extern __shared__ float panel[];  // [B][R]
-  __shared__ float slot_n[2][kMaxCluster][2];
-  __shared__ float slot_d[2][kMaxCluster][B];
+  __shared__ float slot[2][kMaxCluster][2 * B];
   __shared__ float red[B][kPanelThreads / 32 + 1];
-  __shared__ float s_red[kPanelThreads / 32];
+  __shared__ float sums[2 * B];  // [0, B): x_j . a_c ; [B, 2B): a_c[k]
+  __shared__ float s_piv[B];
+  __shared__ float s_coef[B];
   __shared__ float s_ww[B], s_beta[B];
   __shared__ float gram[B][B + 1];
   __shared__ float tmat[B][B + 1];
-  __shared__ float s_dot[B];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarp = nthr >> 5;
@@ -188,37 +195,58 @@ __global__ void __launch_bounds__(kPanelThreads)
       at_hi[o] = 0.f;
       at_lo[o] = 0.f;
     }
-  const float thr = rtol * q.tau[0];
-  int active = bw;
-  cl.sync();
+  if (tid < B) s_piv[tid] = 0.f;
+  __syncthreads();
 
-  for (int j = 0; j < bw; ++j) {
-    const int k = k0 + j;
-    const int par = j & 1;
-    const int lo_e = max(k, e0);
-    float* wr = panel + j * R;
-    // ||x||^2 over my elements, and x_0 if element k is mine
-    float s = 0.f;
-    for (int e = lo_e + tid; e < e1; e += nthr) s = fmaf(wr[e - e0], wr[e - e0], s);
-    s = warp_sum(s);
-    if (lane == 0) s_red[warp] = s;
+  // block-reduce acc[] (and the pivot row) for column `jn`, exchange with the
+  // cluster through slot[par], and leave the totals in sums[]
+  auto reduce_and_share = [&](float (&acc)[B], int par) {
+    const float part = warp_transpose_sum(acc);
+    red[lane][warp] = part;
     __syncthreads();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < nwarp; ++w) t += s_red[w];
-      const float xk = (k >= e0 && k < e1) ? wr[k - e0] : 0.f;
-      for (int c = 0; c < cs; ++c) {
-        float* dst = cl.map_shared_rank(&slot_n[par][crank][0], c);
-        dst[0] = t;
-        dst[1] = xk;
+    if (tid < 2 * B) {
+      float t;
+      if (tid < B) {
+        t = 0.f;
+        for (int w = 0; w < nwarp; ++w) t += red[tid][w];
+      } else {
+        t = s_piv[tid - B];
       }
+      for (int c = 0; c < cs; ++c) *cl.map_shared_rank(&slot[par][crank][tid], c) = t;
     }
     cl.sync();
-    float sn = 0.f, x0 = 0.f;
-    for (int c = 0; c < cs; ++c) {
-      sn += slot_n[par][c][0];
-      x0 += slot_n[par][c][1];
+    if (tid < 2 * B) {
+      float t = 0.f;
+      for (int c = 0; c < cs; ++c) t += slot[par][c][tid];
+      sums[tid] = t;
+      if (tid >= B) s_piv[tid - B] = 0.f;
     }
+    __syncthreads();
+  };
+
+  // sums for column 0: x_0 . a_c over my elements >= k0, pivot row a_c[k0]
+  {
+    float acc[B];
+#pragma unroll
+    for (int c = 0; c < B; ++c) acc[c] = 0.f;
+    for (int e = e0 + tid; e < e1; e += nthr) {
+      const float xn = panel[e - e0];
+#pragma unroll
+      for (int c = 0; c < B; ++c)
+        if (c < bw) acc[c] = fmaf(xn, panel[c * R + (e - e0)], acc[c]);
+      if (e == k0)
+        for (int c = 0; c < bw; ++c) s_piv[c] = panel[c * R + (e - e0)];
+    }
+    __syncthreads();
+    reduce_and_share(acc, 0);
+  }
+
+  const float thr = rtol * q.tau[0];
+  int active = bw;
+  for (int j = 0; j < bw; ++j) {
+    const int k = k0 + j;
+    const float sn = sums[j];
+    const float x0 = sums[B + j];
     const float nx = sqrtf(sn);
     if (nx <= thr) {  // numerical rank reached: H_k .. are identities
       active = j;
@@ -227,45 +255,40 @@ __global__ void __launch_bounds__(kPanelThreads)
     const float beta = x0 >= 0.f ? -nx : nx;
     const float w0 = x0 - beta;
     const float ww = 2.f * fmaf(fabsf(x0), nx, sn);  // ||x - beta e0||^2, no cancellation
+    if (tid < bw && tid != j) {
+      const float d = sums[tid] - beta * sums[B + tid];  // w_j . a_c
+      if (tid < j) gram[tid][j] = d;
+      else s_coef[tid] = 2.f * d / ww;
+    }
     if (tid == 0) {
-      if (k >= e0 && k < e1) wr[k - e0] = w0;
       s_ww[j] = ww;
       s_beta[j] = beta;
+      if (k >= e0 && k < e1) panel[j * R + (k - e0)] = w0;
     }
     __syncthreads();
+    if (j + 1 == bw) break;  // nothing after the last column
 
-    // dots of w with the other panel rows over my elements >= k
+    // apply H_k to columns j+1.. (my elements >= k) and accumulate column
+    // j+1's sums over my elements >= k+1
     float acc[B];
 #pragma unroll
     for (int c = 0; c < B; ++c) acc[c] = 0.f;
-    for (int e = lo_e + tid; e < e1; e += nthr) {
-      const float we = wr[e - e0];
+    const float* wr = panel + j * R;
+    for (int e = max(k, e0) + tid; e < e1; e += nthr) {
+      const int o = e - e0;
+      const float we = wr[o];
+      for (int c = j + 1; c < bw; ++c) panel[c * R + o] -= s_coef[c] * we;
+      if (e > k) {
+        const float xn = panel[(j + 1) * R + o];
 #pragma unroll
-      for (int c = 0; c < B; ++c)
-        if (c < bw && c != j) acc[c] = fmaf(we, panel[c * R + (e - e0)], acc[c]);
-    }
-    const float part = warp_transpose_sum(acc);
-    red[lane][warp] = part;
-    __syncthreads();
-    if (tid < B) {
-      float t = 0.f;
-      for (int w = 0; w < nwarp; ++w) t += red[tid][w];
-      for (int c = 0; c < cs; ++c) *cl.map_shared_rank(&slot_d[par][crank][tid], c) = t;
-    }
-    cl.sync();
-    if (tid < B) {
-      float t = 0.f;
-      for (int c = 0; c < cs; ++c) t += slot_d[par][c][tid];
-      s_dot[tid] = t;
-      if (tid < j) gram[tid][j] = t;
+        for (int c = 0; c < B; ++c)
+          if (c < bw) acc[c] = fmaf(xn, panel[c * R + o], acc[c]);
+        if (e == k + 1)
+          for (int c = 0; c < bw; ++c) s_piv[c] = panel[c * R + o];
+      }
     }
     __syncthreads();
-    // apply H_k to the remaining panel rows (my elements >= k)
-    for (int e = lo_e + tid; e < e1; e += nthr) {
-      const float we = wr[e - e0];
-      for (int c = j + 1; c < bw; ++c) panel[c * R + (e - e0)] -= (2.f * s_dot[c] / ww) * we;
-    }
-    __syncthreads();
+    reduce_and_share(acc, (j + 1) & 1);
   }
 
   // zero the R entries inside the panel (elements < k of reflector row k)
@@ -540,8 +563,9 @@ GemmProblem gp(int M, int N, int K, const float* ah, const float* al, int lda, c
   return P;
 }
 
-int launch_panel(const QrBatch& b, int k0, float rtol, int cs, int R, cudaStream_t stream) {
-  const size_t smem = sizeof(float) * (size_t)B * R;
+int panel_slice(int pmax, int cs) { return ((pmax + cs - 1) / cs + 3) / 4 * 4; }
+
+int configure_panel(size_t smem) {
   static size_t configured = 0;
   if (smem > configured) {
     if (cudaFuncSetAttribute(qr_panel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -551,6 +575,45 @@ int launch_panel(const QrBatch& b, int k0, float rtol, int cs, int R, cudaStream
       return ROT_ECUDA;
     configured = smem;
   }
+  return ROT_OK;
+}
+
+// Cluster size for the panel kernel: at least enough CTAs that a slice of
+// the panel fits in shared memory (<= 1536 elements x 32 rows = 192 KB); then
+// the largest size (up to 16, each CTA keeping >= 256 elements) at which
+// every cluster of the batch can be resident at once.
+int pick_cluster(int count, int pmax, int sms) {
+  const int lo = std::max(1, (pmax + 1535) / 1536);
+  int best = std::min(lo, kMaxCluster);
+  for (int cs = best; cs <= kMaxCluster; ++cs) {
+    if (cs > lo && pmax / cs < 256) break;
+    if (cs * count > sms) break;
+    const size_t smem = sizeof(float) * (size_t)B * panel_slice(pmax, cs);
+    if (configure_panel(smem) != ROT_OK) break;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(count * cs));
+    cfg.blockDim = dim3(kPanelThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, qr_panel_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      break;
+    }
+    if (clusters >= count) best = cs;
+  }
+  return best;
+}
+
+int launch_panel(const QrBatch& b, int k0, float rtol, int cs, int R, cudaStream_t stream) {
+  const size_t smem = sizeof(float) * (size_t)B * R;
+  if (configure_panel(smem) != ROT_OK) return ROT_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(b.count * cs));
   cfg.blockDim = dim3(kPanelThreads);
@@ -633,13 +696,8 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       pmax = std::max(pmax, b.p[i].p);
     }
     const unsigned n = (unsigned)b.count;
-    // cluster size: enough CTAs that a panel slice fits in shared memory
-    // (<= 1536 elements x 32 rows = 192 KB), more while free SMs allow it and
-    // each CTA keeps >= 256 elements
-    int cs = std::max(1, (pmax + 1535) / 1536);
-    while (cs < kMaxCluster && (cs + 1) * b.count <= sms && pmax / (cs + 1) >= 256) ++cs;
-    cs = std::min(cs, kMaxCluster);
-    const int R = ((pmax + cs - 1) / cs + 3) / 4 * 4;
+    const int cs = pick_cluster(b.count, pmax, sms);
+    const int R = panel_slice(pmax, cs);
     {
       ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
       qr_init_kernel<<<n, 64, 0, stream>>>(b);
@@ -735,9 +793,10 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       }
       if (tr.empty()) continue;
       if (launch_transpose(tr, stream) != ROT_OK) return ROT_ECUDA;
-      if (gemm_grouped(q1, ROT_PREC_3XTF32, status, stream) != ROT_OK) return ROT_ECUDA;
-      if (gemm_grouped(q2, ROT_PREC_3XTF32, status, stream) != ROT_OK) return ROT_ECUDA;
-      if (gemm_grouped(q3, ROT_PREC_3XTF32, status, stream) != ROT_OK) return ROT_ECUDA;
+      // precise: Q's orthogonality error adds up over all p^2 entries
+      if (gemm_grouped(q1, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+      if (gemm_grouped(q2, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+      if (gemm_grouped(q3, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
     }
     const int tiles = (pmax + 31) / 32;
     {

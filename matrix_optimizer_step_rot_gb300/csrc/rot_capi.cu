@@ -270,7 +270,9 @@ int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void*
   if (!W || !G || !state || !work) return ROT_EINVAL;
   if ((reinterpret_cast<uintptr_t>(state) & 255) || (reinterpret_cast<uintptr_t>(work) & 255))
     return ROT_EINVAL;
-  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32) return ROT_EINVAL;
+  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
+      precision != ROT_PREC_3XTF32_PRECISE)
+    return ROT_EINVAL;
   if (!(rank_rtol >= 1e-6f && rank_rtol < 1.f)) return ROT_EINVAL;
   for (int32_t i = 0; i < plan->count; ++i) {
     if (!W[i] || !G[i]) return ROT_EINVAL;

@@ -58,10 +58,10 @@ struct GemmProblem {
   float alpha;
 };
 
-// Internal precision code (not in the public ABI): 3xTF32 with each K block
-// accumulated afresh and summed in float32 registers, and hi*hi kept apart
-// from the cross terms; for products whose results cancel.
-constexpr int kPrecPrecise = 4;
+// 3xTF32 with each K block accumulated afresh and summed in float32
+// registers, hi*hi kept apart from the cross terms (ROT_PREC_3XTF32_PRECISE);
+// used for products whose results cancel.
+constexpr int kPrecPrecise = ROT_PREC_3XTF32_PRECISE;
 
 // Upper bound on every device-side wait, in nanoseconds.
 extern uint64_t g_wait_limit_ns;

@@ -4,6 +4,10 @@
 
 using namespace rot;
 
+namespace rot {
+int launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
+}
+
 namespace {
 uint64_t split_bytes(int64_t rows, int64_t ld) { return align256(4ull * rows * ld); }
 }  // namespace
@@ -22,7 +26,8 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
                   void* stream) {
   if (M < 1 || N < 1 || K < 1 || !A || !B || !C || !work) return ROT_EINVAL;
   if (lda < K || ldb < K || epi < kEpiStoreSplit || epi > kEpiApplySplit) return ROT_EINVAL;
-  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 && precision != kPrecPrecise)
+  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
+      precision != ROT_PREC_3XTF32_PRECISE)
     return ROT_EINVAL;
   const bool transposed = epi == kEpiStoreSplitT || epi == kEpiStoreF32T;
   if (ldc < (transposed ? M : N)) return ROT_EINVAL;
@@ -49,13 +54,20 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
   P.b_lo = b_lo;
   P.ldb = ldk;
   P.c_hi = C;
-  P.c_lo = (epi == kEpiStoreSplit) ? C + (int64_t)M * ldc
-           : (epi == kEpiStoreSplitT) ? C + (int64_t)N * ldc
-                                      : nullptr;
+  // split outputs keep lo right after hi: M x ldc rows, or N x ldc for C^T
+  P.c_lo = (epi == kEpiStoreSplit || epi == kEpiApplySplit) ? C + (int64_t)M * ldc
+           : (epi == kEpiStoreSplitT)                       ? C + (int64_t)N * ldc
+                                                            : nullptr;
   P.ldc = ldc;
   P.epi = epi;
   P.alpha = alpha;
   return gemm_grouped({P}, precision, reinterpret_cast<int*>(status), s);
+}
+
+int rot_test_wait_timeout(uint64_t limit_ns, int32_t* status, void* stream) {
+  if (!status || limit_ns > 10000000000ull) return ROT_EINVAL;
+  return launch_wait_timeout(limit_ns, reinterpret_cast<int*>(status),
+                             static_cast<cudaStream_t>(stream));
 }
 
 uint64_t rot_set_wait_timeout_ns(uint64_t ns) {

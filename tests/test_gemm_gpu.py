@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [(128, 256, 32), (64, 64, 64), (300, 520, 100), (1, 40, 7), (33, 1, 65),
           (1000, 1000, 1000), (2048, 256, 4096), (130, 300, 2000)]
-PRECISE = 4  # the 3xTF32 variant with per-K-block float32 summation
+PRECISE = B.ROT_PREC_3XTF32_PRECISE
 TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3, PRECISE: 1.5e-6}
 
 
