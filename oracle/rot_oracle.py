@@ -34,8 +34,10 @@ fusion, no reordering beyond what the definitions allow.
 
 from __future__ import annotations
 
+import ctypes
 import dataclasses
-from typing import Dict, List, Optional, Sequence, Tuple
+import os
+from typing import Callable, Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -158,6 +160,43 @@ def hqr_plus(A: np.ndarray, rank_rtol: float) -> Tuple[np.ndarray, int, np.ndarr
     return Q, r, np.array(betas)
 
 
+_C = None
+
+
+def _c_lib():
+    """The C build of the same QR+ (oracle/hqr.c), or None if not built."""
+    global _C
+    if _C is None:
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhqr.so")
+        if not os.path.exists(path):
+            return None
+        lib = ctypes.CDLL(path)
+        lib.hqr_plus_f64.restype = ctypes.c_long
+        lib.hqr_plus_f64.argtypes = [ctypes.c_long, ctypes.c_void_p, ctypes.c_double,
+                                     ctypes.c_void_p, ctypes.c_void_p]
+        _C = lib
+    return _C
+
+
+def hqr_plus_c(A: np.ndarray, rank_rtol: float) -> Tuple[np.ndarray, int, np.ndarray]:
+    """hqr_plus() computed by oracle/hqr.c (same steps, column-major C loops)."""
+    lib = _c_lib()
+    if lib is None:
+        raise RuntimeError("oracle/libhqr.so is not built (oracle/build_oracle.py)")
+    p = A.shape[0]
+    a = np.array(A, dtype=np.float64, order="F", copy=True)
+    Q = np.empty((p, p), dtype=np.float64, order="F")
+    beta = np.zeros(max(p, 1), dtype=np.float64)
+    r = lib.hqr_plus_f64(p, a.ctypes.data, float(rank_rtol), Q.ctypes.data, beta.ctypes.data)
+    if r < 0:
+        raise MemoryError("hqr_plus_f64")
+    return np.ascontiguousarray(Q), int(r), beta[:r].copy()
+
+
+def default_qr():
+    return hqr_plus_c if _c_lib() is not None else hqr_plus
+
+
 # ---------------------------------------------------------------------------
 # One optimizer step for one matrix
 # ---------------------------------------------------------------------------
@@ -177,17 +216,26 @@ def init_state(m: int, n: int) -> MatrixState:
     return MatrixState(M=np.zeros((m, n)), v=np.zeros((m, n)), U=np.eye(m), V=np.eye(n))
 
 
-def refresh_basis(M: np.ndarray, U: np.ndarray, V: np.ndarray, rank_rtol: float):
-    """One subspace-iteration step on each side: U <- QR+(M M^T U), V <- QR+(M^T M V)."""
+def refresh_basis(M: np.ndarray, U: np.ndarray, V: np.ndarray, rank_rtol: float,
+                  qr: Optional[Callable] = None, perturb: Optional[Callable] = None):
+    """One subspace-iteration step on each side: U <- QR+(M M^T U), V <- QR+(M^T M V).
+
+    `qr` picks the QR+ implementation (default: the C build if present);
+    `perturb`, used only to measure the method's sensitivity, maps each QR
+    input to a perturbed copy."""
+    qr = qr or default_qr()
     A_U = M @ (M.T @ U)
     A_V = M.T @ (M @ V)
-    U_new, r_u, _ = hqr_plus(A_U, rank_rtol)
-    V_new, r_v, _ = hqr_plus(A_V, rank_rtol)
+    if perturb is not None:
+        A_U, A_V = perturb(A_U), perturb(A_V)
+    U_new, r_u, _ = qr(A_U, rank_rtol)
+    V_new, r_v, _ = qr(A_V, rank_rtol)
     return U_new, V_new, r_u, r_v
 
 
 def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: float,
-         eps: float, lr: float, refresh: bool, rank_rtol: float) -> np.ndarray:
+         eps: float, lr: float, refresh: bool, rank_rtol: float,
+         perturb: Optional[Callable] = None) -> np.ndarray:
     """One rotated-Adam step; updates `st` in place and returns the new W (float64).
 
     (1) M <- beta1 M + (1 - beta1) G
@@ -198,7 +246,8 @@ def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: flo
     G = np.asarray(G, dtype=np.float64)
     st.M = beta1 * st.M + (1.0 - beta1) * G
     if refresh:
-        st.U, st.V, st.rank_u, st.rank_v = refresh_basis(st.M, st.U, st.V, rank_rtol)
+        st.U, st.V, st.rank_u, st.rank_v = refresh_basis(st.M, st.U, st.V, rank_rtol,
+                                                         perturb=perturb)
     Gt = (st.U.T @ G) @ st.V
     Mt = (st.U.T @ st.M) @ st.V
     st.v = beta2 * st.v + (1.0 - beta2) * (Gt * Gt)
@@ -211,11 +260,17 @@ def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: flo
 # ---------------------------------------------------------------------------
 
 def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
-        first_step: int = 1) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
+        first_step: int = 1, perturb_seed: Optional[int] = None,
+        perturb_rel: float = 2.0 ** -22) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
     """Run `steps` steps (default: the workload's) for the chosen matrices.
 
     `wl` is a workload object exposing shapes, hyper, refresh(t), w0(i) and
     grad(i, t).  Returns {i: (W, state)} with W in float64.
+
+    With perturb_seed set, every QR input is multiplied element-wise by
+    (1 + perturb_rel * xi), xi ~ N(0, 1): the same method run on inputs that
+    differ at float32 rounding level.  How far that moves W is the method's
+    own sensitivity (its floor for any float32 implementation).
     """
     items = list(range(wl.count)) if items is None else list(items)
     steps = wl.steps if steps is None else steps
@@ -225,11 +280,26 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         m, n = wl.shapes[i]
         W = wl.w0(i).astype(np.float64)
         st = init_state(m, n)
+        perturb = None
+        if perturb_seed is not None:
+            rng = np.random.default_rng([perturb_seed, i])
+            perturb = lambda A, rng=rng: A * (1.0 + perturb_rel * rng.standard_normal(A.shape))
         for t in range(first_step, first_step + steps):
             W = step(W, wl.grad(i, t), st, h.beta1, h.beta2, h.eps, h.lr, wl.refresh(t),
-                     h.rank_rtol)
+                     h.rank_rtol, perturb=perturb)
         out[i] = (W, st)
     return out
+
+
+def floor(wl, item: int, W_ref: np.ndarray, seeds: Sequence[int] = (1, 2, 3),
+          steps: Optional[int] = None) -> float:
+    """Largest relative change of the final W over runs whose QR inputs are
+    perturbed at float32 level (see run())."""
+    worst = 0.0
+    for s in seeds:
+        Wp, _ = run(wl, [item], steps=steps, perturb_seed=s)[item]
+        worst = max(worst, float(np.linalg.norm(Wp - W_ref) / np.linalg.norm(W_ref)))
+    return worst
 
 
 def orthogonality_error(Q: np.ndarray) -> float:

@@ -6,8 +6,12 @@ import itertools
 import numpy as np
 import pytest
 
+from oracle import build_oracle
 from oracle import rot_oracle as orc
 from matrix_optimizer_step_rot_gb300 import inputs
+
+build_oracle.build()
+QR_IMPLS = [orc.hqr_plus, orc.hqr_plus_c]
 
 H = inputs.Hyper()
 B1, B2, EPS, LR = H.beta1, H.beta2, H.eps, H.lr
@@ -93,10 +97,11 @@ def test_rotation_directions_closed_form():
 # P4: Householder QR+ against LAPACK (numpy.linalg.qr)
 # --------------------------------------------------------------------------
 
+@pytest.mark.parametrize("qr", QR_IMPLS)
 @pytest.mark.parametrize("p", [1, 2, 8, 33, 64])
-def test_hqr_full_rank_matches_lapack_with_sign_fix(p):
+def test_hqr_full_rank_matches_lapack_with_sign_fix(p, qr):
     A = rng(10 + p).normal(size=(p, p))
-    Q, r, beta = orc.hqr_plus(A, 1e-3)
+    Q, r, beta = qr(A, 1e-3)
     assert r == p
     Qn, Rn = np.linalg.qr(A)
     Qn = Qn * np.sign(np.diag(Rn))[None, :]
@@ -108,14 +113,15 @@ def test_hqr_full_rank_matches_lapack_with_sign_fix(p):
     assert np.abs(np.tril(R, -1)).max() <= 1e-12 * np.abs(A).max() * p
 
 
+@pytest.mark.parametrize("qr", QR_IMPLS)
 @pytest.mark.parametrize("p,rk", [(6, 2), (17, 5), (40, 39)])
-def test_hqr_rank_deficient_completion_matches_lapack(p, rk):
+def test_hqr_rank_deficient_completion_matches_lapack(p, rk, qr):
     """A = [B | 0]: LAPACK's reflectors for the zero columns are identities, so
     its complete Q is H_0..H_{r-1} I, the completion the numerical-rank stop uses.
     The opposite reflector sign convention would give a different completion."""
     B = rng(20 + p).normal(size=(p, rk))
     A = np.hstack([B, np.zeros((p, p - rk))])
-    Q, r, beta = orc.hqr_plus(A, 1e-3)
+    Q, r, beta = qr(A, 1e-3)
     assert r == rk
     Qn, Rn = np.linalg.qr(A, mode="complete")
     signs = np.ones(p)
@@ -124,14 +130,15 @@ def test_hqr_rank_deficient_completion_matches_lapack(p, rk):
     assert orc.orthogonality_error(Q) <= 1e-12
 
 
-def test_hqr_rank_one_closed_form_completion():
+@pytest.mark.parametrize("qr", QR_IMPLS)
+def test_hqr_rank_one_closed_form_completion(qr):
     """Rank one: a single reflector; every column is written out by hand."""
     p = 9
     a = rng(30).normal(size=p)
     a[0] = -abs(a[0])                       # exercise the negative-x0 branch
     c = rng(31).normal(size=p)
     A = np.outer(a, c)
-    Q, r, beta = orc.hqr_plus(A, 1e-6)
+    Q, r, beta = qr(A, 1e-6)
     assert r == 1
     x = A[:, 0]
     nx = np.linalg.norm(x)
@@ -147,9 +154,23 @@ def test_hqr_rank_one_closed_form_completion():
     np.testing.assert_allclose(Q[:, 0], np.sign(c[0]) * a / np.linalg.norm(a), atol=1e-13)
 
 
-def test_hqr_zero_matrix_is_identity():
-    Q, r, _ = orc.hqr_plus(np.zeros((5, 5)), 1e-3)
+@pytest.mark.parametrize("qr", QR_IMPLS)
+def test_hqr_zero_matrix_is_identity(qr):
+    Q, r, _ = qr(np.zeros((5, 5)), 1e-3)
     assert r == 0 and np.array_equal(Q, np.eye(5))
+
+
+def test_c_qr_matches_numpy_definition_on_refresh_inputs():
+    """The C build follows the numpy definition step for step (rounding order
+    aside) on Gram-type inputs with a rank stop inside, as the refresh makes."""
+    for m, n, seed in [(70, 40, 1), (40, 70, 2), (96, 96, 3)]:
+        M = rng(seed).normal(size=(m, n))
+        for A in (M @ M.T, M.T @ M):
+            Qn, rn, bn = orc.hqr_plus(A, 1e-3)
+            Qc, rc, bc = orc.hqr_plus_c(A, 1e-3)
+            assert rn == rc
+            np.testing.assert_allclose(Qc, Qn, rtol=0, atol=1e-11)
+            np.testing.assert_allclose(bc, bn, rtol=1e-12, atol=0)
 
 
 # --------------------------------------------------------------------------
