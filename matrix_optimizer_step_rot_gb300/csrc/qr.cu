@@ -11,9 +11,9 @@
 //
 // Storage: the input arrives transposed and split (row j of `at` = column j
 // of A, as hi + lo), so a column and a reflector are contiguous.  Reflector k
-// overwrites row k from element k on (w_0 at the diagonal, the tail of x
-// after it); the R entries the factorisation leaves in front of it are
-// zeroed, so rows of `at` serve directly as the reflector matrix Y^T.
+// overwrites row k from element k on, normalised to unit length (v = w/||w||,
+// H_k = I - 2 v v^T); the R entries the factorisation leaves in front of it
+// are zeroed, so rows of `at` serve directly as the reflector matrix Y^T.
 //
 // Blocking (compact WY: Schreiber & Van Loan, "A storage-efficient WY
 // representation for products of Householder transformations", 1989; Golub &
@@ -291,12 +291,17 @@ __global__ void __launch_bounds__(kPanelThreads)
     reduce_and_share(acc, (j + 1) & 1);
   }
 
-  // zero the R entries inside the panel (elements < k of reflector row k)
-  // and the rows past the rank; write my slice back as a split
+  // Reflectors are stored normalised, v = w / ||w|| (H = I - 2 v v^T), so the
+  // triangular factors and Gram matrices built from them are well scaled
+  // whatever the column norms were.  Zero the R entries inside the panel
+  // (elements < k of reflector row k) and the rows past the rank; write my
+  // slice back as a split.
+  if (tid < B) s_coef[tid] = tid < active ? 1.f / sqrtf(s_ww[tid]) : 0.f;
+  __syncthreads();
   for (int i = tid; i < bw * R; i += nthr) {
     const int j = i / R, e = e0 + i % R;
     if (e >= e1) continue;
-    float x = panel[i];
+    float x = panel[i] * s_coef[j];
     if (j >= active || e < k0 + j) x = 0.f;
     float h, l;
     split_tf32(x, h, l);
@@ -306,15 +311,17 @@ __global__ void __launch_bounds__(kPanelThreads)
   }
 
   if (crank == 0) {
-    // panel factor T: T_jj = 2 / ww_j ; T[0:j, j] = -T_jj * T[0:j, 0:j] * gram[0:j, j]
+    // panel factor T of the normalised reflectors: T_jj = 2,
+    // T[0:j, j] = -2 T[0:j, 0:j] (v_{0:j}^T v_j), v_l . v_j = gram[l][j] / (||w_l|| ||w_j||)
     if (warp == 0) {
       for (int i = lane; i < B * (B + 1); i += 32) (&tmat[0][0])[i] = 0.f;
       __syncwarp();
       for (int j = 0; j < active; ++j) {
-        const float tjj = 2.f / s_ww[j];
+        const float tjj = 2.f;
         float t = 0.f;
         if (lane < j)
-          for (int l = lane; l < j; ++l) t = fmaf(tmat[lane][l], gram[l][j], t);
+          for (int l = lane; l < j; ++l)
+            t = fmaf(tmat[lane][l], gram[l][j] * s_coef[l] * s_coef[j], t);
         __syncwarp();
         if (lane < j) tmat[lane][j] = -tjj * t;
         if (lane == j) tmat[j][j] = tjj;
