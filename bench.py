@@ -244,12 +244,12 @@ def run_ours(args):
         dist.barrier()
 
     # ---- end to end through the public API with host buffers
-    g_host = [g.cpu().pin_memory() for g in Gsets[0]]
-    w_host = [w.cpu().pin_memory() for w in W]
-    g_dev = [torch.empty_like(g) for g in Gsets[0]]
+    e_steps = 0 if args.no_e2e else max(1, min(args.steps, 5))
+    g_host = [g.cpu().pin_memory() for g in Gsets[0]] if e_steps else []
+    w_host = [w.cpu().pin_memory() for w in W] if e_steps else []
+    g_dev = [torch.empty_like(g) for g in Gsets[0]] if e_steps else []
     h2d = sum(g.numel() * 4 for g in g_host)
     d2h = sum(w.numel() * 4 for w in w_host)
-    e_steps = max(1, min(args.steps, 5))
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -264,12 +264,12 @@ def run_ours(args):
             wh.copy_(wd, non_blocking=True)
     x1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = x0.elapsed_time(x1)
+    e2e_ms = x0.elapsed_time(x1) if e_steps else 0.0
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
-    e2e_sched = schedule(wl, t - e_steps + 1, e_steps)
+    e2e_sched = schedule(wl, t - e_steps + 1, e_steps) if e_steps else []
 
     if rank == 0:
         peaks, peak_kind = load_peaks()
@@ -322,7 +322,7 @@ def run_ours(args):
             },
             "elementwise_hbm": {"achieved_gbs": ew_gbs, "peak_gbs": hbm,
                                 "frac": ew_gbs / hbm if ew_gbs else None},
-            "e2e": {"value": world * wl.count * e_steps / (e2e_ms / 1000.0), "unit": UNIT,
+            "e2e": None if not e_steps else {"value": world * wl.count * e_steps / (e2e_ms / 1000.0), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e_steps, "refresh_steps": sum(e2e_sched)},
             "gpu_launches": launches,
@@ -394,6 +394,7 @@ def main():
     ap.add_argument("--workload", default="full", choices=list(inputs.WORKLOADS))
     ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "tf32", "3xtf32-precise"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

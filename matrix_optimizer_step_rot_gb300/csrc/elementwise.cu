@@ -67,7 +67,7 @@ __global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b,
     split_tf32(m, h, l);
     s.m_hi[o] = h;
     s.m_lo[o] = l;
-    split_tf32(g, h, l);
+    split_tf32_mma(g, h, l);
     s.g_hi[o] = h;
     s.g_lo[o] = l;
   }
@@ -87,7 +87,7 @@ __global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float b
     s.v[o] = v;
     const float d = s.mt[o] / (sqrtf(v) + eps);
     float h, l;
-    split_tf32(d, h, l);
+    split_tf32_mma(d, h, l);
     s.d_hi[o] = h;
     s.d_lo[o] = l;
   }
@@ -122,7 +122,11 @@ __global__ void transpose_kernel(const __grid_constant__ SegBatch<TransposeSeg> 
         const int64_t o = (int64_t)c * s.ld_dst + r;
         if (s.dst_is_split) {
           float h, l;
-          split_tf32(v, h, l);
+          if (s.dst_mma_only) {
+            split_tf32_mma(v, h, l);
+          } else {
+            split_tf32(v, h, l);
+          }
           s.d_hi[o] = h;
           s.d_lo[o] = l;
         } else {
@@ -153,7 +157,7 @@ __global__ void split_kernel(const __grid_constant__ SegBatch<SplitSeg> b) {
        e += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
     float h, l;
-    split_tf32(s.src[(int64_t)r * s.ld_src + c], h, l);
+    split_tf32_mma(s.src[(int64_t)r * s.ld_src + c], h, l);
     const int64_t o = (int64_t)r * s.ld_dst + c;
     s.hi[o] = h;
     s.lo[o] = l;

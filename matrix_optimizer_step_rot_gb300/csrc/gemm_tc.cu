@@ -46,6 +46,7 @@ struct TcProblem {
   int epi;
   int ldc;
   float alpha;
+  int mma_only;
   float* c_hi;
   float* c_lo;
 };
@@ -106,7 +107,11 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
           const int64_t o = (int64_t)(col0 + t) * P.ldc + row;
           if (split) {
             float h, l;
-            split_tf32(v, h, l);
+            if (P.mma_only) {
+              split_tf32_mma(v, h, l);
+            } else {
+              split_tf32(v, h, l);
+            }
             P.c_hi[o] = h;
             P.c_lo[o] = l;
           } else {
@@ -133,7 +138,11 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
           for (int u = 0; u < 4; ++u) {
             const float v = __uint_as_float(r[t + u]);
             if (split) {
-              split_tf32(v, hp[u], lp[u]);
+              if (P.mma_only) {
+                split_tf32_mma(v, hp[u], lp[u]);
+              } else {
+                split_tf32(v, hp[u], lp[u]);
+              }
             } else {
               hp[u] = v;
             }
@@ -148,7 +157,11 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
             const float v = __uint_as_float(r[t]);
             if (split) {
               float h, l;
-              split_tf32(v, h, l);
+              if (P.mma_only) {
+                split_tf32_mma(v, h, l);
+              } else {
+                split_tf32(v, h, l);
+              }
               hi[t] = h;
               lo[t] = l;
             } else {
@@ -649,6 +662,7 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
       P.epi = G.epi;
       P.ldc = G.ldc;
       P.alpha = G.alpha;
+      P.mma_only = G.mma_only;
       P.c_hi = G.c_hi;
       P.c_lo = G.c_lo;
       total += ((G.M + BM - 1) / BM) * P.tiles_n;

@@ -481,10 +481,10 @@ __global__ void __launch_bounds__(NB) qr_tblock_kernel(const __grid_constant__ Q
   for (int i = tid; i < NB * NB; i += blockDim.x) {
     const int r = i / NB, c = i % NB;
     float h, l;
-    split_tf32(tsm[r * LD + c], h, l);
+    split_tf32_mma(tsm[r * LD + c], h, l);
     th[i] = h;
     tl[i] = l;
-    split_tf32(tsm[c * LD + r], h, l);
+    split_tf32_mma(tsm[c * LD + r], h, l);
     uh[i] = h;
     ul[i] = l;
   }
@@ -522,7 +522,7 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
         v = q.qt.hi[oi] + q.qt.lo[oi];
         if (r < rank && q.beta[r] < 0.f) v = -v;  // row r of Q^T = column r of Q
         float h, l;
-        split_tf32(v, h, l);
+        split_tf32_mma(v, h, l);  // the bases feed only tensor cores
         const int64_t o = (int64_t)r * q.ld_out + c;
         q.ut.hi[o] = h;
         q.ut.lo[o] = l;
@@ -534,7 +534,7 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
       const int r = c0 + i, c = r0 + tx;  // U[r][c] = Q^T[c][r]
       if (r < q.p && c < q.p) {
         float h, l;
-        split_tf32(tile[tx][i], h, l);
+        split_tf32_mma(tile[tx][i], h, l);
         const int64_t o = (int64_t)r * q.ld_out + c;
         q.u.hi[o] = h;
         q.u.lo[o] = l;
@@ -551,8 +551,9 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
 
 GemmProblem gp(int M, int N, int K, const float* ah, const float* al, int lda, const float* bh,
                const float* bl, int ldb, float* ch, float* cl, int ldc, int epi,
-               float alpha = 0.f) {
+               float alpha = 0.f, int mma_only = 0) {
   GemmProblem P;
+  P.mma_only = mma_only;
   P.M = M;
   P.N = N;
   P.K = K;
@@ -756,12 +757,12 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
         const int nb = NB, L = q.p - kb0, nr = q.rmax - kend;
         const int blk = kb0 / NB;
         const int64_t oy = (int64_t)kb0 * q.ld + kb0, ox = (int64_t)kend * q.ld + kb0;
-        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, NB, nb, L, 1, 1});
+        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, NB, nb, L, 1, 1, 1});
         f1.push_back(gp(nb, L, nb, q.tbt.hi + (int64_t)blk * NB * NB,
                         q.tbt.lo + (int64_t)blk * NB * NB, NB, q.yt.hi, q.yt.lo, NB, q.w1t.hi,
-                        q.w1t.lo, q.ld, kEpiStoreSplit));
+                        q.w1t.lo, q.ld, kEpiStoreSplit, 0.f, 1));
         f2.push_back(gp(nr, nb, L, q.at.hi + ox, q.at.lo + ox, q.ld, q.w1t.hi, q.w1t.lo, q.ld,
-                        q.z.hi, q.z.lo, NB, kEpiStoreSplit));
+                        q.z.hi, q.z.lo, NB, kEpiStoreSplit, 0.f, 1));
         f3.push_back(gp(nr, L, nb, q.z.hi, q.z.lo, NB, q.yt.hi, q.yt.lo, NB, q.at.hi + ox,
                         q.at.lo + ox, q.ld, kEpiApplySplit, 1.f));
       }
@@ -789,12 +790,12 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
         const int nb = std::min(NB, q.rmax - kb0), L = q.p - kb0;
         const int blk = kb0 / NB;
         const int64_t oy = (int64_t)kb0 * q.ld + kb0;
-        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, NB, nb, L, 1, 1});
+        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, NB, nb, L, 1, 1, 1});
         q1.push_back(gp(nb, L, nb, q.tb.hi + (int64_t)blk * NB * NB,
                         q.tb.lo + (int64_t)blk * NB * NB, NB, q.yt.hi, q.yt.lo, NB, q.w1t.hi,
-                        q.w1t.lo, q.ld, kEpiStoreSplit));
+                        q.w1t.lo, q.ld, kEpiStoreSplit, 0.f, 1));
         q2.push_back(gp(L, nb, L, q.qt.hi + oy, q.qt.lo + oy, q.ld, q.w1t.hi, q.w1t.lo, q.ld,
-                        q.z.hi, q.z.lo, NB, kEpiStoreSplit));
+                        q.z.hi, q.z.lo, NB, kEpiStoreSplit, 0.f, 1));
         q3.push_back(gp(L, L, nb, q.z.hi, q.z.lo, NB, q.yt.hi, q.yt.lo, NB, q.qt.hi + oy,
                         q.qt.lo + oy, q.ld, kEpiApplySplit, 1.f));
       }

@@ -37,8 +37,9 @@ inline const float* F(const void* base, uint64_t off) {
 
 GemmProblem gp(int M, int N, int K, const float* ah, const float* al, int lda, const float* bh,
                const float* bl, int ldb, float* ch, float* cl, int ldc, int epi,
-               float alpha = 0.f) {
+               float alpha = 0.f, int mma_only = 0) {
   GemmProblem P;
+  P.mma_only = mma_only;
   P.M = M;
   P.N = N;
   P.K = K;
@@ -102,7 +103,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       tr[k] = {F(state, L.m_hi), F(state, L.m_lo), L.ldn, F(work, x.mT_hi), F(work, x.mT_lo),
-               L.ldm, L.m, L.n, 1, 1};
+               L.ldm, L.m, L.n, 1, 1, 1};
     }
     ROT_TRY(launch_transpose(tr, s));
 
@@ -120,26 +121,26 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       if (n < m) {
         // Z_U = M^T U (n x m), stored transposed (m x n);  A_U = M Z_U
         first.push_back(gp(n, m, m, MTh, MTl, L.ldm, F(state, L.ut_hi), F(state, L.ut_lo), L.ldm,
-                           Zuh, Zul, x.zu_ld, kEpiStoreSplitT));
+                           Zuh, Zul, x.zu_ld, kEpiStoreSplitT, 0.f, 1));
         second.push_back(gp(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, Auh, Aul, L.ldm,
                             kEpiStoreSplitT));
       } else {
         // Gram M M^T (m x m);  A_U = Gram U
         first.push_back(gp(m, m, n, Mh, Ml, L.ldn, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld,
-                           kEpiStoreSplit));
+                           kEpiStoreSplit, 0.f, 1));
         second.push_back(gp(m, m, m, Zuh, Zul, x.zu_ld, F(state, L.ut_hi), F(state, L.ut_lo),
                             L.ldm, Auh, Aul, L.ldm, kEpiStoreSplitT));
       }
       if (m < n) {
         // Z_V = M V (m x n), stored transposed (n x m);  A_V = M^T Z_V
         first.push_back(gp(m, n, n, Mh, Ml, L.ldn, F(state, L.vt_hi), F(state, L.vt_lo), L.ldn,
-                           Zvh, Zvl, x.zv_ld, kEpiStoreSplitT));
+                           Zvh, Zvl, x.zv_ld, kEpiStoreSplitT, 0.f, 1));
         second.push_back(gp(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, Avh, Avl, L.ldn,
                             kEpiStoreSplitT));
       } else {
         // Gram M^T M (n x n);  A_V = Gram V
         first.push_back(gp(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
-                           kEpiStoreSplit));
+                           kEpiStoreSplit, 0.f, 1));
         second.push_back(gp(n, n, n, Zvh, Zvl, x.zv_ld, F(state, L.vt_hi), F(state, L.vt_lo),
                             L.ldn, Avh, Avl, L.ldn, kEpiStoreSplitT));
       }
@@ -189,9 +190,9 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const int m = L.m, n = L.n;
       const float *Vth = F(state, L.vt_hi), *Vtl = F(state, L.vt_lo);
       a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, Vth, Vtl, L.ldn,
-                     F(work, x.sg_hi), F(work, x.sg_lo), L.ldm, kEpiStoreSplitT));
+                     F(work, x.sg_hi), F(work, x.sg_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
       a.push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
-                     F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT));
+                     F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
       const float *Uth = F(state, L.ut_hi), *Utl = F(state, L.ut_lo);
       b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
                      F(work, x.gt), nullptr, L.ldn, kEpiStoreF32));
@@ -224,7 +225,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const int m = L.m, n = L.n;
       a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, F(state, L.vb_hi),
                      F(state, L.vb_lo), L.ldn, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
-                     kEpiStoreSplitT));
+                     kEpiStoreSplitT, 0.f, 1));
       b.push_back(gp(m, n, m, F(state, L.u_hi), F(state, L.u_lo), L.ldm, F(work, x.sg_hi),
                      F(work, x.sg_lo), L.ldm, W[i], nullptr, n, kEpiApply, lr));
     }

@@ -56,6 +56,7 @@ struct GemmProblem {
   int ldc;
   int epi;
   float alpha;
+  int mma_only = 0;  // split outputs feed only tensor cores: round lo to TF32
 };
 
 // 3xTF32 with each K block accumulated afresh and summed in float32
@@ -78,9 +79,9 @@ int gemm_grouped(const std::vector<GemmProblem>& probs, int precision, int* stat
 
 struct MomentumSeg {
   const float* g;  // caller's gradient, row-major, ld = cols
-  float* m_hi;     // state momentum split, ld = ldm
+  float* m_hi;     // state momentum split (exact), ld = ldm
   float* m_lo;
-  float* g_hi;     // workspace gradient split, ld = ldm
+  float* g_hi;     // workspace gradient split (tensor-core operand), ld = ldm
   float* g_lo;
   int rows, cols, ldm;
 };
@@ -108,6 +109,7 @@ struct TransposeSeg {
   int rows, cols;
   int src_is_split;
   int dst_is_split;
+  int dst_mma_only = 0;  // the split output feeds only tensor cores
 };
 int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream);
 

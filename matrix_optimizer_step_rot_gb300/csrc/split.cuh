@@ -20,4 +20,14 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
   lo = x - hi;
 }
 
+// Split for operands that only the tensor cores read: lo is rounded to TF32
+// as well (round to nearest).  The tensor cores would otherwise truncate lo's
+// low 13 bits (2^-21 relative to x); rounded, the pair carries x to within
+// 2^-22 relative.  hi + lo is then not exactly x, so arrays that are also
+// recombined into float32 keep the exact split above.
+__device__ __forceinline__ void split_tf32_mma(float x, float& hi, float& lo) {
+  hi = tf32_round(x);
+  lo = tf32_round(x - hi);
+}
+
 }  // namespace rot
