@@ -73,19 +73,27 @@ __global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b,
   }
 }
 
-// v <- beta2 v + (1 - beta2) G~^2 ;  D = M~ / (sqrt(v) + eps)  (D as a split)
-__global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float beta2, float eps) {
+// [M~ <- beta1 M~ + (1 - beta1) G~;]  v <- beta2 v + (1 - beta2) G~^2 ;
+// D = M~ / (sqrt(v) + eps)  (D as a split)
+__global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float beta1, float beta2,
+                            float eps, int incremental) {
   const AdamSeg& s = b.seg[blockIdx.y];
   const int64_t total = (int64_t)s.rows * s.cols;
+  const float one_minus1 = 1.0f - beta1;
   const float one_minus = 1.0f - beta2;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
     const int64_t o = (int64_t)r * s.ld + c;
     const float g = s.gt[o];
+    float m = s.mt[o];
+    if (incremental) {
+      m = beta1 * m + one_minus1 * g;
+      s.mt[o] = m;
+    }
     const float v = beta2 * s.v[o] + one_minus * (g * g);
     s.v[o] = v;
-    const float d = s.mt[o] / (sqrtf(v) + eps);
+    const float d = m / (sqrtf(v) + eps);
     float h, l;
     split_tf32_mma(d, h, l);
     s.d_hi[o] = h;
@@ -182,9 +190,11 @@ int launch_momentum(const std::vector<MomentumSeg>& segs, float beta1, cudaStrea
   return launch_segs(segs, 28.0, momentum_kernel, stream, beta1);
 }
 
-int launch_adam(const std::vector<AdamSeg>& segs, float beta2, float eps, cudaStream_t stream) {
-  // read G~, M~, v (12); write v (4) and D's split (8)
-  return launch_segs(segs, 24.0, adam_kernel, stream, beta2, eps);
+int launch_adam(const std::vector<AdamSeg>& segs, float beta1, float beta2, float eps,
+                int incremental, cudaStream_t stream) {
+  // read G~, M~, v (12); write v (4) and D's split (8); incremental: write M~ (4)
+  return launch_segs(segs, incremental ? 28.0 : 24.0, adam_kernel, stream, beta1, beta2, eps,
+                     incremental);
 }
 
 int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream) {

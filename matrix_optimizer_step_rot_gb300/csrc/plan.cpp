@@ -127,6 +127,7 @@ void build_layout(rot_plan* p) {
     L.m_hi = s.floats(m, L.ldn);
     L.m_lo = s.floats(m, L.ldn);
     L.v = s.floats(m, L.ldn);
+    L.mt = s.floats(m, L.ldn);
     L.u_hi = s.floats(m, L.ldm);
     L.u_lo = s.floats(m, L.ldm);
     L.ut_hi = s.floats(m, L.ldm);

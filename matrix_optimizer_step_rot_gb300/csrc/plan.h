@@ -16,6 +16,7 @@ struct ItemLayout {
   int m, n, ldm, ldn;                 // ldm = pad(m), ldn = pad(n)
   uint64_t m_hi, m_lo;                // momentum split, m x ldn
   uint64_t v;                         // second moment, m x ldn
+  uint64_t mt;                        // M~ = U^T M V (float32), m x ldn
   uint64_t u_hi, u_lo, ut_hi, ut_lo;  // U and U^T splits, m x ldm
   uint64_t vb_hi, vb_lo, vt_hi, vt_lo;  // V and V^T splits, n x ldn
 };

@@ -345,47 +345,54 @@ __global__ void __launch_bounds__(kPanelThreads)
 
 // ---------------------------------------------------------------------------
 // within-block update: rows k0+b .. (block end)-1 of `at` get the panel's
-// reflectors, a <- a - Y (T^T (Y^T a)), elements k0..p-1 (CUDA cores)
+// reflectors, a <- a - Y (T^T (Y^T a)), elements k0..p-1 (CUDA cores).
+// Split along the elements so that every launch fills the GPU: the first
+// kernel writes, per 256-element chunk and 32-row tile, the partial products
+// Y^T a; the second adds the chunks' partials in a fixed order (so results
+// do not depend on scheduling), applies T^T and updates its chunk.
 // ---------------------------------------------------------------------------
 
 constexpr int kRows = 32;
+constexpr int kChunk = 256;
+constexpr int kRowTiles = (NB - B) / kRows;  // rows after the first panel of a block
 
-__global__ void __launch_bounds__(256) qr_panel_apply_kernel(const __grid_constant__ QrBatch b,
-                                                             int k0) {
-  const QrProblem& q = b.p[blockIdx.y];
-  if (k0 >= q.rmax) return;
-  const int panel = k0 / B;
-  const int active = q.ctrl[2 + panel];
-  if (active == 0) return;
-  const int p = q.p, ld = q.ld;
-  const int row_end = min(q.rmax, (k0 / NB) * NB + NB);
-  const int r0 = k0 + B + blockIdx.x * kRows;
-  if (r0 >= row_end) return;
-  float* xh = q.at.hi;
-  float* xl = q.at.lo;
+__device__ __forceinline__ bool apply_tile(const QrProblem& q, int k0, int& active, int& r0,
+                                           int& row_end, int& e_begin, int& e_end) {
+  if (k0 >= q.rmax) return false;
+  active = q.ctrl[2 + k0 / B];
+  if (active == 0) return false;
+  row_end = min(q.rmax, (k0 / NB) * NB + NB);
+  r0 = k0 + B + blockIdx.y * kRows;
+  if (r0 >= row_end) return false;
+  e_begin = k0 + blockIdx.x * kChunk;
+  if (e_begin >= q.p) return false;
+  e_end = min(q.p, e_begin + kChunk);
+  return true;
+}
 
+__global__ void __launch_bounds__(256) qr_apply_partial_kernel(const __grid_constant__ QrBatch b,
+                                                               int k0) {
+  const QrProblem& q = b.p[blockIdx.z];
+  int active, r0, row_end, e_begin, e_end;
+  if (!apply_tile(q, k0, active, r0, row_end, e_begin, e_end)) return;
+  const int ld = q.ld;
+  const float* xh = q.at.hi;
+  const float* xl = q.at.lo;
   __shared__ float xs[kRows][33];
   __shared__ float ys[B][33];
-  __shared__ float z[kRows][B + 1];
-  __shared__ float zt[kRows][B + 1];
-  __shared__ float tm[B][B + 1];
-  const int tid = threadIdx.x;
-  const float* tf = q.tf + (int64_t)panel * B * B;
-  for (int i = tid; i < B * B; i += 256) tm[i / B][i % B] = tf[i];
-
-  const int r = tid >> 3, i4 = (tid & 7) * 4;
+  const int tid = threadIdx.x, r = tid >> 3, i4 = (tid & 7) * 4;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int e0 = k0; e0 < p; e0 += 32) {
+  for (int c0 = e_begin; c0 < e_end; c0 += 32) {
     __syncthreads();
     for (int t = tid; t < kRows * 32; t += 256) {
-      const int rr = t >> 5, ee = t & 31, e = e0 + ee;
+      const int rr = t >> 5, ee = t & 31, e = c0 + ee;
       const int row = r0 + rr;
       float xv = 0.f, yv = 0.f;
-      if (row < row_end && e < p) {
+      if (row < row_end && e < e_end) {
         const int64_t o = (int64_t)row * ld + e;
         xv = xh[o] + xl[o];
       }
-      if (rr < active && e < p && e >= k0 + rr) {
+      if (rr < active && e < e_end && e >= k0 + rr) {
         const int64_t o = (int64_t)(k0 + rr) * ld + e;
         yv = xh[o] + xl[o];
       }
@@ -400,24 +407,50 @@ __global__ void __launch_bounds__(256) qr_panel_apply_kernel(const __grid_consta
       for (int c = 0; c < 4; ++c) acc[c] = fmaf(xv, ys[i4 + c][ee], acc[c]);
     }
   }
+  float* part = q.part + ((int64_t)blockIdx.x * kRowTiles + blockIdx.y) * (kRows * B);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) z[r][i4 + c] = acc[c];
+  for (int c = 0; c < 4; ++c) part[r * B + i4 + c] = acc[c];
+}
+
+__global__ void __launch_bounds__(256) qr_apply_update_kernel(const __grid_constant__ QrBatch b,
+                                                              int k0) {
+  const QrProblem& q = b.p[blockIdx.z];
+  int active, r0, row_end, e_begin, e_end;
+  if (!apply_tile(q, k0, active, r0, row_end, e_begin, e_end)) return;
+  const int ld = q.ld;
+  float* xh = q.at.hi;
+  float* xl = q.at.lo;
+  __shared__ float ys[B][33];
+  __shared__ float z[kRows][B + 1];
+  __shared__ float zt[kRows][B + 1];
+  __shared__ float tm[B][B + 1];
+  const int tid = threadIdx.x;
+  const float* tf = q.tf + (int64_t)(k0 / B) * B * B;
+  for (int i = tid; i < B * B; i += 256) tm[i / B][i % B] = tf[i];
+  // z = sum of the chunks' partials, in chunk order
+  const int nchunks = (q.p - k0 + kChunk - 1) / kChunk;
+  for (int i = tid; i < kRows * B; i += 256) {
+    float t = 0.f;
+    for (int c = 0; c < nchunks; ++c)
+      t += q.part[((int64_t)c * kRowTiles + blockIdx.y) * (kRows * B) + i];
+    z[i / B][i % B] = t;
+  }
   __syncthreads();
+  const int r = tid >> 3, i4 = (tid & 7) * 4;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int i = i4 + c;
     float t = 0.f;
-    for (int jj = 0; jj < B; ++jj) t = fmaf(z[r][jj], tm[jj][i], t);
+    for (int jj = 0; jj < B; ++jj) t = fmaf(z[r][jj], tm[jj][i], t);  // (T^T z)_i
     zt[r][i] = t;
   }
-  __syncthreads();
   const int e4 = (tid & 7) * 4;
-  for (int e0 = k0; e0 < p; e0 += 32) {
+  for (int c0 = e_begin; c0 < e_end; c0 += 32) {
     __syncthreads();
     for (int t = tid; t < B * 32; t += 256) {
-      const int yi = t >> 5, ee = t & 31, e = e0 + ee;
+      const int yi = t >> 5, ee = t & 31, e = c0 + ee;
       float yv = 0.f;
-      if (yi < active && e < p && e >= k0 + yi) {
+      if (yi < active && e < e_end && e >= k0 + yi) {
         const int64_t o = (int64_t)(k0 + yi) * ld + e;
         yv = xh[o] + xl[o];
       }
@@ -428,8 +461,8 @@ __global__ void __launch_bounds__(256) qr_panel_apply_kernel(const __grid_consta
     if (row < row_end) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int e = e0 + e4 + c;
-        if (e < p) {
+        const int e = c0 + e4 + c;
+        if (e < e_end) {
           float t = 0.f;
 #pragma unroll 8
           for (int i = 0; i < B; ++i) t = fmaf(zt[r][i], ys[i][e4 + c], t);
@@ -455,20 +488,21 @@ __global__ void __launch_bounds__(NB) qr_tblock_kernel(const __grid_constant__ Q
                                                        int kb0) {
   const QrProblem& q = b.p[blockIdx.x];
   if (kb0 >= q.rmax) return;
-  extern __shared__ float tsm[];  // [NB][NB + 1]
+  extern __shared__ float tsm[];  // T [NB][NB + 1], then S [NB][NB + 1]
+  constexpr int LD = NB + 1;
+  float* S = tsm + NB * LD;
   const int nb = min(NB, q.rmax - kb0);
   const int act = max(0, min(nb, rank_now(q) - kb0));
   const int blk = kb0 / NB;
-  const float* S = q.s;
   const int tid = threadIdx.x;
-  constexpr int LD = NB + 1;
   for (int i = tid; i < NB * LD; i += blockDim.x) tsm[i] = 0.f;
+  for (int i = tid; i < NB * NB; i += blockDim.x) S[(i / NB) * LD + i % NB] = q.s[i];
   __syncthreads();
   for (int i = 0; i < act; ++i) {
-    const float tii = 2.f / S[(int64_t)i * NB + i];
+    const float tii = 2.f / S[i * LD + i];
     float t = 0.f;
     if (tid < i)
-      for (int l = tid; l < i; ++l) t = fmaf(tsm[tid * LD + l], S[(int64_t)l * NB + i], t);
+      for (int l = tid; l < i; ++l) t = fmaf(tsm[tid * LD + l], S[l * LD + i], t);
     __syncthreads();
     if (tid < i) tsm[tid * LD + i] = -tii * t;
     if (tid == i) tsm[i * LD + i] = tii;
@@ -651,7 +685,8 @@ uint64_t qr_aux_bytes(int p, int rmax) {
          + 2 * align256((uint64_t)NB * ld * 4)      // w1t split
          + 2 * align256((uint64_t)p * NB * 4)       // z split
          + align256((uint64_t)NB * NB * 4)          // Gram S
-         + 4 * align256(nbk * NB * NB * 4);         // T and T^T splits per block
+         + 4 * align256(nbk * NB * NB * 4)          // T and T^T splits per block
+         + align256(((uint64_t)p / kChunk + 1) * kRowTiles * kRows * B * 4);  // partials
 }
 
 void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax) {
@@ -678,6 +713,7 @@ void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax) {
   q.tb.lo = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
   q.tbt.hi = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
   q.tbt.lo = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
+  q.part = reinterpret_cast<float*>(take(((uint64_t)p / kChunk + 1) * kRowTiles * kRows * B * 4));
 }
 
 int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status,
@@ -689,7 +725,7 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
   static bool tattr = false;
   if (!tattr) {
     if (cudaFuncSetAttribute(qr_tblock_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(NB * (NB + 1) * sizeof(float))) != cudaSuccess)
+                             (int)(2 * NB * (NB + 1) * sizeof(float))) != cudaSuccess)
       return ROT_ECUDA;
     tattr = true;
   }
@@ -728,8 +764,16 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
             const int re = std::min(q.rmax, kb0 + NB);
             if (k0 < q.rmax && re > k0 + B) f += 4.0 * B * (double)(re - k0 - B) * (q.p - k0);
           }
-          ProfScope prof(ROT_PROF_QR_APPLY, f, stream);
-          qr_panel_apply_kernel<<<dim3((rows + kRows - 1) / kRows, n), 256, 0, stream>>>(b, k0);
+          const dim3 grid((unsigned)((pmax - k0 + kChunk - 1) / kChunk),
+                          (unsigned)((rows + kRows - 1) / kRows), n);
+          {
+            ProfScope prof(ROT_PROF_QR_APPLY, f * 0.5, stream);
+            qr_apply_partial_kernel<<<grid, 256, 0, stream>>>(b, k0);
+          }
+          {
+            ProfScope prof(ROT_PROF_QR_APPLY, f * 0.5, stream);
+            qr_apply_update_kernel<<<grid, 256, 0, stream>>>(b, k0);
+          }
         }
       }
       // block factor T from the Gram of the block's reflectors
@@ -745,7 +789,7 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       if (gemm_grouped(gram, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
       {
         ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
-        qr_tblock_kernel<<<n, NB, NB * (NB + 1) * sizeof(float), stream>>>(b, kb0);
+        qr_tblock_kernel<<<n, NB, 2 * NB * (NB + 1) * sizeof(float), stream>>>(b, kb0);
       }
       // trailing columns kb0+NB .. rmax-1: a <- a - Y (T^T (Y^T a))
       std::vector<TransposeSeg> tr;

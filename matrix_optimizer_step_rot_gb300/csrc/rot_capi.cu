@@ -181,7 +181,10 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     ROT_TRY(qr_batched(qp, rank_rtol, status, s));
   }
 
-  // (3) rotation: S_G^T = (G V)^T, S_M^T = (M V)^T ; G~ = U^T S_G, M~ = U^T S_M
+  // (3) rotation: S_G^T = (G V)^T ; G~ = U^T S_G.  M~ = U^T M V is recomputed
+  // from M only when the bases change (refresh steps); otherwise it follows
+  // M~ <- beta1 M~ + (1 - beta1) G~ inside the Adam kernel, which is the same
+  // quantity since U and V are unchanged.
   {
     std::vector<GemmProblem> a, b;
     for (size_t k = 0; k < n_items; ++k) {
@@ -191,13 +194,15 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const float *Vth = F(state, L.vt_hi), *Vtl = F(state, L.vt_lo);
       a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, Vth, Vtl, L.ldn,
                      F(work, x.sg_hi), F(work, x.sg_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
-      a.push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
-                     F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
+      if (refresh)
+        a.push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
+                       F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
       const float *Uth = F(state, L.ut_hi), *Utl = F(state, L.ut_lo);
       b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
                      F(work, x.gt), nullptr, L.ldn, kEpiStoreF32));
-      b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
-                     F(work, x.mt), nullptr, L.ldn, kEpiStoreF32));
+      if (refresh)
+        b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
+                       F(state, L.mt), nullptr, L.ldn, kEpiStoreF32));
     }
     ROT_TRY(gemm_grouped(a, precision, status, s));
     ROT_TRY(gemm_grouped(b, precision, status, s));
@@ -209,10 +214,10 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
-      segs[k] = {F(work, x.gt), F(work, x.mt), F(state, L.v), F(work, x.g_hi), F(work, x.g_lo),
+      segs[k] = {F(work, x.gt), F(state, L.mt), F(state, L.v), F(work, x.g_hi), F(work, x.g_lo),
                  L.m, L.n, L.ldn};
     }
-    ROT_TRY(launch_adam(segs, beta2, eps, s));
+    ROT_TRY(launch_adam(segs, beta1, beta2, eps, refresh ? 0 : 1, s));
   }
 
   // (4) back-rotation: (D V^T)^T into S_G's buffer; W -= lr U (D V^T)
@@ -255,6 +260,7 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream) {
     const ItemLayout& L = plan->items[i];
     segs.push_back({F(state, L.m_hi), F(state, L.m_lo), L.m, L.n, L.ldn, 0});
     segs.push_back({F(state, L.v), nullptr, L.m, L.n, L.ldn, 0});
+    segs.push_back({F(state, L.mt), nullptr, L.m, L.n, L.ldn, 0});
     segs.push_back({F(state, L.u_hi), F(state, L.u_lo), L.m, L.m, L.ldm, 1});
     segs.push_back({F(state, L.ut_hi), F(state, L.ut_lo), L.m, L.m, L.ldm, 1});
     segs.push_back({F(state, L.vb_hi), F(state, L.vb_lo), L.n, L.n, L.ldn, 1});

@@ -89,13 +89,16 @@ int launch_momentum(const std::vector<MomentumSeg>& segs, float beta1, cudaStrea
 
 struct AdamSeg {
   const float* gt;  // G~ float32, ld
-  const float* mt;  // M~ float32, ld
+  float* mt;        // state M~ float32, ld (updated in place when incremental)
   float* v;         // state second moment, ld
   float* d_hi;      // D split out, ld
   float* d_lo;
   int rows, cols, ld;
 };
-int launch_adam(const std::vector<AdamSeg>& segs, float beta2, float eps, cudaStream_t stream);
+// incremental != 0: M~ <- beta1 M~ + (1 - beta1) G~ first (bases unchanged
+// since the last step); else M~ was just recomputed as U^T M V.
+int launch_adam(const std::vector<AdamSeg>& segs, float beta1, float beta2, float eps,
+                int incremental, cudaStream_t stream);
 
 // dst (cols x rows, ld_dst) = src^T, where src (rows x cols, ld_src) is a split;
 // dst is written as a split.  src_is_split = 0 reads float32 from src.hi.
@@ -154,6 +157,7 @@ struct QrProblem {
   Split tb;     // per block: T (kQrBlock x kQrBlock)
   Split tbt;    // per block: T^T
   float* tf;    // per panel: 32 x 32 triangular factor
+  float* part;  // within-block update: per element chunk and row tile, Y^T a partials
   float* beta;  // rmax: R diagonal before the sign fix
   int* ctrl;    // [0] rank, [1] stopped flag, [2..] per-panel active counts
   float* tau;   // largest column norm of A

@@ -1,8 +1,10 @@
 """Analytic work of the rotated-Adam step (what the method itself needs).
 
-Per matrix W (m x n), every step:
-  rotation   G~ = U^T G V, M~ = U^T M V, and U D V^T: three two-sided
-             products, 6 (m^2 n + m n^2) flops.
+Per matrix W (m x n):
+  rotation   G~ = U^T G V and U D V^T every step: two two-sided products,
+             4 (m^2 n + m n^2) flops; M~ = U^T M V, a third, only when the
+             bases change (refresh steps; in between M~ follows
+             beta1 M~ + (1 - beta1) G~ element-wise, the same quantity).
 On refresh steps, in addition:
   products   A_U = M (M^T U) when n < m (4 m^2 n), else (M M^T) U
              (2 m^2 n + 2 m^3); the same with m and n exchanged for A_V.
@@ -19,8 +21,8 @@ Element-wise work (momentum, v, D) is counted in bytes, not flops.
 from __future__ import annotations
 
 
-def rotation_flops(m: int, n: int) -> float:
-    return 6.0 * (m * m * n + m * n * n)
+def rotation_flops(m: int, n: int, refresh: bool = True) -> float:
+    return (6.0 if refresh else 4.0) * (m * m * n + m * n * n)
 
 
 def product_flops(m: int, n: int) -> float:
@@ -50,7 +52,7 @@ def refresh_flops(m: int, n: int) -> float:
 
 
 def matrix_step_flops(m: int, n: int, refresh: bool) -> float:
-    return rotation_flops(m, n) + (refresh_flops(m, n) if refresh else 0.0)
+    return rotation_flops(m, n, refresh) + (refresh_flops(m, n) if refresh else 0.0)
 
 
 def step_flops(shapes, refresh: bool) -> float:
