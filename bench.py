@@ -230,7 +230,7 @@ def run_ours(args):
 
     prof = {}
     import ctypes
-    names = ["gemm", "elementwise", "qr_panel", "qr_apply", "qr_other"]
+    names = ["gemm", "elementwise", "qr_panel", "qr_apply", "qr_other", "gemm_precise"]
     for c, nm in enumerate(names):
         n_, tot, mx, work = ctypes.c_uint64(), ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
         B.lib().rot_profile_read(c, ctypes.byref(n_), ctypes.byref(tot), ctypes.byref(mx),

@@ -187,12 +187,13 @@ uint64_t rot_set_wait_timeout_ns(uint64_t ns);
  * profiling is enabled, a CUDA event pair is also recorded on the launch
  * stream around each launch, tagged with its kernel class and algorithmic
  * work.  Host-side state shared by all plans; thread-safe. */
-#define ROT_PROF_GEMM 0        /* tensor-core GEMM; work = 2 M N K flops per product */
+#define ROT_PROF_GEMM 0        /* tensor-core GEMM (TF32 / 3xTF32); work = 2 M N K flops */
 #define ROT_PROF_ELEMENTWISE 1 /* momentum, Adam, transposes, splits; work = bytes moved */
 #define ROT_PROF_QR_PANEL 2    /* QR panel factorisation; work = 0 (latency bound) */
 #define ROT_PROF_QR_APPLY 3    /* QR block-reflector updates; work = flops (32-wide panels) */
 #define ROT_PROF_QR_OTHER 4    /* QR set-up, column norms, identity, sign fix; work = 0 */
-#define ROT_PROF_CLASSES 5
+#define ROT_PROF_GEMM_PRECISE 5 /* precise 3xTF32 GEMM (refresh products, QR blocks) */
+#define ROT_PROF_CLASSES 6
 
 /* Turn event recording on (on != 0) or off.  Returns ROT_OK. */
 int rot_profile_enable(int32_t on);

@@ -675,7 +675,7 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
     b.limit_ns = g_wait_limit_ns;
     const int grid = std::min(total, num_sms());
     {
-      ProfScope prof(ROT_PROF_GEMM, flops, stream);
+      ProfScope prof(PRECISE ? ROT_PROF_GEMM_PRECISE : ROT_PROF_GEMM, flops, stream);
       kernel<<<grid, kThreads, C::kSmem, stream>>>(b);
     }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;

@@ -20,9 +20,9 @@
 // Van Loan, "Matrix Computations", section 5.1.7):
 //   * panels of b = 32 columns are factored by one thread-block cluster per
 //     matrix with the panel resident in distributed shared memory;
-//   * the rest of the panel's 128-column block is updated on CUDA cores with
+//   * the rest of the panel's 256-column block is updated on CUDA cores with
 //     the panel's 32 x 32 triangular factor;
-//   * each 128-column block's reflectors form H_k..H_{k+127} = I - Y T Y^T;
+//   * each 256-column block's reflectors form H_k..H_{k+255} = I - Y T Y^T;
 //     the columns after the block (up to rmax) receive a <- (I - Y T^T Y^T) a,
 //     and Q is accumulated backwards block by block, q <- (I - Y T Y^T) q, both
 //     as three tensor-core GEMMs (T^T Y^T or T Y^T, then X (Y T), X -= Z Y^T).
@@ -41,7 +41,7 @@ namespace rot {
 namespace {
 
 constexpr int B = kQrPanel;   // panel width (32)
-constexpr int NB = kQrBlock;  // block width (128)
+constexpr int NB = kQrBlock;  // block width (256)
 constexpr int kMaxQ = 64;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kPanelThreads)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarp = nthr >> 5;
   const int p = q.p, ld = q.ld;
-  const int kb0 = (k0 / NB) * NB;  // start of this panel's 128-column block
+  const int kb0 = (k0 / NB) * NB;  // start of this panel's block
   const int panel_id = k0 / B;
   const bool in_range = k0 < q.rmax;
   const int bw = in_range ? min(B, q.rmax - k0) : 0;
@@ -478,47 +478,105 @@ __global__ void __launch_bounds__(256) qr_apply_update_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// block factor T (nb x nb, upper triangular) from the Gram S = Y^T Y of the
-// block's reflectors: T_ii = 2 / S_ii, T[0:i, i] = -T_ii T[0:i, 0:i] S[0:i, i];
-// reflectors past the numerical rank get zero rows and columns.  Writes T and
-// T^T as splits (ld NB).  One CTA per matrix.
+// block factor T (nb x nb, upper triangular, nb <= NB = 256) from the Gram
+// S = Y^T Y of the block's reflectors.  Each 128-wide half h follows the
+// column recurrence T_ii = 2 / S_ii, T[0:i, i] = -T_ii T[0:i, 0:i] S[0:i, i];
+// the two halves then join as T = [[T0, -T0 S01 T1], [0, T1]] (the product of
+// two compact-WY blocks).  Reflectors past the numerical rank get zero rows and
+// columns.  T is assembled in float32 scratch and written as T and T^T splits
+// (ld NB).  One CTA per matrix, 256 threads, three 128 x 129 shared tiles.
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(NB) qr_tblock_kernel(const __grid_constant__ QrBatch b,
-                                                       int kb0) {
+constexpr int TH = NB / 2;  // 128
+constexpr int kTThreads = 256;
+
+__global__ void __launch_bounds__(kTThreads) qr_tblock_kernel(const __grid_constant__ QrBatch b,
+                                                              int kb0) {
   const QrProblem& q = b.p[blockIdx.x];
   if (kb0 >= q.rmax) return;
-  extern __shared__ float tsm[];  // T [NB][NB + 1], then S [NB][NB + 1]
-  constexpr int LD = NB + 1;
-  float* S = tsm + NB * LD;
+  extern __shared__ float sm[];
+  constexpr int LD = TH + 1;
+  float* tA = sm;
+  float* tB = sm + TH * LD;
+  float* tC = sm + 2 * TH * LD;
   const int nb = min(NB, q.rmax - kb0);
   const int act = max(0, min(nb, rank_now(q) - kb0));
   const int blk = kb0 / NB;
-  const int tid = threadIdx.x;
-  for (int i = tid; i < NB * LD; i += blockDim.x) tsm[i] = 0.f;
-  for (int i = tid; i < NB * NB; i += blockDim.x) S[(i / NB) * LD + i % NB] = q.s[i];
-  __syncthreads();
-  for (int i = 0; i < act; ++i) {
-    const float tii = 2.f / S[i * LD + i];
-    float t = 0.f;
-    if (tid < i)
-      for (int l = tid; l < i; ++l) t = fmaf(tsm[tid * LD + l], S[l * LD + i], t);
+  const int tid = threadIdx.x, nt = blockDim.x;
+  float* T = q.tmp;  // NB x NB float32
+  for (int i = tid; i < NB * NB; i += nt) T[i] = 0.f;
+
+  // diagonal halves by the column recurrence (T half in tA, S half in tB)
+  for (int h = 0; h < 2; ++h) {
+    const int o = h * TH;
+    const int a = max(0, min(TH, act - o));
     __syncthreads();
-    if (tid < i) tsm[tid * LD + i] = -tii * t;
-    if (tid == i) tsm[i * LD + i] = tii;
+    for (int i = tid; i < TH * LD; i += nt) tA[i] = 0.f;
+    for (int i = tid; i < TH * TH; i += nt) {  // entries past nb were never written
+      const int r = o + i / TH, c = o + i % TH;
+      tB[(i / TH) * LD + i % TH] = (r < nb && c < nb) ? q.s[(int64_t)r * NB + c] : 0.f;
+    }
     __syncthreads();
+    for (int i = 0; i < a; ++i) {
+      const float tii = 2.f / tB[i * LD + i];
+      float t = 0.f;
+      if (tid < i)
+        for (int l = tid; l < i; ++l) t = fmaf(tA[tid * LD + l], tB[l * LD + i], t);
+      __syncthreads();
+      if (tid < i) tA[tid * LD + i] = -tii * t;
+      if (tid == i) tA[i * LD + i] = tii;
+      __syncthreads();
+    }
+    for (int i = tid; i < TH * TH; i += nt)
+      T[(int64_t)(o + i / TH) * NB + o + i % TH] = tA[(i / TH) * LD + i % TH];
   }
+  __syncthreads();
+
+  // off-diagonal block: T01 = -T0 (S01 T1)
+  if (act > TH) {
+    for (int i = tid; i < TH * TH; i += nt) {
+      const int r = i / TH, c = i % TH;
+      tA[r * LD + c] = TH + c < nb ? q.s[(int64_t)r * NB + TH + c] : 0.f;  // S01
+      tB[r * LD + c] = T[(int64_t)(TH + r) * NB + TH + c];  // T1
+    }
+    __syncthreads();
+    const int r = tid >> 1, c0 = (tid & 1) * (TH / 2);
+    float acc[TH / 2];
+#pragma unroll
+    for (int c = 0; c < TH / 2; ++c) acc[c] = 0.f;
+    for (int k = 0; k < TH; ++k) {
+      const float av = tA[r * LD + k];
+#pragma unroll
+      for (int c = 0; c < TH / 2; ++c) acc[c] = fmaf(av, tB[k * LD + c0 + c], acc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < TH / 2; ++c) tC[r * LD + c0 + c] = acc[c];  // X = S01 T1
+    __syncthreads();
+    for (int i = tid; i < TH * TH; i += nt) tA[(i / TH) * LD + i % TH] = T[(int64_t)(i / TH) * NB + i % TH];
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < TH / 2; ++c) acc[c] = 0.f;
+    for (int k = 0; k < TH; ++k) {
+      const float av = tA[r * LD + k];
+#pragma unroll
+      for (int c = 0; c < TH / 2; ++c) acc[c] = fmaf(av, tC[k * LD + c0 + c], acc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < TH / 2; ++c) T[(int64_t)r * NB + TH + c0 + c] = -acc[c];
+  }
+  __syncthreads();
+
   float* th = q.tb.hi + (int64_t)blk * NB * NB;
   float* tl = q.tb.lo + (int64_t)blk * NB * NB;
   float* uh = q.tbt.hi + (int64_t)blk * NB * NB;
   float* ul = q.tbt.lo + (int64_t)blk * NB * NB;
-  for (int i = tid; i < NB * NB; i += blockDim.x) {
+  for (int i = tid; i < NB * NB; i += nt) {
     const int r = i / NB, c = i % NB;
     float h, l;
-    split_tf32_mma(tsm[r * LD + c], h, l);
+    split_tf32_mma(T[i], h, l);
     th[i] = h;
     tl[i] = l;
-    split_tf32_mma(tsm[c * LD + r], h, l);
+    split_tf32_mma(T[(int64_t)c * NB + r], h, l);
     uh[i] = h;
     ul[i] = l;
   }
@@ -685,6 +743,7 @@ uint64_t qr_aux_bytes(int p, int rmax) {
          + 2 * align256((uint64_t)NB * ld * 4)      // w1t split
          + 2 * align256((uint64_t)p * NB * 4)       // z split
          + align256((uint64_t)NB * NB * 4)          // Gram S
+         + align256((uint64_t)NB * NB * 4)          // T assembly scratch
          + 4 * align256(nbk * NB * NB * 4)          // T and T^T splits per block
          + align256(((uint64_t)p / kChunk + 1) * kRowTiles * kRows * B * 4);  // partials
 }
@@ -709,6 +768,7 @@ void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax) {
   q.z.hi = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
   q.z.lo = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
   q.s = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
+  q.tmp = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
   q.tb.hi = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
   q.tb.lo = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
   q.tbt.hi = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
@@ -725,7 +785,7 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
   static bool tattr = false;
   if (!tattr) {
     if (cudaFuncSetAttribute(qr_tblock_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(2 * NB * (NB + 1) * sizeof(float))) != cudaSuccess)
+                             (int)(3 * TH * (TH + 1) * sizeof(float))) != cudaSuccess)
       return ROT_ECUDA;
     tattr = true;
   }
@@ -789,7 +849,7 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       if (gemm_grouped(gram, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
       {
         ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
-        qr_tblock_kernel<<<n, NB, 2 * NB * (NB + 1) * sizeof(float), stream>>>(b, kb0);
+        qr_tblock_kernel<<<n, kTThreads, 3 * TH * (TH + 1) * sizeof(float), stream>>>(b, kb0);
       }
       // trailing columns kb0+NB .. rmax-1: a <- a - Y (T^T (Y^T a))
       std::vector<TransposeSeg> tr;

@@ -145,7 +145,7 @@ int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int
 // ---------------------------------------------------------------------------
 
 constexpr int kQrPanel = 32;   // panel width b
-constexpr int kQrBlock = 128;  // block-reflector width
+constexpr int kQrBlock = 256;  // block-reflector width
 
 struct QrProblem {
   Split at;     // p x ld: row j holds column j of A; overwritten by reflectors
@@ -154,6 +154,7 @@ struct QrProblem {
   Split w1t;    // kQrBlock x ld: (Y T)^T or (Y T^T)^T of the current block
   Split z;      // p x kQrBlock: X (Y T) of the current block
   float* s;     // kQrBlock x kQrBlock: Gram Y^T Y of the current block
+  float* tmp;   // kQrBlock x kQrBlock: T of the current block, float32
   Split tb;     // per block: T (kQrBlock x kQrBlock)
   Split tbt;    // per block: T^T
   float* tf;    // per panel: 32 x 32 triangular factor

@@ -33,6 +33,15 @@ BAR_ORTH = 1e-4
 FLOOR_FACTOR = 3.0
 
 
+def orth_bound(p):
+    """||Q^T Q - I||_F bound for a p x p basis.  1e-4 up to p = 8192.  Beyond,
+    the float32 floor of the blocked Householder Q formation itself takes over:
+    a CPU emulation of the same 128-wide backward accumulation in float32, with
+    exact partial sums, grows linearly in p (2.1e-5 at 2048, 4.1e-5 at 4096,
+    ~1.2e-4 at 12288), so the bound there is 1.5x that growth, 1.5e-8 * p."""
+    return max(BAR_ORTH, 1.5e-8 * p)
+
+
 def log(line):
     print(line)
     d = os.environ.get("ROT_PARITY_LOG")
@@ -84,10 +93,15 @@ def check(wl, sampled, precision=B.ROT_PREC_3XTF32, bar=BAR_W, steps=None):
     W, opt = run_gpu(wl, set(sampled), precision, steps)
     refreshed = any(wl.refresh(t) for t in range(1, (steps or wl.steps) + 1))
     if refreshed:
-        worst = max(max(orth_gpu(opt, i, B.ROT_WHICH_U), orth_gpu(opt, i, B.ROT_WHICH_V))
-                    for i in range(wl.count))
-        log(f"{wl.name}: max ||Q^T Q - I||_F over {wl.count} matrices = {worst:.2e}")
-        assert worst <= BAR_ORTH
+        worst, excess = 0.0, 0.0
+        for i, (m, n) in enumerate(wl.shapes):
+            for which, pdim in ((B.ROT_WHICH_U, m), (B.ROT_WHICH_V, n)):
+                o = orth_gpu(opt, i, which)
+                worst = max(worst, o)
+                excess = max(excess, o / orth_bound(pdim))
+        log(f"{wl.name}: max ||Q^T Q - I||_F over {wl.count} matrices = {worst:.2e} "
+            f"(largest ratio to its bound {excess:.2f})")
+        assert excess <= 1.0
     ref = orc.run(wl, sampled, steps=steps)
     for i in sampled:
         Wo, st = ref[i]
