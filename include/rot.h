@@ -96,6 +96,50 @@ int rot_plan_create(const rot_shape* shapes, int32_t count, uint64_t c_max_bytes
 int rot_plan_create_ex(const rot_shape* shapes, int32_t count, uint64_t c_max_bytes,
                        int32_t ranks, rot_plan** out);
 
+/* ---- data-parallel partition (host only, no device work) -----------------
+ *
+ * Where the matrices of a model are split across data-parallel ranks (each
+ * rank updates the matrices it owns; the rest are gathered afterwards), these
+ * entry points give the owner of every matrix.  Items are given in physical
+ * order and grouped into consecutive buckets (bucket b = the next
+ * bucket_sizes[b] items); a bucket is cut into `ranks` consecutive pieces,
+ * rank r taking piece r, with every cut on an item boundary (an item is never
+ * split).  The sizes must be >= 0 and add up to `count`.
+ */
+
+/* Work (processing-time proxy) of each item: m^2 n + m n^2 + m^3 + n^3, the
+ * micro-group planner's cost.  Errors: ROT_EINVAL for null pointers with
+ * count > 0, count < 0 or a dimension outside [1, ROT_MAX_DIM]. */
+int rot_item_work(const rot_shape* shapes, int32_t count, uint64_t* work);
+
+/* Static ownership by parameter start (Canzona page, section 3.1.1), bucket by
+ * bucket as a ZeRO-1 flat buffer is sharded: bucket b's items lie back to back
+ * in E_b elements (elems[i] each), cut into shards of ceil(E_b / ranks)
+ * elements; an item belongs to the shard holding its first element.
+ * owners: `count` entries written.  Errors: ROT_EINVAL for null pointers with
+ * count > 0 (or n_buckets > 0), ranks < 1, a negative size, sizes not adding
+ * up to `count`, or a bucket total above 2^64 - 1. */
+int rot_partition_static(const uint64_t* elems, int32_t count, const int32_t* bucket_sizes,
+                         int32_t n_buckets, int32_t ranks, int32_t* owners);
+
+/* alpha-balanced greedy LPT partition (Canzona page, section 3.2.1).  Buckets
+ * are visited by total work W_b, largest first (ties: lower index first).  For
+ * each, with per-rank loads L so far: ideal A = (sum L + W_b) / ranks; deficit
+ * d_r = max(0, A - L_r); fill share d_r / sum d (1/ranks if every d_r is 0);
+ * share s_r = (1 - alpha) / ranks + alpha * fill_r; cut r goes to the item
+ * boundary whose prefix work is nearest to W_b (s_0 + ... + s_r) (ties: the
+ * earlier boundary); L grows by each piece's work.  alpha = 0 splits every
+ * bucket evenly, alpha = 1 fills the ranks furthest below the ideal.  The
+ * floating-point steps are float64, in this order, with no contraction, so
+ * every host gets the same cuts.
+ * owners: `count` entries; loads (may be NULL): `ranks` entries, each rank's
+ * total work.  Errors: ROT_EINVAL as rot_partition_static, plus alpha outside
+ * [0, 1] (or NaN) and total work >= 2^53 (loads must stay exact in a double);
+ * ROT_ENOMEM. */
+int rot_partition_alpha(const uint64_t* work, int32_t count, const int32_t* bucket_sizes,
+                        int32_t n_buckets, int32_t ranks, double alpha, int32_t* owners,
+                        uint64_t* loads);
+
 /* Free a plan (NULL is accepted). */
 void rot_plan_destroy(rot_plan* plan);
 

@@ -73,6 +73,11 @@ _SIGS = {
                              _vp, _u64, _vp, _vp]),
     "rot_test_gemm_work_bytes": (_u64, [_i32, _i32, _i32]),
     "rot_test_wait_timeout": (_i32, [_u64, _vp, _vp]),
+    "rot_item_work": (_i32, [ctypes.POINTER(rot_shape), _i32, ctypes.POINTER(_u64)]),
+    "rot_partition_static": (_i32, [ctypes.POINTER(_u64), _i32, ctypes.POINTER(_i32), _i32, _i32,
+                                    ctypes.POINTER(_i32)]),
+    "rot_partition_alpha": (_i32, [ctypes.POINTER(_u64), _i32, ctypes.POINTER(_i32), _i32, _i32,
+                                   ctypes.c_double, ctypes.POINTER(_i32), ctypes.POINTER(_u64)]),
 }
 
 
@@ -162,6 +167,38 @@ class Plan:
         _check(lib().rot_state_bytes(self.handle, ctypes.byref(s), ctypes.byref(w)),
                "rot_state_bytes")
         return s.value, w.value
+
+
+def item_work(shapes: Sequence[Tuple[int, int]]) -> List[int]:
+    """rot_item_work: the planner's cost of each m x n matrix."""
+    n = len(shapes)
+    arr = (rot_shape * max(n, 1))(*[rot_shape(m, k) for m, k in shapes])
+    out = (_u64 * max(n, 1))()
+    _check(lib().rot_item_work(arr, n, out), "rot_item_work")
+    return [out[i] for i in range(n)]
+
+
+def partition_static(elems: Sequence[int], bucket_sizes: Sequence[int], ranks: int) -> List[int]:
+    """rot_partition_static: owner of every item by its start in its bucket."""
+    n, nb = len(elems), len(bucket_sizes)
+    e = (_u64 * max(n, 1))(*elems)
+    b = (_i32 * max(nb, 1))(*bucket_sizes)
+    out = (_i32 * max(n, 1))()
+    _check(lib().rot_partition_static(e, n, b, nb, ranks, out), "rot_partition_static")
+    return [out[i] for i in range(n)]
+
+
+def partition_alpha(work: Sequence[int], bucket_sizes: Sequence[int], ranks: int,
+                    alpha: float) -> Tuple[List[int], List[int]]:
+    """rot_partition_alpha: (owner of every item, total work per rank)."""
+    n, nb = len(work), len(bucket_sizes)
+    w = (_u64 * max(n, 1))(*work)
+    b = (_i32 * max(nb, 1))(*bucket_sizes)
+    out = (_i32 * max(n, 1))()
+    loads = (_u64 * max(ranks, 1))()
+    _check(lib().rot_partition_alpha(w, n, b, nb, ranks, float(alpha), out, loads),
+           "rot_partition_alpha")
+    return [out[i] for i in range(n)], [loads[r] for r in range(ranks)]
 
 
 def rot_set_wait_timeout_ns(ns: int) -> int:

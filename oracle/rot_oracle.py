@@ -9,7 +9,9 @@ Sources (page titles as published):
 * Canzona page ("Canzona" matrix-optimizer framework, aitangshan.cn), section
   3.2.2 "微组调度算法": global LPT sort by compute cost, then greedy grouping
   with rollback, a min-heap load simulation and a byte cap per micro-group
-  (section 6.1 / the 3.2.2 tip give 512 MB as a typical cap).
+  (section 6.1 / the 3.2.2 tip give 512 MB as a typical cap); section 3.2.1
+  (the α-balanced greedy LPT partition of data-parallel buckets) and 3.1.1
+  (static ownership by parameter start).
 * "分布式训练中的流水线并行与梯度陈旧性优化", section 2.1 (the per-coordinate
   Adam update m/(sqrt(v)+eps), no bias correction) and section 2.2 (momentum
   kept as an m x n matrix; power iteration plus QR every K iterations; the
@@ -107,6 +109,109 @@ def plan(shapes: Sequence[Tuple[int, int]], c_max: int, ranks: int = 1) -> Plan:
     return Plan(groups=groups, owners=owners,
                 group_bytes=[sum(nbytes[i] for i in g) for g in groups],
                 group_cost=[sum(cost[i] for i in g) for g in groups])
+
+
+# ---------------------------------------------------------------------------
+# Data-parallel partition (Canzona page, section 3.2.1 "α平衡贪心LPT算法",
+# and section 3.1.1 for the static baseline)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Partition:
+    owners: List[int]   # rank of every item (input order)
+    loads: List[int]    # total work per rank
+
+
+def static_partition(elems: Sequence[int], bucket_sizes: Sequence[int], ranks: int) -> List[int]:
+    """Ownership by parameter start (section 3.1.1), bucket by bucket as a
+    ZeRO-1 flat buffer is sharded: bucket b's items lie back to back in E_b =
+    sum of their elements, cut into `ranks` equal shards of S_b = ceil(E_b /
+    ranks) elements; an item belongs to the shard holding its first element."""
+    if sum(bucket_sizes) != len(elems):
+        raise ValueError("bucket sizes must cover the items")
+    owners, i = [], 0
+    for c in bucket_sizes:
+        total = sum(elems[i:i + c])
+        shard = max(1, -(-total // ranks))
+        start = 0
+        for e in elems[i:i + c]:
+            owners.append(min(ranks - 1, start // shard))
+            start += e
+        i += c
+    return owners
+
+
+def alpha_partition(work: Sequence[int], bucket_sizes: Sequence[int], ranks: int,
+                    alpha: float) -> Partition:
+    """α-balanced greedy LPT partition of buckets of items (section 3.2.1).
+
+    Items lie in physical order; bucket b is the next bucket_sizes[b] of them
+    and its work W_b is the sum of its items' work.
+    1. Visit the buckets by W_b, largest first (equal W_b: lower index first).
+    2. For the bucket at hand, with per-rank loads L so far: the ideal load is
+       A = (sum(L) + W_b) / R (the even share once this bucket is placed);
+       deficit d_r = max(0, A - L_r); fill shares v_fill = d / sum(d) (1/R each
+       if every deficit is zero); even shares 1/R; mixed shares
+       v*_r = (1 - alpha) / R + alpha * v_fill_r.
+    3. The bucket is cut into R consecutive pieces, rank r taking piece r.  Cut
+       r (after rank r's piece) is the item boundary j whose prefix work P_j is
+       nearest to W_b * (v*_0 + ... + v*_r); on a tie the earlier boundary.
+       Cuts therefore fall on item boundaries only (no item is split).
+    4. Each rank's load grows by the work of its piece.
+    Floating-point steps are done in float64 in exactly this order; prefix
+    work and loads are exact integers.
+    """
+    if ranks < 1:
+        raise ValueError("ranks must be >= 1")
+    if sum(bucket_sizes) != len(work):
+        raise ValueError("bucket sizes must cover the items")
+    starts, s = [], 0
+    for c in bucket_sizes:
+        starts.append(s)
+        s += c
+    bwork = [sum(work[starts[b]:starts[b] + bucket_sizes[b]]) for b in range(len(bucket_sizes))]
+    order = sorted(range(len(bucket_sizes)), key=lambda b: (-bwork[b], b))
+    owners = [-1] * len(work)
+    loads = [0] * ranks
+    for b in order:
+        items = list(range(starts[b], starts[b] + bucket_sizes[b]))
+        ideal = float(sum(loads) + bwork[b]) / float(ranks)
+        deficit = [max(0.0, ideal - float(l)) for l in loads]
+        dsum = 0.0
+        for d in deficit:
+            dsum += d
+        if dsum > 0.0:
+            fill = [d / dsum for d in deficit]
+        else:
+            fill = [1.0 / float(ranks)] * ranks
+        share = [(1.0 - alpha) / float(ranks) + alpha * f for f in fill]
+        prefix = [0]
+        for i in items:
+            prefix.append(prefix[-1] + work[i])
+        cuts, cum = [], 0.0
+        for r in range(ranks - 1):
+            cum += share[r]
+            target = float(bwork[b]) * cum
+            best = 0
+            for j in range(len(prefix)):
+                if abs(float(prefix[j]) - target) < abs(float(prefix[best]) - target):
+                    best = j
+            cuts.append(best)
+        cuts.append(len(items))
+        lo = 0
+        for r in range(ranks):
+            hi = max(lo, cuts[r])
+            for j in range(lo, hi):
+                owners[items[j]] = r
+            loads[r] += prefix[hi] - prefix[lo]
+            lo = hi
+    return Partition(owners=owners, loads=loads)
+
+
+def imbalance(values: Sequence[float]) -> float:
+    """max / mean of per-rank totals (1.0 = perfectly even)."""
+    mean = sum(values) / len(values)
+    return max(values) / mean if mean > 0 else 1.0
 
 
 # ---------------------------------------------------------------------------
