@@ -243,25 +243,54 @@ def run_ours(args):
         ms = float(tt.item())
         dist.barrier()
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Each step's
+    # gradients come from pinned host memory and its updated W goes back to
+    # pinned host memory.  The next step's gradients are copied in on a side
+    # stream while the current step computes (two device buffers); W's copy out
+    # runs on another side stream, and the next step waits for it because it
+    # updates W in place.
     e_steps = 0 if args.no_e2e else max(1, min(args.steps, 5))
     g_host = [g.cpu().pin_memory() for g in Gsets[0]] if e_steps else []
     w_host = [w.cpu().pin_memory() for w in W] if e_steps else []
-    g_dev = [torch.empty_like(g) for g in Gsets[0]] if e_steps else []
+    g_dev = [[torch.empty_like(g) for g in Gsets[0]] for _ in range(2)] if e_steps else []
     h2d = sum(g.numel() * 4 for g in g_host)
     d2h = sum(w.numel() * 4 for w in w_host)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     x0 = torch.cuda.Event(enable_timing=True)
     x1 = torch.cuda.Event(enable_timing=True)
-    x0.record(stream)
-    for _ in range(e_steps):
-        for gd, gh in zip(g_dev, g_host):
-            gd.copy_(gh, non_blocking=True)
-        step(g_dev)
-        for wh, wd in zip(w_host, W):
-            wh.copy_(wd, non_blocking=True)
+    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_done = [torch.cuda.Event() for _ in range(max(e_steps, 1))]
+    ev_out = [torch.cuda.Event() for _ in range(max(e_steps, 1))]
+    x0.record(s_in)
+    if e_steps:
+        with torch.cuda.stream(s_in):
+            for gd, gh in zip(g_dev[0], g_host):
+                gd.copy_(gh, non_blocking=True)
+        ev_in[0].record(s_in)
+    for i in range(e_steps):
+        stream.wait_event(ev_in[i % 2])
+        if i > 0:
+            stream.wait_event(ev_out[i - 1])
+        step(g_dev[i % 2])
+        ev_done[i].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[i])
+            for wh, wd in zip(w_host, W):
+                wh.copy_(wd, non_blocking=True)
+        ev_out[i].record(s_out)
+        if i + 1 < e_steps:
+            with torch.cuda.stream(s_in):
+                if i > 0:
+                    s_in.wait_event(ev_done[i - 1])  # buffer (i+1)%2 last read by step i-1
+                for gd, gh in zip(g_dev[(i + 1) % 2], g_host):
+                    gd.copy_(gh, non_blocking=True)
+            ev_in[(i + 1) % 2].record(s_in)
+    if e_steps:
+        stream.wait_event(ev_out[e_steps - 1])
     x1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = x0.elapsed_time(x1) if e_steps else 0.0

@@ -392,27 +392,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // Precise 3xTF32 variant (BN = 128).  The tensor cores truncate every partial
 // sum they add into a TMEM accumulator, an error that grows with K and that
 // cancellation (a - Y T Y^T a with a small result) then magnifies.  Here each
-// K block of 32 is accumulated afresh: hi*hi into one TMEM accumulator and the
-// cross terms hi*lo + lo*hi into another, and the epilogue warps add both to a
-// float32 running sum held in registers (round to nearest), one K block at a
-// time, double-buffered against the MMAs of the next block.
-// TMEM: 2 buffers x (hi*hi, cross) x 128 columns = 512 columns.
+// K block of 32 is accumulated afresh in TMEM and the epilogue warps add it to
+// a float32 running sum held in registers (round to nearest).  Within a block
+// the cross terms hi*lo + lo*hi (2^-11 of the result) are issued first and the
+// four hi*hi MMAs last, so only those four adds truncate at the result's
+// magnitude -- the same count as with a separate hi*hi accumulator, at half
+// the TMEM reads.
+// TMEM: 4 K-block buffers x 128 columns = 512 columns.  Eight epilogue warps:
+// warp w reads TMEM lanes 32 (w % 4) .. +31 and columns 64 ((w - 2) / 4) .. +63.
 // ---------------------------------------------------------------------------
 
+constexpr int kThreadsPrecise = 320;
+constexpr int kPreciseBufs = 4;
+constexpr int kPreciseEpiWarps = 8;
+
 template <int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsPrecise, 1)
     gemm_tc_precise_kernel(const __grid_constant__ TcBatch b) {
   constexpr int BN = 128;
+  constexpr int kHalf = BN / 2;  // columns per epilogue warp
   using C = Cfg<BN, STAGES, true>;
   constexpr uint32_t kCols = 512;
+  static_assert(kPreciseBufs * BN == kCols, "TMEM budget");
+  static_assert((2 * STAGES + 2 * kPreciseBufs + 1) * 8 + 8 <= 256, "barrier area");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + kPreciseBufs;
+  uint64_t* drain = tempty + kPreciseBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -424,9 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kPreciseBufs; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 4);
+      ptx::mbar_init(&tempty[a], kPreciseEpiWarps);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -491,26 +501,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode(b, tile, pi, m0, nt);
       const int kblocks = (b.p[pi].K + BK - 1) / BK;
       for (int kb = 0; kb < kblocks; ++kb, ++chunk) {
-        const uint32_t buf = chunk & 1u, use = chunk >> 1;
+        const uint32_t buf = chunk % kPreciseBufs, use = chunk / kPreciseBufs;
         if (!ptx::mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, limit) ||
             !ptx::mbar_wait(&full[stage], phase, abort_flag, limit)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_big = tmem_base + buf * 256u, d_small = d_big + 128u;
+        const uint32_t d = tmem_base + buf * BN;
         const uint32_t s = ptx::smem_u32(smem + stage * C::kStageBytes);
         const uint64_t ah = ptx::sw128_kmajor_desc(s);
         const uint64_t al = ptx::sw128_kmajor_desc(s + C::kABytes);
         const uint64_t bh = ptx::sw128_kmajor_desc(s + 2 * C::kABytes);
         const uint64_t bl = ptx::sw128_kmajor_desc(s + 2 * C::kABytes + C::kBBytes);
 #pragma unroll
-        for (int kk = 0; kk < BK / 8; ++kk) {
+        for (int kk = 0; kk < BK / 8; ++kk) {  // cross terms first ...
           const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);
-          const uint32_t accum = kk > 0 ? 1u : 0u;
-          ptx::umma_tf32(d_small, ah + off, bl + off, idesc, accum);
-          ptx::umma_tf32(d_small, al + off, bh + off, idesc, 1u);
-          ptx::umma_tf32(d_big, ah + off, bh + off, idesc, accum);
+          ptx::umma_tf32(d, ah + off, bl + off, idesc, kk > 0 ? 1u : 0u);
+          ptx::umma_tf32(d, al + off, bh + off, idesc, 1u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {  // ... then hi*hi
+          const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);
+          ptx::umma_tf32(d, ah + off, bh + off, idesc, 1u);
         }
         ptx::umma_commit(&empty[stage]);
         ptx::umma_commit(&tfull[buf]);
@@ -525,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t chunk = 0;
     bool ok = true;
@@ -534,39 +548,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TcProblem& P = b.p[pi];
       const int n0 = nt * BN;
       const int kblocks = (P.K + BK - 1) / BK;
-      float acc[BN];
+      float acc[kHalf];
 #pragma unroll
-      for (int c = 0; c < BN; ++c) acc[c] = 0.f;
+      for (int c = 0; c < kHalf; ++c) acc[c] = 0.f;
       for (int kb = 0; kb < kblocks; ++kb, ++chunk) {
-        const uint32_t buf = chunk & 1u, use = chunk >> 1;
+        const uint32_t buf = chunk % kPreciseBufs, use = chunk / kPreciseBufs;
         if (!ptx::mbar_wait(&tfull[buf], use & 1u, abort_flag, limit)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t t_big = tmem_base + lane_off + buf * 256u;
-#pragma unroll
-        for (int h = 0; h < 2 * (BN / 32); ++h) {  // hi*hi chunks, then cross-term chunks
-          const int q = h % (BN / 32);
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(t_big + (h < BN / 32 ? 0u : 128u) + q * 32, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int t = 0; t < 32; ++t) acc[q * 32 + t] += __uint_as_float(r[t]);
-        }
+        const uint32_t t = tmem_base + lane_off + buf * BN + half * kHalf;
+        uint32_t r0[32], r1[32];
+        ptx::tmem_ld_32x32b_x32(t, r0);
+        ptx::tmem_ld_32x32b_x32(t + 32, r1);
+        ptx::tmem_wait_ld();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          acc[c] += __uint_as_float(r0[c]);
+          acc[32 + c] += __uint_as_float(r1[c]);
+        }
       }
       if (!ok) break;
       const int row = m0 + quarter * 32 + lane;
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        if (n0 + q * 32 < P.N) {
+      for (int q = 0; q < kHalf / 32; ++q) {
+        const int col0 = n0 + half * kHalf + q * 32;
+        if (col0 < P.N) {
           uint32_t r[32];
 #pragma unroll
-          for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(acc[q * 32 + t]);
-          store_chunk(P, row, n0 + q * 32, r);
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(acc[q * 32 + c]);
+          store_chunk(P, row, col0, r);
         }
       }
     }
@@ -676,7 +691,7 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
     const int grid = std::min(total, num_sms());
     {
       ProfScope prof(PRECISE ? ROT_PROF_GEMM_PRECISE : ROT_PROF_GEMM, flops, stream);
-      kernel<<<grid, kThreads, C::kSmem, stream>>>(b);
+      kernel<<<grid, PRECISE ? kThreadsPrecise : kThreads, C::kSmem, stream>>>(b);
     }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
   }

@@ -680,13 +680,13 @@ int configure_panel(size_t smem) {
 
 // Cluster size for the panel kernel: at least enough CTAs that a slice of
 // the panel fits in shared memory (<= 1536 elements x 32 rows = 192 KB); then
-// the largest size (up to 16, each CTA keeping >= 256 elements) at which
+// the largest size (up to 16, each CTA keeping >= 640 elements) at which
 // every cluster of the batch can be resident at once.
 int pick_cluster(int count, int pmax, int sms) {
   const int lo = std::max(1, (pmax + 1535) / 1536);
   int best = std::min(lo, kMaxCluster);
   for (int cs = best; cs <= kMaxCluster; ++cs) {
-    if (cs > lo && pmax / cs < 256) break;
+    if (cs > lo && pmax / cs < 640) break;  // small slices: cluster barriers dominate
     if (cs * count > sms) break;
     const size_t smem = sizeof(float) * (size_t)B * panel_slice(pmax, cs);
     if (configure_panel(smem) != ROT_OK) break;
