@@ -59,8 +59,11 @@ extern "C" {
 #define ROT_PREC_TF32 1      /* one TF32 tensor-core product per GEMM */
 #define ROT_PREC_3XTF32 3    /* hi*hi + hi*lo + lo*hi TF32 split, ~fp32 accuracy */
 #define ROT_PREC_3XTF32_PRECISE 4 /* 3xTF32 with each K block of 32 summed in float32
-                                     registers and hi*hi kept apart from the cross
-                                     terms: float32-level accuracy at any K */
+                                     registers: float32-level accuracy at any K */
+#define ROT_PREC_3XF16 5     /* the three split products on power-of-two-scaled fp16
+                                splits (11 + 11 significant bits, as 3XTF32) at twice
+                                the TF32 tensor-core rate; basis refresh products
+                                stay 3XTF32_PRECISE */
 
 #define ROT_MAX_DIM 65536
 
@@ -171,8 +174,10 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream);
  * row-major, float32) is updated in place, G[i] is read only.  state: the
  * initialised state blob; work: the workspace blob.  refresh != 0 runs the
  * basis refresh (2) before the rotated update.  precision of the rotation
- * products: ROT_PREC_TF32, ROT_PREC_3XTF32 or ROT_PREC_3XTF32_PRECISE (the
- * basis refresh always uses ROT_PREC_3XTF32_PRECISE).  rank_rtol in
+ * products: ROT_PREC_TF32, ROT_PREC_3XTF32, ROT_PREC_3XTF32_PRECISE or
+ * ROT_PREC_3XF16 (the basis refresh always uses ROT_PREC_3XTF32_PRECISE, and
+ * in 3XF16 mode the refresh-step product U^T M V uses 3XTF32).  The mode may
+ * change from step to step.  rank_rtol in
  * [1e-6, 1): the QR's numerical-rank threshold relative to the largest
  * column norm.  Non-finite inputs propagate (IEEE).
  * Errors: ROT_EINVAL (null pointers, unknown precision, rank_rtol out of
@@ -237,7 +242,8 @@ uint64_t rot_set_wait_timeout_ns(uint64_t ns);
 #define ROT_PROF_QR_APPLY 3    /* QR block-reflector updates; work = flops (32-wide panels) */
 #define ROT_PROF_QR_OTHER 4    /* QR set-up, column norms, identity, sign fix; work = 0 */
 #define ROT_PROF_GEMM_PRECISE 5 /* precise 3xTF32 GEMM (refresh products, QR blocks) */
-#define ROT_PROF_CLASSES 6
+#define ROT_PROF_GEMM_F16 6    /* 3xF16 tensor-core GEMM; work = 2 M N K flops */
+#define ROT_PROF_CLASSES 7
 
 /* Turn event recording on (on != 0) or off.  Returns ROT_OK. */
 int rot_profile_enable(int32_t on);

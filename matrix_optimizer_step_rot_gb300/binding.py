@@ -30,6 +30,7 @@ ROT_NOALLOC_MAX_BYTES = 64 << 20
 ROT_PREC_TF32 = 1
 ROT_PREC_3XTF32 = 3
 ROT_PREC_3XTF32_PRECISE = 4
+ROT_PREC_3XF16 = 5
 ROT_WHICH_M, ROT_WHICH_V2, ROT_WHICH_U, ROT_WHICH_V = 0, 1, 2, 3
 
 

@@ -101,6 +101,153 @@ __global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float b
   }
 }
 
+// Sum and max over the block (256 threads); every thread gets both.
+__device__ __forceinline__ void block_sum_max(float& sum, float& mx) {
+  __shared__ float ssum[kThreads / 32], smax[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  __syncthreads();  // the previous row's readers are done with ssum / smax
+  if (lane == 0) {
+    ssum[warp] = sum;
+    smax[warp] = mx;
+  }
+  __syncthreads();
+  sum = 0.f;
+  mx = 0.f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    sum += ssum[w];
+    mx = fmaxf(mx, smax[w]);
+  }
+}
+
+// Upper bound on a row's 2-norm from its sum of squares and max |x|: the sum
+// may overflow float32 for finite rows, then sqrt(cols) max|x| bounds it.
+__device__ __forceinline__ float row_norm_bound(float sum, float mx, int cols) {
+  const float rn = sqrtf(sum);
+  return (rn <= 3.402823466e38f || !(mx <= 3.402823466e38f)) ? rn : mx * sqrtf((float)cols);
+}
+
+// Non-negative float maximum through its bit pattern (monotone for x >= 0;
+// a NaN wins, so that non-finite values reach the scale logic).
+__device__ __forceinline__ void atomic_max_nonneg(float* slot, float x) {
+  atomicMax(reinterpret_cast<int*>(slot), __float_as_int(x));
+}
+
+// 3xF16 momentum: one block per row (blockIdx.x strides over rows).  First
+// pass: M's update and the row's max |g| and sum g^2; second pass (G re-read,
+// from L2): the scaled fp16 split of G.
+__global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg> b,
+                                  float beta1) {
+  const Momentum16Seg& s = b.seg[blockIdx.y];
+  const float one_minus = 1.0f - beta1;
+  for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
+    const float* g = s.g + (int64_t)r * s.cols;
+    float sum = 0.f, mx = 0.f;
+    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+      const int64_t o = (int64_t)r * s.ldm + c;
+      const float x = g[c];
+      const float m = beta1 * (s.m_hi[o] + s.m_lo[o]) + one_minus * x;
+      float h, l;
+      split_tf32(m, h, l);
+      s.m_hi[o] = h;
+      s.m_lo[o] = l;
+      sum = fmaf(x, x, sum);
+      mx = fmaxf(mx, fabsf(x));
+    }
+    block_sum_max(sum, mx);
+    const float scale = pow2_below(mx, kF16ScaleExp);
+    if (threadIdx.x == 0) {
+      s.g_rinv[r] = pow2_below_inv(mx, kF16ScaleExp);
+      atomic_max_nonneg(s.g_rmax, row_norm_bound(sum, mx, s.cols));
+    }
+    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+      const int64_t o = (int64_t)r * s.ldm + c;
+      split_f16(g[c] * scale, s.g_hi[o], s.g_lo[o]);
+    }
+  }
+}
+
+// 3xF16 Adam: one block per row.  First pass as adam_kernel (M~, v; D's row
+// max and sum of squares); second pass recomputes D from the M~ and v this
+// thread just wrote (bitwise the same values) and stores its scaled split.
+__global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, float beta1,
+                              float beta2, float eps, int incremental) {
+  const Adam16Seg& s = b.seg[blockIdx.y];
+  const float one_minus1 = 1.0f - beta1;
+  const float one_minus = 1.0f - beta2;
+  for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
+    float sum = 0.f, mx = 0.f;
+    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+      const int64_t o = (int64_t)r * s.ld + c;
+      const float g = s.gt[o];
+      float m = s.mt[o];
+      if (incremental) {
+        m = beta1 * m + one_minus1 * g;
+        s.mt[o] = m;
+      }
+      const float v = beta2 * s.v[o] + one_minus * (g * g);
+      s.v[o] = v;
+      const float d = m / (sqrtf(v) + eps);
+      sum = fmaf(d, d, sum);
+      mx = fmaxf(mx, fabsf(d));
+    }
+    block_sum_max(sum, mx);
+    const float scale = pow2_below(mx, kF16ScaleExp);
+    if (threadIdx.x == 0) {
+      s.d_rinv[r] = pow2_below_inv(mx, kF16ScaleExp);
+      atomic_max_nonneg(s.d_rmax, row_norm_bound(sum, mx, s.cols));
+    }
+    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+      const int64_t o = (int64_t)r * s.ld + c;
+      const float d = s.mt[o] / (sqrtf(s.v[o]) + eps);
+      split_f16(d * scale, s.d_hi[o], s.d_lo[o]);
+    }
+  }
+}
+
+// Scaled fp16 split of a float32 matrix, one block per row: per-row scales
+// (rinv set) or one scale from *bound; rmax (if set) grows to the largest row
+// 2-norm.  hi == nullptr: norms only.
+__global__ void split16_kernel(const __grid_constant__ SegBatch<Split16Seg> b) {
+  const Split16Seg& s = b.seg[blockIdx.y];
+  for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
+    const float* x = s.src + (int64_t)r * s.ld_src;
+    float sum = 0.f, mx = 0.f;
+    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+      sum = fmaf(x[c], x[c], sum);
+      mx = fmaxf(mx, fabsf(x[c]));
+    }
+    block_sum_max(sum, mx);
+    const float scale = s.bound ? pow2_below(*s.bound, kF16ScaleExp) : pow2_below(mx, kF16ScaleExp);
+    if (threadIdx.x == 0) {
+      if (s.rinv) s.rinv[r] = pow2_below_inv(mx, kF16ScaleExp);
+      if (s.rmax) atomic_max_nonneg(s.rmax, row_norm_bound(sum, mx, s.cols));
+    }
+    if (s.hi)
+      for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+        const int64_t o = (int64_t)r * s.ld_dst + c;
+        split_f16(x[c] * scale, s.hi[o], s.lo[o]);
+      }
+  }
+}
+
+__global__ void to_f16_kernel(const __grid_constant__ SegBatch<ToF16Seg> b) {
+  const ToF16Seg& s = b.seg[blockIdx.y];
+  const int64_t total = (int64_t)s.rows * s.cols;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
+    const int64_t i = (int64_t)r * s.ld_src + c;
+    const int64_t o = (int64_t)r * s.ld_dst + c;
+    split_f16((s.s_hi[i] + s.s_lo[i]) * kF16UnitScale, s.hi[o], s.lo[o]);
+  }
+}
+
 // Tiled transpose through shared memory (32 x 32 tiles, padded against bank
 // conflicts).  blockIdx.y = matrix, blockIdx.x strides over tiles.
 __global__ void transpose_kernel(const __grid_constant__ SegBatch<TransposeSeg> b) {
@@ -195,6 +342,50 @@ int launch_adam(const std::vector<AdamSeg>& segs, float beta1, float beta2, floa
   // read G~, M~, v (12); write v (4) and D's split (8); incremental: write M~ (4)
   return launch_segs(segs, incremental ? 28.0 : 24.0, adam_kernel, stream, beta1, beta2, eps,
                      incremental);
+}
+
+// One block per row: grid.x covers the rows (up to 1024 blocks per matrix).
+template <class Seg, class Kernel, class... Args>
+int launch_rows(const std::vector<Seg>& segs, double bytes_per_elem, Kernel kernel,
+                cudaStream_t stream, Args... args) {
+  for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
+    SegBatch<Seg> b;
+    std::memset(&b, 0, sizeof(b));
+    b.count = (int)std::min<size_t>(kMaxSegs, segs.size() - base);
+    int most = 0;
+    double elems = 0.0;
+    for (int i = 0; i < b.count; ++i) {
+      b.seg[i] = segs[base + i];
+      if (b.seg[i].cols > 0) most = std::max(most, b.seg[i].rows);
+      elems += (double)b.seg[i].rows * b.seg[i].cols;
+    }
+    if (most == 0) continue;
+    dim3 grid((unsigned)std::min(most, 1024), b.count);
+    ProfScope prof(ROT_PROF_ELEMENTWISE, elems * bytes_per_elem, stream);
+    kernel<<<grid, kThreads, 0, stream>>>(b, args...);
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+  }
+  return ROT_OK;
+}
+
+int launch_momentum16(const std::vector<Momentum16Seg>& segs, float beta1, cudaStream_t stream) {
+  // read G (4) and M's split (8); write M's split (8) and G's fp16 split (4)
+  return launch_rows(segs, 24.0, momentum16_kernel, stream, beta1);
+}
+
+int launch_adam16(const std::vector<Adam16Seg>& segs, float beta1, float beta2, float eps,
+                  int incremental, cudaStream_t stream) {
+  // read G~, M~, v (12); write v (4) and D's fp16 split (4); incremental: write M~ (4)
+  return launch_rows(segs, incremental ? 24.0 : 20.0, adam16_kernel, stream, beta1, beta2, eps,
+                     incremental);
+}
+
+int launch_split16(const std::vector<Split16Seg>& segs, cudaStream_t stream) {
+  return launch_rows(segs, 8.0, split16_kernel, stream);
+}
+
+int launch_to_f16(const std::vector<ToF16Seg>& segs, cudaStream_t stream) {
+  return launch_segs(segs, 12.0, to_f16_kernel, stream);
 }
 
 int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream) {

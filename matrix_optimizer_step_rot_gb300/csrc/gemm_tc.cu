@@ -4,7 +4,10 @@
 //
 // ROT_PREC_3XTF32 issues three kind::tf32 MMAs per K step (hi*lo, lo*hi,
 // hi*hi) and recovers about float32 accuracy; ROT_PREC_TF32 issues one
-// (hi*hi).  Accumulation is float32 in TMEM either way.
+// (hi*hi).  ROT_PREC_3XF16 issues the same three products on power-of-two
+// scaled fp16 splits (kind::f16, twice the TF32 rate, 22 significant bits as
+// well); its operands are fp16 arrays and its epilogue undoes the scaling.
+// Accumulation is float32 in TMEM in every mode.
 //
 // Structure: a persistent kernel, one CTA per SM, walks the flattened tile
 // list of every problem in the launch.  Per CTA:
@@ -49,6 +52,13 @@ struct TcProblem {
   int mma_only;
   float* c_hi;
   float* c_lo;
+  // 3xF16 scaling (powers of two): the accumulator is multiplied by
+  // c0 * row_inv[row] (if set) / pow2_below(*in_r) (if set); fp16 split
+  // outputs are then multiplied by pow2_below(*out_r) (if set).
+  const float* row_inv;
+  const float* in_r;
+  const float* out_r;
+  float c0;
 };
 
 struct TcBatch {
@@ -217,9 +227,31 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
   }
 }
 
-template <int BN, int STAGES, bool SPLIT3>
+// kEpiStoreF16SplitT: C^T (N x M fp16 rows, ldc elements) <- fp16 split of
+// acc * f; the warp's 32 lanes (32 consecutive rows i) write 64 contiguous
+// bytes per column.
+__device__ __forceinline__ void store_chunk_f16t(const TcProblem& P, int row, int col0,
+                                                 const uint32_t (&r)[32], float f) {
+  if (row >= P.M) return;
+  const int ncol = min(32, P.N - col0);
+  unsigned short* hi = reinterpret_cast<unsigned short*>(P.c_hi);
+  unsigned short* lo = reinterpret_cast<unsigned short*>(P.c_lo);
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    if (t < ncol) {
+      unsigned short h, l;
+      split_f16(__uint_as_float(r[t]) * f, h, l);
+      const int64_t o = (int64_t)(col0 + t) * P.ldc + row;
+      hi[o] = h;
+      lo[o] = l;
+    }
+  }
+}
+
+template <int BN, int STAGES, bool SPLIT3, bool F16 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcBatch b) {
   using C = Cfg<BN, STAGES, SPLIT3>;
+  constexpr int BKE = F16 ? 2 * BK : BK;  // elements per 128-byte K block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -271,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       decode(b, tile, pi, m0, nt);
       const TcProblem& P = b.p[pi];
       const int n0 = nt * BN;
-      const int kblocks = (P.K + BK - 1) / BK;
+      const int kblocks = (P.K + BKE - 1) / BKE;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit)) {
           ok = false;
@@ -281,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
         armed_mask |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        const int x = kb * BK;
+        const int x = kb * BKE;
         ptx::tma_load_2d(st, &P.a_hi, &full[stage], x, m0);
         if (SPLIT3) {
           ptx::tma_load_2d(st + C::kABytes, &P.a_lo, &full[stage], x, m0);
@@ -301,7 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       if (armed_mask & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u, limit);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issue
-    constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
+    constexpr uint32_t idesc = F16 ? ptx::idesc_f16(BM, BN) : ptx::idesc_tf32(BM, BN);
+    auto mma = [&](uint32_t d, uint64_t a, uint64_t bb, uint32_t accum) {
+      if (F16) {
+        ptx::umma_f16(d, a, bb, idesc, accum);
+      } else {
+        ptx::umma_tf32(d, a, bb, idesc, accum);
+      }
+    };
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -310,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
       int pi, m0, nt;
       decode(b, tile, pi, m0, nt);
-      const int kblocks = (b.p[pi].K + BK - 1) / BK;
+      const int kblocks = (b.p[pi].K + BKE - 1) / BKE;
       if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, limit)) break;
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -326,15 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const uint64_t bh = ptx::sw128_kmajor_desc(s + (SPLIT3 ? 2 : 1) * C::kABytes);
         const uint64_t bl = ptx::sw128_kmajor_desc(s + 2 * C::kABytes + C::kBBytes);
 #pragma unroll
-        for (int kk = 0; kk < BK / 8; ++kk) {
-          const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);  // 8 tf32 = 32 bytes
+        for (int kk = 0; kk < BK / 8; ++kk) {  // 32 bytes per step: 8 tf32 or 16 fp16
+          const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);
           const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
           if (SPLIT3) {
-            ptx::umma_tf32(d_tmem, ah + off, bl + off, idesc, accum);
-            ptx::umma_tf32(d_tmem, al + off, bh + off, idesc, 1u);
-            ptx::umma_tf32(d_tmem, ah + off, bh + off, idesc, 1u);
+            mma(d_tmem, ah + off, bl + off, accum);
+            mma(d_tmem, al + off, bh + off, 1u);
+            mma(d_tmem, ah + off, bh + off, 1u);
           } else {
-            ptx::umma_tf32(d_tmem, ah + off, bh + off, idesc, accum);
+            mma(d_tmem, ah + off, bh + off, accum);
           }
         }
         ptx::umma_commit(&empty[stage]);  // frees the stage once these MMAs finish
@@ -366,11 +405,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       const int row = m0 + quarter * 32 + lane;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      float f = 1.f, fout = 1.f;
+      if (F16) {  // undo the operands' power-of-two scales (exact)
+        f = P.c0;
+        if (P.row_inv && row < P.M) f *= P.row_inv[row];
+        if (P.in_r) f *= pow2_below_inv(*P.in_r, kF16ScaleExp);
+        if (P.out_r) fout = pow2_below(*P.out_r, kF16ScaleExp);
+      }
       for (int c = 0; c < BN && n0 + c < P.N; c += 32) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c), r);
         ptx::tmem_wait_ld();
-        store_chunk(P, row, n0 + c, r);
+        if (F16 && P.epi == kEpiStoreF16SplitT) {
+          store_chunk_f16t(P, row, n0 + c, r, f * fout);
+        } else {
+          if (F16) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * f);
+          }
+          store_chunk(P, row, n0 + c, r);
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -613,15 +667,19 @@ int get_encoder() {
   return ROT_OK;
 }
 
-// Row-major rows x K float32 matrix (leading dimension ld), boxes of
-// box_rows x 32 with 128-byte swizzle; out-of-range elements read as 0.
-int encode(CUtensorMap* map, const float* base, int rows, int K, int ld, int box_rows) {
-  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld & 3)) return ROT_EINVAL;
+// Row-major rows x K matrix (leading dimension ld elements) of float32 or
+// fp16, boxes of box_rows x 128 bytes with 128-byte swizzle; out-of-range
+// elements read as 0.
+int encode(CUtensorMap* map, const float* base, int rows, int K, int ld, int box_rows,
+           bool f16 = false) {
+  const int esize = f16 ? 2 : 4;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || ((int64_t)ld * esize) % 16) return ROT_EINVAL;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
+  CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        2, const_cast<float*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -639,11 +697,12 @@ int num_sms() {
   return n;
 }
 
-template <int BN, int STAGES, bool SPLIT3, bool PRECISE = false>
+template <int BN, int STAGES, bool SPLIT3, bool PRECISE = false, bool F16 = false>
 int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stream) {
   using C = Cfg<BN, STAGES, SPLIT3>;
-  static_assert(!PRECISE || (BN == 128 && SPLIT3), "precise variant is 3xTF32, BN = 128");
-  auto kernel = PRECISE ? gemm_tc_precise_kernel<STAGES> : gemm_tc_kernel<BN, STAGES, SPLIT3>;
+  static_assert(!PRECISE || (BN == 128 && SPLIT3 && !F16), "precise variant is 3xTF32, BN = 128");
+  auto kernel =
+      PRECISE ? gemm_tc_precise_kernel<STAGES> : gemm_tc_kernel<BN, STAGES, SPLIT3, F16>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
@@ -661,13 +720,14 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
     while (i < probs.size() && b.count < kMaxP) {
       const GemmProblem& G = probs[i++];
       if (G.M <= 0 || G.N <= 0) continue;
-      if (G.K <= 0) return ROT_EINVAL;
+      if (G.K <= 0 || (G.f16 != 0) != F16) return ROT_EINVAL;
+      if (G.epi == kEpiStoreF16SplitT && !F16) return ROT_EINVAL;
       TcProblem& P = b.p[b.count];
-      if (encode(&P.a_hi, G.a_hi, G.M, G.K, G.lda, BM) != ROT_OK ||
-          encode(&P.b_hi, G.b_hi, G.N, G.K, G.ldb, BN) != ROT_OK)
+      if (encode(&P.a_hi, G.a_hi, G.M, G.K, G.lda, BM, F16) != ROT_OK ||
+          encode(&P.b_hi, G.b_hi, G.N, G.K, G.ldb, BN, F16) != ROT_OK)
         return ROT_EINVAL;
-      if (SPLIT3 && (encode(&P.a_lo, G.a_lo, G.M, G.K, G.lda, BM) != ROT_OK ||
-                     encode(&P.b_lo, G.b_lo, G.N, G.K, G.ldb, BN) != ROT_OK))
+      if (SPLIT3 && (encode(&P.a_lo, G.a_lo, G.M, G.K, G.lda, BM, F16) != ROT_OK ||
+                     encode(&P.b_lo, G.b_lo, G.N, G.K, G.ldb, BN, F16) != ROT_OK))
         return ROT_EINVAL;
       P.M = G.M;
       P.N = G.N;
@@ -680,6 +740,10 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
       P.mma_only = G.mma_only;
       P.c_hi = G.c_hi;
       P.c_lo = G.c_lo;
+      P.row_inv = G.row_inv;
+      P.in_r = G.in_r;
+      P.out_r = G.out_r;
+      P.c0 = G.c0;
       total += ((G.M + BM - 1) / BM) * P.tiles_n;
       flops += 2.0 * G.M * (double)G.N * G.K;
       ++b.count;
@@ -690,7 +754,8 @@ int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stre
     b.limit_ns = g_wait_limit_ns;
     const int grid = std::min(total, num_sms());
     {
-      ProfScope prof(PRECISE ? ROT_PROF_GEMM_PRECISE : ROT_PROF_GEMM, flops, stream);
+      ProfScope prof(PRECISE ? ROT_PROF_GEMM_PRECISE : (F16 ? ROT_PROF_GEMM_F16 : ROT_PROF_GEMM),
+                     flops, stream);
       kernel<<<grid, PRECISE ? kThreadsPrecise : kThreads, C::kSmem, stream>>>(b);
     }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
@@ -725,6 +790,12 @@ int launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream) {
 int gemm_tc(const std::vector<GemmProblem>& probs, int precision, int* status,
             cudaStream_t stream) {
   if (precision == kPrecPrecise) return launch<128, 3, true, true>(probs, status, stream);
+  if (precision == ROT_PREC_3XF16) {
+    bool narrow16 = true;
+    for (const GemmProblem& P : probs) narrow16 = narrow16 && P.N <= 128;
+    return narrow16 ? launch<128, 3, true, false, true>(probs, status, stream)
+                    : launch<256, 2, true, false, true>(probs, status, stream);
+  }
   // narrow products (every N <= 128) use 128-wide tiles so no MMA column is wasted
   bool narrow = true;
   for (const GemmProblem& P : probs) narrow = narrow && P.N <= 128;

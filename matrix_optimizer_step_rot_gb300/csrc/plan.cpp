@@ -108,6 +108,7 @@ struct Cursor {
     return o;
   }
   uint64_t floats(int64_t rows, int64_t ld) { return take(4ull * (uint64_t)rows * (uint64_t)ld); }
+  uint64_t halves(int64_t rows, int64_t ld) { return take(2ull * (uint64_t)rows * (uint64_t)ld); }
 };
 
 }  // namespace
@@ -136,6 +137,14 @@ void build_layout(rot_plan* p) {
     L.vb_lo = s.floats(n, L.ldn);
     L.vt_hi = s.floats(n, L.ldn);
     L.vt_lo = s.floats(n, L.ldn);
+    L.u16_hi = s.halves(m, L.ldm);
+    L.u16_lo = s.halves(m, L.ldm);
+    L.ut16_hi = s.halves(m, L.ldm);
+    L.ut16_lo = s.halves(m, L.ldm);
+    L.vb16_hi = s.halves(n, L.ldn);
+    L.vb16_lo = s.halves(n, L.ldn);
+    L.vt16_hi = s.halves(n, L.ldn);
+    L.vt16_lo = s.halves(n, L.ldn);
   }
   p->state_bytes = s.at;
 
@@ -159,6 +168,15 @@ void build_layout(rot_plan* p) {
       x.sm_lo = w.floats(L.n, L.ldm);
       x.gt = w.floats(L.m, L.ldn);
       x.mt = w.floats(L.m, L.ldn);
+      x.g_rinv = w.floats(1, L.m);
+      x.d_rinv = w.floats(1, L.m);
+    }
+    {
+      const uint64_t norms = w.floats(1, 2 * (int64_t)WL.size());
+      for (size_t k = 0; k < WL.size(); ++k) {
+        WL[k].g_rmax = norms + 8 * k;
+        WL[k].d_rmax = norms + 8 * k + 4;
+      }
     }
     for (size_t k = 0; k < p->groups[g].size(); ++k) {
       const ItemLayout& L = p->items[p->groups[g][k]];

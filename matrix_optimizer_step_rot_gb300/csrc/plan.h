@@ -19,6 +19,10 @@ struct ItemLayout {
   uint64_t mt;                        // M~ = U^T M V (float32), m x ldn
   uint64_t u_hi, u_lo, ut_hi, ut_lo;  // U and U^T splits, m x ldm
   uint64_t vb_hi, vb_lo, vt_hi, vt_lo;  // V and V^T splits, n x ldn
+  // fp16 splits of U, U^T (m x ldm) and V, V^T (n x ldn), scaled by 2^14, for
+  // the 3xF16 rotation products; rewritten whenever the bases change
+  uint64_t u16_hi, u16_lo, ut16_hi, ut16_lo;
+  uint64_t vb16_hi, vb16_lo, vt16_hi, vt16_lo;
 };
 
 // Offsets (bytes from the workspace blob's base) of one matrix's temporaries
@@ -29,6 +33,13 @@ struct WorkLayout {
   uint64_t sg_hi, sg_lo;  // (G V)^T split (n x ldm); later (D V^T)^T split
   uint64_t sm_hi, sm_lo;  // (M V)^T split (n x ldm)
   uint64_t gt, mt;        // G~, M~ float32 (m x ldn)
+  // 3xF16: G's and D's fp16 splits live in g_hi / g_lo, (G V)^T's and
+  // (D V^T)^T's in sg_hi / sg_lo.  Scale slots: per row of G and of D the
+  // inverse of its power-of-two scale (m floats each), and the largest row
+  // 2-norm of G and of D (one float each, set by atomic max; the group's
+  // row-norm slots are contiguous from WorkLayout of its first item's g_rmax,
+  // two floats per item, so one memset clears them).
+  uint64_t g_rinv, d_rinv, g_rmax, d_rmax;
   // refresh region
   uint64_t mT_hi, mT_lo;  // M^T split (n x ldm)
   int zu_rows, zu_ld;

@@ -57,6 +57,40 @@ GemmProblem gp(int M, int N, int K, const float* ah, const float* al, int lda, c
   return P;
 }
 
+constexpr float kF16Inv = 1.f / 16384.f;  // undoes the bases' fixed 2^14 scale
+
+inline unsigned short* H(void* base, uint64_t off) {
+  return reinterpret_cast<unsigned short*>(static_cast<char*>(base) + off);
+}
+
+// A 3xF16 problem: a_*, b_* (and c_* for kEpiStoreF16SplitT) are fp16 arrays.
+GemmProblem gp16(int M, int N, int K, const unsigned short* ah, const unsigned short* al, int lda,
+                 const unsigned short* bh, const unsigned short* bl, int ldb, void* ch, void* cl,
+                 int ldc, int epi, float c0, const float* row_inv, const float* in_r,
+                 const float* out_r, float alpha = 0.f) {
+  GemmProblem P = gp(M, N, K, reinterpret_cast<const float*>(ah), reinterpret_cast<const float*>(al),
+                     lda, reinterpret_cast<const float*>(bh), reinterpret_cast<const float*>(bl),
+                     ldb, static_cast<float*>(ch), static_cast<float*>(cl), ldc, epi, alpha);
+  P.f16 = 1;
+  P.c0 = c0;
+  P.row_inv = row_inv;
+  P.in_r = in_r;
+  P.out_r = out_r;
+  return P;
+}
+
+// fp16 copies (scaled by 2^14) of U, U^T, V, V^T for the 3xF16 products.
+void push_f16_bases(std::vector<ToF16Seg>& segs, void* state, const ItemLayout& L) {
+  segs.push_back({F(state, L.u_hi), F(state, L.u_lo), L.ldm, H(state, L.u16_hi),
+                  H(state, L.u16_lo), L.ldm, L.m, L.m});
+  segs.push_back({F(state, L.ut_hi), F(state, L.ut_lo), L.ldm, H(state, L.ut16_hi),
+                  H(state, L.ut16_lo), L.ldm, L.m, L.m});
+  segs.push_back({F(state, L.vb_hi), F(state, L.vb_lo), L.ldn, H(state, L.vb16_hi),
+                  H(state, L.vb16_lo), L.ldn, L.n, L.n});
+  segs.push_back({F(state, L.vt_hi), F(state, L.vt_lo), L.ldn, H(state, L.vt16_hi),
+                  H(state, L.vt16_lo), L.ldn, L.n, L.n});
+}
+
 int check_device() {
   static int cached = 0;  // 1 ok, -1 not supported
   if (cached == 0) {
@@ -83,8 +117,22 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   int* status = static_cast<int*>(state);
   const size_t n_items = items.size();
 
-  // (1) momentum, and the TF32 split of G
-  {
+  const bool f16 = precision == ROT_PREC_3XF16;
+
+  // (1) momentum, and the TF32 split of G (3xF16: its scaled fp16 split)
+  if (f16) {
+    if (cudaMemsetAsync(F(work, WL[0].g_rmax), 0, 8 * n_items, s) != cudaSuccess) return ROT_ECUDA;
+    std::vector<Momentum16Seg> segs(n_items);
+    for (size_t k = 0; k < n_items; ++k) {
+      const int i = items[k];
+      const ItemLayout& L = p->items[i];
+      const WorkLayout& x = WL[k];
+      if (!W[i] || !G[i]) return ROT_EINVAL;
+      segs[k] = {G[i], F(state, L.m_hi), F(state, L.m_lo), H(work, x.g_hi), H(work, x.g_lo),
+                 F(work, x.g_rinv), F(work, x.g_rmax), L.m, L.n, L.ldn};
+    }
+    ROT_TRY(launch_momentum16(segs, beta1, s));
+  } else {
     std::vector<MomentumSeg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
@@ -179,37 +227,66 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       }
     }
     ROT_TRY(qr_batched(qp, rank_rtol, status, s));
+    std::vector<ToF16Seg> conv;
+    for (size_t k = 0; k < n_items; ++k) push_f16_bases(conv, state, p->items[items[k]]);
+    ROT_TRY(launch_to_f16(conv, s));
   }
 
   // (3) rotation: S_G^T = (G V)^T ; G~ = U^T S_G.  M~ = U^T M V is recomputed
   // from M only when the bases change (refresh steps); otherwise it follows
   // M~ <- beta1 M~ + (1 - beta1) G~ inside the Adam kernel, which is the same
-  // quantity since U and V are unchanged.
+  // quantity since U and V are unchanged.  In 3xF16 mode the G side runs on
+  // the fp16 splits (G's rows scaled by s_r, U and V by 2^14, S_G by a power
+  // of two below its bound, the largest row norm of G); the refresh-only M
+  // side stays 3xTF32.
   {
-    std::vector<GemmProblem> a, b;
+    std::vector<GemmProblem> a, b, am, bm;
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       const int m = L.m, n = L.n;
       const float *Vth = F(state, L.vt_hi), *Vtl = F(state, L.vt_lo);
-      a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, Vth, Vtl, L.ldn,
-                     F(work, x.sg_hi), F(work, x.sg_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
-      if (refresh)
-        a.push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
-                       F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
       const float *Uth = F(state, L.ut_hi), *Utl = F(state, L.ut_lo);
-      b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
-                     F(work, x.gt), nullptr, L.ldn, kEpiStoreF32));
-      if (refresh)
-        b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
-                       F(state, L.mt), nullptr, L.ldn, kEpiStoreF32));
+      if (f16) {
+        a.push_back(gp16(m, n, n, H(work, x.g_hi), H(work, x.g_lo), L.ldn, H(state, L.vt16_hi),
+                         H(state, L.vt16_lo), L.ldn, H(work, x.sg_hi), H(work, x.sg_lo), L.ldm,
+                         kEpiStoreF16SplitT, kF16Inv, F(work, x.g_rinv), nullptr,
+                         F(work, x.g_rmax)));
+        b.push_back(gp16(m, n, m, H(state, L.ut16_hi), H(state, L.ut16_lo), L.ldm,
+                         H(work, x.sg_hi), H(work, x.sg_lo), L.ldm, F(work, x.gt), nullptr, L.ldn,
+                         kEpiStoreF32, kF16Inv, nullptr, F(work, x.g_rmax), nullptr));
+      } else {
+        a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, Vth, Vtl, L.ldn,
+                       F(work, x.sg_hi), F(work, x.sg_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
+        b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
+                       F(work, x.gt), nullptr, L.ldn, kEpiStoreF32));
+      }
+      if (refresh) {
+        (f16 ? am : a)
+            .push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
+                          F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
+        (f16 ? bm : b)
+            .push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
+                          F(state, L.mt), nullptr, L.ldn, kEpiStoreF32));
+      }
     }
     ROT_TRY(gemm_grouped(a, precision, status, s));
+    if (!am.empty()) ROT_TRY(gemm_grouped(am, ROT_PREC_3XTF32, status, s));
     ROT_TRY(gemm_grouped(b, precision, status, s));
+    if (!bm.empty()) ROT_TRY(gemm_grouped(bm, ROT_PREC_3XTF32, status, s));
   }
 
   // (3') Adam in rotated coordinates; D's split overwrites G's split
-  {
+  if (f16) {
+    std::vector<Adam16Seg> segs(n_items);
+    for (size_t k = 0; k < n_items; ++k) {
+      const ItemLayout& L = p->items[items[k]];
+      const WorkLayout& x = WL[k];
+      segs[k] = {F(work, x.gt), F(state, L.mt), F(state, L.v), H(work, x.g_hi), H(work, x.g_lo),
+                 F(work, x.d_rinv), F(work, x.d_rmax), L.m, L.n, L.ldn};
+    }
+    ROT_TRY(launch_adam16(segs, beta1, beta2, eps, refresh ? 0 : 1, s));
+  } else {
     std::vector<AdamSeg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
@@ -220,7 +297,9 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     ROT_TRY(launch_adam(segs, beta1, beta2, eps, refresh ? 0 : 1, s));
   }
 
-  // (4) back-rotation: (D V^T)^T into S_G's buffer; W -= lr U (D V^T)
+  // (4) back-rotation: (D V^T)^T into S_G's buffer; W -= lr U (D V^T).  In
+  // 3xF16 mode D's rows carry their own scales and (D V^T)^T one below the
+  // largest row norm of D.
   {
     std::vector<GemmProblem> a, b;
     for (size_t k = 0; k < n_items; ++k) {
@@ -228,11 +307,21 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const ItemLayout& L = p->items[i];
       const WorkLayout& x = WL[k];
       const int m = L.m, n = L.n;
-      a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, F(state, L.vb_hi),
-                     F(state, L.vb_lo), L.ldn, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
-                     kEpiStoreSplitT, 0.f, 1));
-      b.push_back(gp(m, n, m, F(state, L.u_hi), F(state, L.u_lo), L.ldm, F(work, x.sg_hi),
-                     F(work, x.sg_lo), L.ldm, W[i], nullptr, n, kEpiApply, lr));
+      if (f16) {
+        a.push_back(gp16(m, n, n, H(work, x.g_hi), H(work, x.g_lo), L.ldn, H(state, L.vb16_hi),
+                         H(state, L.vb16_lo), L.ldn, H(work, x.sg_hi), H(work, x.sg_lo), L.ldm,
+                         kEpiStoreF16SplitT, kF16Inv, F(work, x.d_rinv), nullptr,
+                         F(work, x.d_rmax)));
+        b.push_back(gp16(m, n, m, H(state, L.u16_hi), H(state, L.u16_lo), L.ldm,
+                         H(work, x.sg_hi), H(work, x.sg_lo), L.ldm, W[i], nullptr, n, kEpiApply,
+                         kF16Inv, nullptr, F(work, x.d_rmax), nullptr, lr));
+      } else {
+        a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, F(state, L.vb_hi),
+                       F(state, L.vb_lo), L.ldn, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
+                       kEpiStoreSplitT, 0.f, 1));
+        b.push_back(gp(m, n, m, F(state, L.u_hi), F(state, L.u_lo), L.ldm, F(work, x.sg_hi),
+                       F(work, x.sg_lo), L.ldm, W[i], nullptr, n, kEpiApply, lr));
+      }
     }
     ROT_TRY(gemm_grouped(a, precision, status, s));
     ROT_TRY(gemm_grouped(b, precision, status, s));
@@ -266,7 +355,10 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream) {
     segs.push_back({F(state, L.vb_hi), F(state, L.vb_lo), L.n, L.n, L.ldn, 1});
     segs.push_back({F(state, L.vt_hi), F(state, L.vt_lo), L.n, L.n, L.ldn, 1});
   }
-  return launch_fill(segs, s);
+  ROT_TRY(launch_fill(segs, s));
+  std::vector<ToF16Seg> conv;
+  for (int32_t i = 0; i < plan->count; ++i) push_f16_bases(conv, state, plan->items[i]);
+  return launch_to_f16(conv, s);
 }
 
 int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void* state,
@@ -278,7 +370,7 @@ int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void*
   if ((reinterpret_cast<uintptr_t>(state) & 255) || (reinterpret_cast<uintptr_t>(work) & 255))
     return ROT_EINVAL;
   if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
-      precision != ROT_PREC_3XTF32_PRECISE)
+      precision != ROT_PREC_3XTF32_PRECISE && precision != ROT_PREC_3XF16)
     return ROT_EINVAL;
   if (!(rank_rtol >= 1e-6f && rank_rtol < 1.f)) return ROT_EINVAL;
   for (int32_t i = 0; i < plan->count; ++i) {

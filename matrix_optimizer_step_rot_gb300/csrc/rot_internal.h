@@ -41,6 +41,7 @@ enum GemmEpi : int {
   kEpiStoreF32T = 3,    // C^T <- acc, float32 into c.hi
   kEpiApply = 4,        // C (row-major, float32 in c.hi) -= alpha * acc
   kEpiApplySplit = 5,   // C (row-major split) <- split(hi + lo - alpha * acc)
+  kEpiStoreF16SplitT = 6,  // C^T (row-major N x M fp16 arrays) <- scaled fp16 split (3xF16)
 };
 
 struct GemmProblem {
@@ -57,6 +58,15 @@ struct GemmProblem {
   int epi;
   float alpha;
   int mma_only = 0;  // split outputs feed only tensor cores: round lo to TF32
+  // ROT_PREC_3XF16 problems: a_* and b_* (and c_* for kEpiStoreF16SplitT) are
+  // fp16 arrays (cast), lda/ldb/ldc in elements.  The accumulator is scaled
+  // by c0 * row_inv[row] / pow2_below(*in_r); a fp16 split output is scaled by
+  // pow2_below(*out_r) (see split.cuh).  Null pointers mean 1.
+  int f16 = 0;
+  const float* row_inv = nullptr;
+  const float* in_r = nullptr;
+  const float* out_r = nullptr;
+  float c0 = 1.f;
 };
 
 // 3xTF32 with each K block accumulated afresh and summed in float32
@@ -99,6 +109,66 @@ struct AdamSeg {
 // since the last step); else M~ was just recomputed as U^T M V.
 int launch_adam(const std::vector<AdamSeg>& segs, float beta1, float beta2, float eps,
                 int incremental, cudaStream_t stream);
+
+// 3xF16 variants, one block per row.  Momentum as above, and G's scaled fp16
+// split: row r gets the power-of-two scale s_r with max|G_r| s_r < 2^14,
+// g_rinv[r] = 1 / s_r, and *g_rmax grows to the largest row 2-norm (it must
+// be 0 or smaller beforehand).  g_hi / g_lo are fp16 arrays (ld = ldm).
+struct Momentum16Seg {
+  const float* g;
+  float* m_hi;
+  float* m_lo;
+  unsigned short* g_hi;
+  unsigned short* g_lo;
+  float* g_rinv;
+  float* g_rmax;
+  int rows, cols, ldm;
+};
+int launch_momentum16(const std::vector<Momentum16Seg>& segs, float beta1, cudaStream_t stream);
+
+// Adam as above with D written as a scaled fp16 split (per-row scales into
+// d_rinv, largest row 2-norm into *d_rmax).
+struct Adam16Seg {
+  const float* gt;
+  float* mt;
+  float* v;
+  unsigned short* d_hi;
+  unsigned short* d_lo;
+  float* d_rinv;
+  float* d_rmax;
+  int rows, cols, ld;
+};
+int launch_adam16(const std::vector<Adam16Seg>& segs, float beta1, float beta2, float eps,
+                  int incremental, cudaStream_t stream);
+
+// hi/lo (fp16, rows x cols, ld_dst) = fp16 split of 2^14 (s_hi + s_lo), for
+// the bases (|entries| <= 1).
+struct ToF16Seg {
+  const float* s_hi;
+  const float* s_lo;
+  int ld_src;
+  unsigned short* hi;
+  unsigned short* lo;
+  int ld_dst;
+  int rows, cols;
+};
+int launch_to_f16(const std::vector<ToF16Seg>& segs, cudaStream_t stream);
+
+// Scaled fp16 split of a float32 matrix (test entry point): per-row scales
+// (rinv != nullptr) or one scale from *bound; rmax (if set) grows to the
+// largest row 2-norm; hi == nullptr computes the norms only.
+struct Split16Seg {
+  const float* src;
+  int ld_src;
+  unsigned short* hi;
+  unsigned short* lo;
+  int ld_dst;
+  int rows, cols;
+  float* rinv;
+  float* rmax;
+  const float* bound;
+};
+int launch_split16(const std::vector<Split16Seg>& segs, cudaStream_t stream);
 
 // dst (cols x rows, ld_dst) = src^T, where src (rows x cols, ld_src) is a split;
 // dst is written as a split.  src_is_split = 0 reads float32 from src.hi.

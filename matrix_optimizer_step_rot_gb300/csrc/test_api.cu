@@ -17,7 +17,9 @@ extern "C" {
 uint64_t rot_test_gemm_work_bytes(int32_t M, int32_t N, int32_t K) {
   if (M < 1 || N < 1 || K < 1) return 0;
   const int64_t ldk = pad_ld(K);
-  return 2 * split_bytes(M, ldk) + 2 * split_bytes(N, ldk);
+  // TF32 splits of A and B; the 3xF16 path's fp16 splits, row scales and
+  // norm slot take less than that plus 1 KB
+  return 2 * split_bytes(M, ldk) + 2 * split_bytes(N, ldk) + 1024;
 }
 
 int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
@@ -27,8 +29,9 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
   if (M < 1 || N < 1 || K < 1 || !A || !B || !C || !work) return ROT_EINVAL;
   if (lda < K || ldb < K || epi < kEpiStoreSplit || epi > kEpiApplySplit) return ROT_EINVAL;
   if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
-      precision != ROT_PREC_3XTF32_PRECISE)
+      precision != ROT_PREC_3XTF32_PRECISE && precision != ROT_PREC_3XF16)
     return ROT_EINVAL;
+  if (precision == ROT_PREC_3XF16 && epi == kEpiApplySplit) return ROT_EINVAL;
   const bool transposed = epi == kEpiStoreSplitT || epi == kEpiStoreF32T;
   if (ldc < (transposed ? M : N)) return ROT_EINVAL;
   if (work_bytes < rot_test_gemm_work_bytes(M, N, K)) return ROT_EINVAL;
@@ -36,6 +39,51 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int ldk = (int)pad_ld(K);
   char* w = static_cast<char*>(work);
+  if (precision == ROT_PREC_3XF16) {
+    // A: per-row scales; B: one scale below its largest row norm (the
+    // epilogue undoes both).  Scaled fp16 splits, then the row scales of A and
+    // B's norm bound in a small tail.
+    const uint64_t ha = align256(2ull * M * ldk), hb = align256(2ull * N * ldk);
+    unsigned short* a16h = reinterpret_cast<unsigned short*>(w);
+    unsigned short* a16l = reinterpret_cast<unsigned short*>(w + ha);
+    unsigned short* b16h = reinterpret_cast<unsigned short*>(w + 2 * ha);
+    unsigned short* b16l = reinterpret_cast<unsigned short*>(w + 2 * ha + hb);
+    float* rinv = reinterpret_cast<float*>(w + 2 * ha + 2 * hb);
+    float* bnorm = reinterpret_cast<float*>(w + 2 * ha + 2 * hb + align256(4ull * M));
+    if (cudaMemsetAsync(bnorm, 0, 4, s) != cudaSuccess) return ROT_ECUDA;
+    std::vector<Split16Seg> pass1 = {{A, lda, a16h, a16l, ldk, M, K, rinv, nullptr, nullptr},
+                                     {B, ldb, nullptr, nullptr, ldk, N, K, nullptr, bnorm, nullptr}};
+    int e = launch_split16(pass1, s);
+    if (e != ROT_OK) return e;
+    std::vector<Split16Seg> pass2 = {{B, ldb, b16h, b16l, ldk, N, K, nullptr, nullptr, bnorm}};
+    e = launch_split16(pass2, s);
+    if (e != ROT_OK) return e;
+    GemmProblem P;
+    P.M = M;
+    P.N = N;
+    P.K = K;
+    P.a_hi = reinterpret_cast<const float*>(a16h);
+    P.a_lo = reinterpret_cast<const float*>(a16l);
+    P.lda = ldk;
+    P.b_hi = reinterpret_cast<const float*>(b16h);
+    P.b_lo = reinterpret_cast<const float*>(b16l);
+    P.ldb = ldk;
+    P.c_hi = C;
+    // kEpiStoreSplitT in this mode writes C^T as a fp16 split, unscaled: hi
+    // in the first N x ldc halves of C, lo right after
+    P.epi = epi == kEpiStoreSplitT ? (int)kEpiStoreF16SplitT : epi;
+    P.c_lo = epi == kEpiStoreSplitT
+                 ? reinterpret_cast<float*>(reinterpret_cast<unsigned short*>(C) + (int64_t)N * ldc)
+             : epi == kEpiStoreSplit ? C + (int64_t)M * ldc
+                                     : nullptr;
+    if (epi == kEpiStoreSplit) return ROT_EINVAL;  // no untransposed fp16 store
+    P.ldc = ldc;
+    P.alpha = alpha;
+    P.f16 = 1;
+    P.row_inv = rinv;
+    P.in_r = bnorm;
+    return gemm_grouped({P}, precision, reinterpret_cast<int*>(status), s);
+  }
   float* a_hi = reinterpret_cast<float*>(w);
   float* a_lo = reinterpret_cast<float*>(w + split_bytes(M, ldk));
   float* b_hi = reinterpret_cast<float*>(w + 2 * split_bytes(M, ldk));

@@ -1,6 +1,6 @@
 """Parity on the five workloads at their full sizes, in the launch
 configuration the benchmark uses (the real plan: same micro-groups, same
-grouped launches).
+grouped launches), in both float32-accuracy modes (3xTF32 and 3xF16).
 
 Matrices are independent, so the oracle runs on a sample of each workload's
 matrices (their inputs come from the shared seeded generator); the other
@@ -31,6 +31,26 @@ pytestmark = pytest.mark.gpu
 BAR_W = 1e-4
 BAR_ORTH = 1e-4
 FLOOR_FACTOR = 3.0
+FULL = [B.ROT_PREC_3XTF32, B.ROT_PREC_3XF16]  # float32-accuracy modes, 1e-4 bar
+
+# the oracle's results and floors do not depend on the GPU's precision mode:
+# computed once per workload and shared by the modes' tests
+_ORACLE = {}
+_FLOOR = {}
+
+
+def oracle_run(wl, sampled, steps):
+    key = (wl.name, tuple(sampled), steps)
+    if key not in _ORACLE:
+        _ORACLE[key] = orc.run(wl, sampled, steps=steps)
+    return _ORACLE[key]
+
+
+def oracle_floor(wl, i, Wo, steps):
+    key = (wl.name, i, steps)
+    if key not in _FLOOR:
+        _FLOOR[key] = orc.floor(wl, i, Wo, seeds=(1, 2, 3, 4, 5), steps=steps)
+    return _FLOOR[key]
 
 
 def orth_bound(p):
@@ -102,7 +122,7 @@ def check(wl, sampled, precision=B.ROT_PREC_3XTF32, bar=BAR_W, steps=None):
         log(f"{wl.name}: max ||Q^T Q - I||_F over {wl.count} matrices = {worst:.2e} "
             f"(largest ratio to its bound {excess:.2f})")
         assert excess <= 1.0
-    ref = orc.run(wl, sampled, steps=steps)
+    ref = oracle_run(wl, sampled, steps)
     for i in sampled:
         Wo, st = ref[i]
         e = float(np.linalg.norm(W[i].cpu().numpy().astype(np.float64) - Wo) / np.linalg.norm(Wo))
@@ -111,15 +131,16 @@ def check(wl, sampled, precision=B.ROT_PREC_3XTF32, bar=BAR_W, steps=None):
         if e <= bar:
             log(f"{wl.name}[{i}] {wl.shapes[i]} prec {precision}: W rel err {e:.2e} <= {bar:.0e}")
             continue
-        fl = orc.floor(wl, i, Wo, seeds=(1, 2, 3, 4, 5), steps=steps)
+        fl = oracle_floor(wl, i, Wo, steps)
         log(f"{wl.name}[{i}] {wl.shapes[i]} prec {precision}: W rel err {e:.2e} > {bar:.0e}; "
             f"method floor (oracle, float32-level QR-input perturbation) {fl:.2e}")
         assert e <= bar + FLOOR_FACTOR * fl, (i, e, fl)
 
 
-def test_block_parity():
+@pytest.mark.parametrize("precision", FULL)
+def test_block_parity(precision):
     wl = inputs.workload("block")
-    check(wl, [0, 1, 4])  # q_proj, k_proj, gate
+    check(wl, [0, 1, 4], precision)  # q_proj, k_proj, gate
 
 
 def test_block_parity_tf32():
@@ -127,16 +148,19 @@ def test_block_parity_tf32():
     check(wl, [1], precision=B.ROT_PREC_TF32, bar=2e-3)
 
 
-def test_full_stack_sampled():
+@pytest.mark.parametrize("precision", FULL)
+def test_full_stack_sampled(precision):
     wl = inputs.workload("full")
-    check(wl, [1, 7 * 13 + 2, 7 * 27])  # L0.k_proj, L13.v_proj, L27.q_proj
+    check(wl, [1, 7 * 13 + 2, 7 * 27], precision)  # L0.k_proj, L13.v_proj, L27.q_proj
 
 
-def test_slice8b_sampled():
+@pytest.mark.parametrize("precision", FULL)
+def test_slice8b_sampled(precision):
     wl = inputs.workload("slice8b")
-    check(wl, [1])  # L0.k_proj 1024 x 4096, refresh on every step
+    check(wl, [1], precision)  # L0.k_proj 1024 x 4096, refresh on every step
 
 
-def test_ragged_sampled():
+@pytest.mark.parametrize("precision", FULL)
+def test_ragged_sampled(precision):
     wl = inputs.workload("ragged")
-    check(wl, list(range(0, 256, 11)))
+    check(wl, list(range(0, 256, 11)), precision)

@@ -12,7 +12,8 @@ pytestmark = pytest.mark.gpu
 SHAPES = [(128, 256, 32), (64, 64, 64), (300, 520, 100), (1, 40, 7), (33, 1, 65),
           (1000, 1000, 1000), (2048, 256, 4096), (130, 300, 2000)]
 PRECISE = B.ROT_PREC_3XTF32_PRECISE
-TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3, PRECISE: 1.5e-6}
+F16 = B.ROT_PREC_3XF16
+TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3, PRECISE: 1.5e-6, F16: 3e-6}
 
 
 def tol(precision, K):
@@ -20,7 +21,7 @@ def tol(precision, K):
     truncate each partial sum, an error that grows with the number of K steps
     (about 2^-24 per step relative to the running sum); 3xTF32 is therefore
     bounded by a K-proportional term on top of the split's own error."""
-    if precision == B.ROT_PREC_3XTF32:
+    if precision in (B.ROT_PREC_3XTF32, F16):
         return TOL[precision] + 2.5e-8 * K
     return TOL[precision]  # TF32: input rounding dominates; precise: K-independent
 
@@ -33,10 +34,13 @@ def built():
     B.lib()
 
 
-def run(M, N, K, epi, precision, alpha=0.5, seed=0):
+def run(M, N, K, epi, precision, alpha=0.5, seed=0, row_spread=False):
     g = torch.Generator(device="cuda").manual_seed(seed)
     A = torch.rand(M, K, device="cuda", generator=g) * 2 - 1
     Bm = torch.rand(N, K, device="cuda", generator=g) * 2 - 1
+    if row_spread:  # rows of very different magnitude (exercises the fp16 scales)
+        A = A * torch.logspace(-12, 6, M, device="cuda")[:, None]
+        Bm = Bm * torch.logspace(-3, 3, N, device="cuda")[:, None]
     ref = A.double() @ Bm.double().T
     transposed = epi in (1, 3)
     rows, ldc = (N, M) if transposed else (M, N)
@@ -56,7 +60,11 @@ def run(M, N, K, epi, precision, alpha=0.5, seed=0):
                     torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    if epi in (0, 1):
+    if epi == 1 and precision == F16:
+        halves = C.view(torch.float16)
+        out = (halves[:rows * ldc].double() + halves[rows * ldc:2 * rows * ldc].double())
+        out = out.view(rows, ldc)
+    elif epi in (0, 1):
         out = (C[:rows * ldc].double() + C[rows * ldc:].double()).view(rows, ldc)
         # the split is exact: hi has 10 explicit mantissa bits
         hi = C[:rows * ldc]
@@ -74,7 +82,7 @@ def run(M, N, K, epi, precision, alpha=0.5, seed=0):
     return out, ref
 
 
-@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32, PRECISE])
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32, PRECISE, F16])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_store_f32(M, N, K, precision):
     out, ref = run(M, N, K, 2, precision)
@@ -91,3 +99,37 @@ def test_gemm_output_modes(M, N, K, epi, precision):
     err = (out - ref).norm() / ref.norm()
     # the apply modes recover the product from a difference of float32 values
     assert err <= (1e-5 if epi in (4, 5) else tol(precision, K)), float(err)
+
+
+@pytest.mark.parametrize("epi", [1, 3, 4])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 100), (64, 64, 64), (1, 40, 7), (257, 129, 4100)])
+def test_gemm_f16_output_modes(M, N, K, epi):
+    """3xF16: the transposed fp16-split store (unscaled, values of order 1),
+    the transposed float32 store and the apply mode."""
+    out, ref = run(M, N, K, epi, F16)
+    err = float((out - ref).norm() / ref.norm())
+    bound = {1: 2e-6 + 2.5e-8 * K, 3: tol(F16, K), 4: 1e-5 + tol(F16, K)}[epi]
+    assert err <= bound, err
+
+
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, F16])
+def test_gemm_rows_of_very_different_magnitude(precision):
+    """Rows of A spanning 18 decades and of B 6: per-row scaling keeps every
+    row's product at float32-level relative accuracy in 3xF16, as 3xTF32
+    (checked row by row, so the small rows are not hidden by the large)."""
+    out, ref = run(384, 200, 1000, 2, precision, row_spread=True)
+    row_err = (out - ref).norm(dim=1) / ref.norm(dim=1)
+    print(f"prec {precision}: worst row rel err {float(row_err.max()):.3e}")
+    assert float(row_err.max()) <= 5e-5, float(row_err.max())
+
+
+def test_gemm_f16_rejects_untransposed_split_modes():
+    M = N = K = 32
+    A = torch.zeros(M, K, device="cuda")
+    C = torch.zeros(2 * M * N, device="cuda")
+    wb = B.rot_test_gemm_work_bytes(M, N, K)
+    work = torch.empty(wb, dtype=torch.uint8, device="cuda")
+    for epi in (0, 5):
+        with pytest.raises(B.RotError):
+            B.rot_test_gemm(M, N, K, A.data_ptr(), K, A.data_ptr(), K, C.data_ptr(), N, epi, 1.0,
+                            F16, work.data_ptr(), wb, 0, torch.cuda.current_stream().cuda_stream)

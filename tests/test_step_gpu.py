@@ -12,7 +12,9 @@ from oracle import rot_oracle as orc
 
 pytestmark = pytest.mark.gpu
 
-TOL_W = {B.ROT_PREC_3XTF32: 1e-4, B.ROT_PREC_TF32: 2e-3}
+F16 = B.ROT_PREC_3XF16
+TOL_W = {B.ROT_PREC_3XTF32: 1e-4, B.ROT_PREC_TF32: 2e-3, F16: 1e-4}
+FULL = [B.ROT_PREC_3XTF32, F16]  # the float32-accuracy modes
 TOL_ORTH = 1e-4
 
 
@@ -46,7 +48,7 @@ def orth(Q):
     return float(np.linalg.norm(Q.T @ Q - np.eye(Q.shape[1])))
 
 
-@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32])
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32, F16])
 def test_tiny_parity(precision):
     wl = inputs.workload("tiny")
     W, opt = run_gpu(wl, precision)
@@ -59,17 +61,18 @@ def test_tiny_parity(precision):
         V = opt.export(i, B.ROT_WHICH_V).cpu().numpy()
         assert orth(U) <= TOL_ORTH and orth(V) <= TOL_ORTH
         assert opt.ranks(i) == (st.rank_u, st.rank_v)
-        if precision == B.ROT_PREC_3XTF32:
+        if precision in FULL:
             M = opt.export(i, B.ROT_WHICH_M).cpu().numpy()
             assert rel(M, st.M) <= 1e-6
             np.testing.assert_allclose(U, st.U, atol=1e-4)
             np.testing.assert_allclose(V, st.V, atol=1e-4)
 
 
-def test_plain_adam_steps_match_closed_form():
+@pytest.mark.parametrize("precision", FULL)
+def test_plain_adam_steps_match_closed_form(precision):
     """Before the first refresh (U = V = I) the GPU step is plain Adam."""
     wl = inputs.workload("tiny")
-    W, opt = run_gpu(wl, B.ROT_PREC_3XTF32, steps=3)
+    W, opt = run_gpu(wl, precision, steps=3)
     h = wl.hyper
     for i in range(wl.count):
         w = wl.w0(i).astype(np.float64)
@@ -83,33 +86,60 @@ def test_plain_adam_steps_match_closed_form():
         assert rel(W[i].cpu().numpy().astype(np.float64), w) <= 1e-6
 
 
-def test_ragged_small_parity():
+@pytest.mark.parametrize("precision", FULL)
+def test_ragged_small_parity(precision):
     """Shapes that are not multiples of the tile sizes, several groups."""
     shapes = ((100, 36), (36, 100), (97, 97), (1, 40), (40, 1), (130, 70), (33, 65))
     wl = inputs.Workload("ragged_small", shapes, tuple(map(str, range(len(shapes)))), 0.02,
                          1e-3, "t3", 6, 3, 40000, 11)
-    W, opt = run_gpu(wl, B.ROT_PREC_3XTF32)
+    W, opt = run_gpu(wl, precision)
     ref = orc.run(wl)
     for i in range(wl.count):
         Wo, st = ref[i]
         e = rel(W[i].cpu().numpy().astype(np.float64), Wo)
-        assert e <= TOL_W[B.ROT_PREC_3XTF32], (i, shapes[i], e)
+        assert e <= TOL_W[precision], (i, shapes[i], e)
         assert opt.ranks(i) == (st.rank_u, st.rank_v), (i, shapes[i])
 
 
-def test_medium_multi_block_parity():
-    """QR inputs wider than one 128-column block (several block reflectors,
+@pytest.mark.parametrize("precision", FULL)
+def test_medium_multi_block_parity(precision):
+    """QR inputs wider than one 256-column block (several block reflectors,
     multi-CTA panel clusters), rectangular both ways and square."""
     shapes = ((520, 300), (300, 520), (384, 384), (1030, 260))
     wl = inputs.Workload("medium", shapes, tuple(map(str, range(len(shapes)))), 0.02, 1e-3,
                          "normal", 4, 2, 1 << 30, 21)
-    W, opt = run_gpu(wl, B.ROT_PREC_3XTF32)
+    W, opt = run_gpu(wl, precision)
     ref = orc.run(wl)
     for i in range(wl.count):
         Wo, st = ref[i]
         e = rel(W[i].cpu().numpy().astype(np.float64), Wo)
-        assert e <= TOL_W[B.ROT_PREC_3XTF32], (i, shapes[i], e)
+        assert e <= TOL_W[precision], (i, shapes[i], e)
         assert opt.ranks(i) == (st.rank_u, st.rank_v), (i, shapes[i])
         U = opt.export(i, B.ROT_WHICH_U).cpu().numpy()
         V = opt.export(i, B.ROT_WHICH_V).cpu().numpy()
         assert orth(U) <= TOL_ORTH and orth(V) <= TOL_ORTH, (i, orth(U), orth(V))
+
+
+def test_f16_mode_handles_gradients_of_any_scale():
+    """3xF16 scales every operand by a power of two.  Gradients of order 1e-9
+    and 1e5 (outside fp16's range: its smallest subnormal is 6e-8, its largest
+    value 65504), with eps scaled alike so that Adam's step is the same, match
+    the oracle as at the usual scale; a zero gradient leaves W unchanged.
+    (The float32 refresh squares magnitudes -- M M^T U, then column norms --
+    so gradients far below 1e-9 or above 1e5 reach float32's own range limits
+    there, in every mode.)"""
+    shapes = ((96, 64), (64, 160))
+    for scale in (1e-6, 1e8):
+        hyper = inputs.Hyper(eps=float(np.float32(1e-8 * scale)))
+        wl = inputs.Workload("scaled", shapes, ("a", "b"), 0.02, 1e-3 * scale, "normal", 4, 2,
+                             1 << 30, 31, hyper)
+        W16, _ = run_gpu(wl, F16)
+        ref = orc.run(wl)
+        for i in range(wl.count):
+            w0 = wl.w0(i).astype(np.float64)
+            e = rel(W16[i].cpu().numpy().astype(np.float64) - w0, ref[i][0] - w0)
+            assert e <= TOL_W[F16], (scale, i, e)
+    wl = inputs.Workload("zero", shapes, ("a", "b"), 0.02, 0.0, "normal", 3, 2, 1 << 30, 32)
+    W16, opt = run_gpu(wl, F16)
+    for i in range(wl.count):
+        np.testing.assert_array_equal(W16[i].cpu().numpy(), wl.w0(i))
