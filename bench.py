@@ -32,6 +32,11 @@ from matrix_optimizer_step_rot_gb300 import inputs  # noqa: E402
 METRIC = "rotated-Adam matrix-steps/s and TFLOP/s (% TF32 TC peak), Qwen3-1.7B shapes"
 UNIT = "matrix-steps/s"
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 : BF16 tensor rates
+# DRAM bytes (read + write) per algorithmic flop of the rotation GEMM, from one
+# ncu capture of the same kernel on one Qwen3-1.7B-shaped block (the stack's
+# micro-groups hold the same shapes, so traffic scales with the flops);
+# commands and figures in profiles/gemm_f16_block.md, gemm_tc_kernel_block.md
+TRAFFIC_PER_FLOP = {"3xf16": 3.2e-3, "3xtf32": 6.85e-3}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -258,6 +263,14 @@ def run_ours(args):
     d2h = sum(w.numel() * 4 for w in w_host)
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
+    if e_steps:
+        # untimed: one round trip through every pinned buffer, so that the
+        # timed copies do not pay for the first device access to fresh pages
+        for buf in g_dev:
+            for gd, gh in zip(buf, g_host):
+                gd.copy_(gh, non_blocking=True)
+        for wh, wd in zip(w_host, W):
+            wh.copy_(wd, non_blocking=True)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -302,6 +315,11 @@ def run_ours(args):
     # device time of the steps themselves inside the end-to-end run; the rest
     # is copies on the critical path (the first H2D and each step's D2H)
     e2e_compute_ms = sum(ev_start[i].elapsed_time(ev_end[i]) for i in range(e_steps))
+    # what lies between: before the first step (its gradients' H2D), between
+    # steps (the previous W's D2H), after the last (its D2H)
+    e2e_gaps_ms = ([x0.elapsed_time(ev_start[0])]
+                   + [ev_end[i].elapsed_time(ev_start[i + 1]) for i in range(e_steps - 1)]
+                   + [ev_end[e_steps - 1].elapsed_time(x1)]) if e_steps else []
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -354,7 +372,9 @@ def run_ours(args):
                 "peak": mma_sust,
                 "unit": "TFLOP/s",
                 "frac": gemm_tflops / mma_sust if gemm_tflops else None,
-                "traffic": None,
+                "traffic": (TRAFFIC_PER_FLOP[args.precision] * g["work"] / g["launches"]
+                            if args.precision in TRAFFIC_PER_FLOP and g["launches"] else None),
+                "traffic_unit": "bytes per launch (ncu, scaled from one block by flops)",
                 "peak_source": (f"{peak_kind} bf16 sustained (fp16 and bf16 share the rate)" if f16
                                 else f"{peak_kind} bf16 sustained x {TF32_OVER_BF16:.4f} "
                                      "(nominal TF32:BF16 dense ratio)"),
@@ -371,7 +391,8 @@ def run_ours(args):
             "e2e": None if not e_steps else {"value": world * wl.count * e_steps / (e2e_ms / 1000.0), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e_steps, "refresh_steps": sum(e2e_sched),
-                    "ms": e2e_ms, "compute_ms": e2e_compute_ms},
+                    "ms": e2e_ms, "compute_ms": e2e_compute_ms,
+                    "gaps_ms": [round(x, 2) for x in e2e_gaps_ms]},
             "gpu_launches": launches,
             "clocks": clocks,
         }
@@ -439,7 +460,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="full", choices=list(inputs.WORKLOADS))
-    ap.add_argument("--precision", default="3xtf32",
+    ap.add_argument("--precision", default="3xf16",
                     choices=["3xtf32", "tf32", "3xtf32-precise", "3xf16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run (profiling)")

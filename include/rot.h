@@ -62,8 +62,8 @@ extern "C" {
                                      registers: float32-level accuracy at any K */
 #define ROT_PREC_3XF16 5     /* the three split products on power-of-two-scaled fp16
                                 splits (11 + 11 significant bits, as 3XTF32) at twice
-                                the TF32 tensor-core rate; basis refresh products
-                                stay 3XTF32_PRECISE */
+                                the TF32 tensor-core rate; the basis refresh's long
+                                products stay 3XTF32_PRECISE */
 
 #define ROT_MAX_DIM 65536
 
@@ -175,9 +175,8 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream);
  * initialised state blob; work: the workspace blob.  refresh != 0 runs the
  * basis refresh (2) before the rotated update.  precision of the rotation
  * products: ROT_PREC_TF32, ROT_PREC_3XTF32, ROT_PREC_3XTF32_PRECISE or
- * ROT_PREC_3XF16 (the basis refresh always uses ROT_PREC_3XTF32_PRECISE, and
- * in 3XF16 mode the refresh-step product U^T M V uses 3XTF32).  The mode may
- * change from step to step.  rank_rtol in
+ * ROT_PREC_3XF16 (the basis refresh always uses ROT_PREC_3XTF32_PRECISE).
+ * The mode may change from step to step.  rank_rtol in
  * [1e-6, 1): the QR's numerical-rank threshold relative to the largest
  * column norm.  Non-finite inputs propagate (IEEE).
  * Errors: ROT_EINVAL (null pointers, unknown precision, rank_rtol out of

@@ -140,61 +140,126 @@ __device__ __forceinline__ void atomic_max_nonneg(float* slot, float x) {
 
 // 3xF16 momentum: one block per row (blockIdx.x strides over rows).  First
 // pass: M's update and the row's max |g| and sum g^2; second pass (G re-read,
-// from L2): the scaled fp16 split of G.
+// from L2): the scaled fp16 split of G.  Four columns per thread and access
+// (16-byte loads) where the row allows, single columns for the rest.
+__device__ __forceinline__ void momentum_elem(float x, float& hi, float& lo, float beta1,
+                                              float one_minus, float& sum, float& mx) {
+  const float m = beta1 * (hi + lo) + one_minus * x;
+  split_tf32(m, hi, lo);
+  sum = fmaf(x, x, sum);
+  mx = fmaxf(mx, fabsf(x));
+}
+
 __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg> b,
                                   float beta1) {
   const Momentum16Seg& s = b.seg[blockIdx.y];
   const float one_minus = 1.0f - beta1;
+  const int nv = ((s.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(s.g) & 15) == 0)
+                     ? s.cols / 4 : 0;
   for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
     const float* g = s.g + (int64_t)r * s.cols;
+    float* mh = s.m_hi + (int64_t)r * s.ldm;
+    float* ml = s.m_lo + (int64_t)r * s.ldm;
+    unsigned short* gh = s.g_hi + (int64_t)r * s.ldm;
+    unsigned short* gl = s.g_lo + (int64_t)r * s.ldm;
     float sum = 0.f, mx = 0.f;
-    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-      const int64_t o = (int64_t)r * s.ldm + c;
-      const float x = g[c];
-      const float m = beta1 * (s.m_hi[o] + s.m_lo[o]) + one_minus * x;
-      float h, l;
-      split_tf32(m, h, l);
-      s.m_hi[o] = h;
-      s.m_lo[o] = l;
-      sum = fmaf(x, x, sum);
-      mx = fmaxf(mx, fabsf(x));
+    for (int q = threadIdx.x; q < nv; q += blockDim.x) {
+      const float4 x = reinterpret_cast<const float4*>(g)[q];
+      float4 h = reinterpret_cast<float4*>(mh)[q];
+      float4 l = reinterpret_cast<float4*>(ml)[q];
+      momentum_elem(x.x, h.x, l.x, beta1, one_minus, sum, mx);
+      momentum_elem(x.y, h.y, l.y, beta1, one_minus, sum, mx);
+      momentum_elem(x.z, h.z, l.z, beta1, one_minus, sum, mx);
+      momentum_elem(x.w, h.w, l.w, beta1, one_minus, sum, mx);
+      reinterpret_cast<float4*>(mh)[q] = h;
+      reinterpret_cast<float4*>(ml)[q] = l;
     }
+    for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x)
+      momentum_elem(g[c], mh[c], ml[c], beta1, one_minus, sum, mx);
     block_sum_max(sum, mx);
     const float scale = pow2_below(mx, kF16ScaleExp);
     if (threadIdx.x == 0) {
       s.g_rinv[r] = pow2_below_inv(mx, kF16ScaleExp);
       atomic_max_nonneg(s.g_rmax, row_norm_bound(sum, mx, s.cols));
     }
-    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-      const int64_t o = (int64_t)r * s.ldm + c;
-      split_f16(g[c] * scale, s.g_hi[o], s.g_lo[o]);
+    if (s.m16_hi) {
+      // M's new row (this thread's own writes above), its scale and split
+      float msum = 0.f, mmx = 0.f;
+      for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+        const float m = mh[c] + ml[c];
+        msum = fmaf(m, m, msum);
+        mmx = fmaxf(mmx, fabsf(m));
+      }
+      block_sum_max(msum, mmx);
+      const float mscale = pow2_below(mmx, kF16ScaleExp);
+      if (threadIdx.x == 0) {
+        s.m_rinv[r] = pow2_below_inv(mmx, kF16ScaleExp);
+        atomic_max_nonneg(s.m_rmax, row_norm_bound(msum, mmx, s.cols));
+      }
+      unsigned short* m16h = s.m16_hi + (int64_t)r * s.ldm;
+      unsigned short* m16l = s.m16_lo + (int64_t)r * s.ldm;
+      for (int c = threadIdx.x; c < s.cols; c += blockDim.x)
+        split_f16((mh[c] + ml[c]) * mscale, m16h[c], m16l[c]);
     }
+    for (int q = threadIdx.x; q < nv; q += blockDim.x) {
+      const float4 x = reinterpret_cast<const float4*>(g)[q];
+      ushort4 h, l;
+      split_f16(x.x * scale, h.x, l.x);
+      split_f16(x.y * scale, h.y, l.y);
+      split_f16(x.z * scale, h.z, l.z);
+      split_f16(x.w * scale, h.w, l.w);
+      reinterpret_cast<ushort4*>(gh)[q] = h;
+      reinterpret_cast<ushort4*>(gl)[q] = l;
+    }
+    for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x)
+      split_f16(g[c] * scale, gh[c], gl[c]);
   }
 }
 
 // 3xF16 Adam: one block per row.  First pass as adam_kernel (M~, v; D's row
 // max and sum of squares); second pass recomputes D from the M~ and v this
 // thread just wrote (bitwise the same values) and stores its scaled split.
+// The rows (library buffers, ld a multiple of 32) take 16-byte accesses.
+__device__ __forceinline__ float adam_elem(float g, float& m, float& v, float beta1,
+                                           float one_minus1, float beta2, float one_minus,
+                                           float eps, int incremental, float& sum, float& mx) {
+  if (incremental) m = beta1 * m + one_minus1 * g;
+  v = beta2 * v + one_minus * (g * g);
+  const float d = m / (sqrtf(v) + eps);
+  sum = fmaf(d, d, sum);
+  mx = fmaxf(mx, fabsf(d));
+  return d;
+}
+
 __global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, float beta1,
                               float beta2, float eps, int incremental) {
   const Adam16Seg& s = b.seg[blockIdx.y];
   const float one_minus1 = 1.0f - beta1;
   const float one_minus = 1.0f - beta2;
+  const int nv = s.cols / 4;
   for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
+    const float* gt = s.gt + (int64_t)r * s.ld;
+    float* mt = s.mt + (int64_t)r * s.ld;
+    float* v = s.v + (int64_t)r * s.ld;
+    unsigned short* dh = s.d_hi + (int64_t)r * s.ld;
+    unsigned short* dl = s.d_lo + (int64_t)r * s.ld;
     float sum = 0.f, mx = 0.f;
-    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-      const int64_t o = (int64_t)r * s.ld + c;
-      const float g = s.gt[o];
-      float m = s.mt[o];
-      if (incremental) {
-        m = beta1 * m + one_minus1 * g;
-        s.mt[o] = m;
-      }
-      const float v = beta2 * s.v[o] + one_minus * (g * g);
-      s.v[o] = v;
-      const float d = m / (sqrtf(v) + eps);
-      sum = fmaf(d, d, sum);
-      mx = fmaxf(mx, fabsf(d));
+    for (int q = threadIdx.x; q < nv; q += blockDim.x) {
+      const float4 g = reinterpret_cast<const float4*>(gt)[q];
+      float4 m = reinterpret_cast<float4*>(mt)[q];
+      float4 w = reinterpret_cast<float4*>(v)[q];
+      adam_elem(g.x, m.x, w.x, beta1, one_minus1, beta2, one_minus, eps, incremental, sum, mx);
+      adam_elem(g.y, m.y, w.y, beta1, one_minus1, beta2, one_minus, eps, incremental, sum, mx);
+      adam_elem(g.z, m.z, w.z, beta1, one_minus1, beta2, one_minus, eps, incremental, sum, mx);
+      adam_elem(g.w, m.w, w.w, beta1, one_minus1, beta2, one_minus, eps, incremental, sum, mx);
+      if (incremental) reinterpret_cast<float4*>(mt)[q] = m;
+      reinterpret_cast<float4*>(v)[q] = w;
+    }
+    for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x) {
+      float m = mt[c], w = v[c];
+      adam_elem(gt[c], m, w, beta1, one_minus1, beta2, one_minus, eps, incremental, sum, mx);
+      if (incremental) mt[c] = m;
+      v[c] = w;
     }
     block_sum_max(sum, mx);
     const float scale = pow2_below(mx, kF16ScaleExp);
@@ -202,11 +267,19 @@ __global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, flo
       s.d_rinv[r] = pow2_below_inv(mx, kF16ScaleExp);
       atomic_max_nonneg(s.d_rmax, row_norm_bound(sum, mx, s.cols));
     }
-    for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-      const int64_t o = (int64_t)r * s.ld + c;
-      const float d = s.mt[o] / (sqrtf(s.v[o]) + eps);
-      split_f16(d * scale, s.d_hi[o], s.d_lo[o]);
+    for (int q = threadIdx.x; q < nv; q += blockDim.x) {
+      const float4 m = reinterpret_cast<const float4*>(mt)[q];
+      const float4 w = reinterpret_cast<const float4*>(v)[q];
+      ushort4 h, l;
+      split_f16(m.x / (sqrtf(w.x) + eps) * scale, h.x, l.x);
+      split_f16(m.y / (sqrtf(w.y) + eps) * scale, h.y, l.y);
+      split_f16(m.z / (sqrtf(w.z) + eps) * scale, h.z, l.z);
+      split_f16(m.w / (sqrtf(w.w) + eps) * scale, h.w, l.w);
+      reinterpret_cast<ushort4*>(dh)[q] = h;
+      reinterpret_cast<ushort4*>(dl)[q] = l;
     }
+    for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x)
+      split_f16(mt[c] / (sqrtf(v[c]) + eps) * scale, dh[c], dl[c]);
   }
 }
 

@@ -170,12 +170,16 @@ void build_layout(rot_plan* p) {
       x.mt = w.floats(L.m, L.ldn);
       x.g_rinv = w.floats(1, L.m);
       x.d_rinv = w.floats(1, L.m);
+      x.m_rinv = w.floats(1, L.m);
+      x.m16_hi = w.halves(L.m, L.ldn);
+      x.m16_lo = w.halves(L.m, L.ldn);
     }
     {
-      const uint64_t norms = w.floats(1, 2 * (int64_t)WL.size());
+      const uint64_t norms = w.floats(1, 3 * (int64_t)WL.size());
       for (size_t k = 0; k < WL.size(); ++k) {
-        WL[k].g_rmax = norms + 8 * k;
-        WL[k].d_rmax = norms + 8 * k + 4;
+        WL[k].g_rmax = norms + 12 * k;
+        WL[k].d_rmax = norms + 12 * k + 4;
+        WL[k].m_rmax = norms + 12 * k + 8;
       }
     }
     for (size_t k = 0; k < p->groups[g].size(); ++k) {

@@ -38,8 +38,11 @@ struct WorkLayout {
   // inverse of its power-of-two scale (m floats each), and the largest row
   // 2-norm of G and of D (one float each, set by atomic max; the group's
   // row-norm slots are contiguous from WorkLayout of its first item's g_rmax,
-  // two floats per item, so one memset clears them).
+  // three floats per item, so one memset clears them).
   uint64_t g_rinv, d_rinv, g_rmax, d_rmax;
+  // refresh steps in 3xF16: M's row-scaled fp16 split (m x ldn), its rows'
+  // inverse scales and row-norm bound (third float of the item's slots)
+  uint64_t m16_hi, m16_lo, m_rinv, m_rmax;
   // refresh region
   uint64_t mT_hi, mT_lo;  // M^T split (n x ldm)
   int zu_rows, zu_ld;

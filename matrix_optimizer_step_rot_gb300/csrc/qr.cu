@@ -905,7 +905,9 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
       }
       if (tr.empty()) continue;
       if (launch_transpose(tr, stream) != ROT_OK) return ROT_ECUDA;
-      // precise: Q's orthogonality error adds up over all p^2 entries
+      // precise: Q's orthogonality error adds up over all p^2 entries (the
+      // rank-256 update too: accumulated in TMEM, in 3xTF32 or 3xF16, it moved
+      // the bases' orthogonality and the W parity measurably)
       if (gemm_grouped(q1, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
       if (gemm_grouped(q2, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
       if (gemm_grouped(q3, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;

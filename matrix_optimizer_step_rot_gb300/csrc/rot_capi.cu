@@ -121,7 +121,8 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
 
   // (1) momentum, and the TF32 split of G (3xF16: its scaled fp16 split)
   if (f16) {
-    if (cudaMemsetAsync(F(work, WL[0].g_rmax), 0, 8 * n_items, s) != cudaSuccess) return ROT_ECUDA;
+    if (cudaMemsetAsync(F(work, WL[0].g_rmax), 0, 12 * n_items, s) != cudaSuccess)
+      return ROT_ECUDA;
     std::vector<Momentum16Seg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
@@ -129,7 +130,9 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const WorkLayout& x = WL[k];
       if (!W[i] || !G[i]) return ROT_EINVAL;
       segs[k] = {G[i], F(state, L.m_hi), F(state, L.m_lo), H(work, x.g_hi), H(work, x.g_lo),
-                 F(work, x.g_rinv), F(work, x.g_rmax), L.m, L.n, L.ldn};
+                 F(work, x.g_rinv), F(work, x.g_rmax), L.m, L.n, L.ldn,
+                 refresh ? H(work, x.m16_hi) : nullptr, H(work, x.m16_lo), F(work, x.m_rinv),
+                 F(work, x.m_rmax)};
     }
     ROT_TRY(launch_momentum16(segs, beta1, s));
   } else {
@@ -235,12 +238,11 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // (3) rotation: S_G^T = (G V)^T ; G~ = U^T S_G.  M~ = U^T M V is recomputed
   // from M only when the bases change (refresh steps); otherwise it follows
   // M~ <- beta1 M~ + (1 - beta1) G~ inside the Adam kernel, which is the same
-  // quantity since U and V are unchanged.  In 3xF16 mode the G side runs on
-  // the fp16 splits (G's rows scaled by s_r, U and V by 2^14, S_G by a power
-  // of two below its bound, the largest row norm of G); the refresh-only M
-  // side stays 3xTF32.
+  // quantity since U and V are unchanged.  In 3xF16 mode both sides run on
+  // the fp16 splits (G's or M's rows scaled by s_r, U and V by 2^14, S_G or
+  // S_M by a power of two below its bound, the largest row norm of G or M).
   {
-    std::vector<GemmProblem> a, b, am, bm;
+    std::vector<GemmProblem> a, b;
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
@@ -261,19 +263,23 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
                        F(work, x.gt), nullptr, L.ldn, kEpiStoreF32));
       }
-      if (refresh) {
-        (f16 ? am : a)
-            .push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
-                          F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
-        (f16 ? bm : b)
-            .push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
-                          F(state, L.mt), nullptr, L.ldn, kEpiStoreF32));
+      if (refresh && f16) {  // the M side as the G side, on M's fp16 split
+        a.push_back(gp16(m, n, n, H(work, x.m16_hi), H(work, x.m16_lo), L.ldn,
+                         H(state, L.vt16_hi), H(state, L.vt16_lo), L.ldn, H(work, x.sm_hi),
+                         H(work, x.sm_lo), L.ldm, kEpiStoreF16SplitT, kF16Inv, F(work, x.m_rinv),
+                         nullptr, F(work, x.m_rmax)));
+        b.push_back(gp16(m, n, m, H(state, L.ut16_hi), H(state, L.ut16_lo), L.ldm,
+                         H(work, x.sm_hi), H(work, x.sm_lo), L.ldm, F(state, L.mt), nullptr,
+                         L.ldn, kEpiStoreF32, kF16Inv, nullptr, F(work, x.m_rmax), nullptr));
+      } else if (refresh) {
+        a.push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
+                       F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
+        b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
+                       F(state, L.mt), nullptr, L.ldn, kEpiStoreF32));
       }
     }
     ROT_TRY(gemm_grouped(a, precision, status, s));
-    if (!am.empty()) ROT_TRY(gemm_grouped(am, ROT_PREC_3XTF32, status, s));
     ROT_TRY(gemm_grouped(b, precision, status, s));
-    if (!bm.empty()) ROT_TRY(gemm_grouped(bm, ROT_PREC_3XTF32, status, s));
   }
 
   // (3') Adam in rotated coordinates; D's split overwrites G's split

@@ -123,6 +123,11 @@ struct Momentum16Seg {
   float* g_rinv;
   float* g_rmax;
   int rows, cols, ldm;
+  // refresh steps: M's row-scaled fp16 split too (m16_hi == nullptr: not)
+  unsigned short* m16_hi;
+  unsigned short* m16_lo;
+  float* m_rinv;
+  float* m_rmax;
 };
 int launch_momentum16(const std::vector<Momentum16Seg>& segs, float beta1, cudaStream_t stream);
 
