@@ -183,11 +183,32 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
       return;
     }
     case kEpiApply: {
+      // every load is issued before the first store: a store may alias a
+      // later load as far as the compiler knows, which would otherwise put
+      // one memory latency between consecutive loads
       if (row >= M) return;
       float* w = P.c_hi + (int64_t)row * P.ldc + col0;
+      if (ncol == 32 && (P.ldc & 3) == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0) {
+        float4 x[8];
 #pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (t < ncol) w[t] = w[t] - P.alpha * __uint_as_float(r[t]);
+        for (int i = 0; i < 8; ++i) x[i] = reinterpret_cast<const float4*>(w)[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[i].x -= P.alpha * __uint_as_float(r[4 * i]);
+          x[i].y -= P.alpha * __uint_as_float(r[4 * i + 1]);
+          x[i].z -= P.alpha * __uint_as_float(r[4 * i + 2]);
+          x[i].w -= P.alpha * __uint_as_float(r[4 * i + 3]);
+          reinterpret_cast<float4*>(w)[i] = x[i];
+        }
+      } else {
+        float x[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (t < ncol) x[t] = w[t];
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (t < ncol) w[t] = x[t] - P.alpha * __uint_as_float(r[t]);
+      }
       return;
     }
     case kEpiApplySplit: {
@@ -196,19 +217,29 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
       float* lo = P.c_lo + (int64_t)row * P.ldc + col0;
       if (ncol == 32 && (P.ldc & 3) == 0 && ((reinterpret_cast<uintptr_t>(hi) & 15) == 0) &&
           ((reinterpret_cast<uintptr_t>(lo) & 15) == 0)) {
+        // per half row-chunk, all eight loads in flight before the first
+        // store (see kEpiApply); halves keep the registers within budget
 #pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          float4 h4 = *reinterpret_cast<const float4*>(hi + t);
-          float4 l4 = *reinterpret_cast<const float4*>(lo + t);
-          float* hp = &h4.x;
-          float* lp = &l4.x;
+        for (int half = 0; half < 2; ++half) {
+          float4 h4[4], l4[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float v = (hp[u] + lp[u]) - P.alpha * __uint_as_float(r[t + u]);
-            split_tf32(v, hp[u], lp[u]);
+          for (int i = 0; i < 4; ++i) {
+            h4[i] = reinterpret_cast<const float4*>(hi)[4 * half + i];
+            l4[i] = reinterpret_cast<const float4*>(lo)[4 * half + i];
           }
-          *reinterpret_cast<float4*>(hi + t) = h4;
-          *reinterpret_cast<float4*>(lo + t) = l4;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float* hp = &h4[i].x;
+            float* lp = &l4[i].x;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float v =
+                  (hp[u] + lp[u]) - P.alpha * __uint_as_float(r[16 * half + 4 * i + u]);
+              split_tf32(v, hp[u], lp[u]);
+            }
+            reinterpret_cast<float4*>(hi)[4 * half + i] = h4[i];
+            reinterpret_cast<float4*>(lo)[4 * half + i] = l4[i];
+          }
         }
       } else {
 #pragma unroll
