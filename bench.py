@@ -445,7 +445,7 @@ def run_reference(args):
         "ms_per_step": secs * 1000.0 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded counter-based generator)",
-        "config": workload_config(wl, "float64 oracle"),
+        "config": workload_config(wl, args.precision),  # the GPU arm's config, unchanged
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -459,6 +459,18 @@ __global__ void __launch_bounds__(256) qr_apply_update_kernel(const __grid_const
     __syncthreads();
     const int row = r0 + r;
     if (row < row_end) {
+      // the four elements' loads go out before any store (a store could
+      // alias a later load as far as the compiler knows)
+      float hv[4], lv[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e = c0 + e4 + c;
+        if (e < e_end) {
+          const int64_t o = (int64_t)row * ld + e;
+          hv[c] = xh[o];
+          lv[c] = xl[o];
+        }
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int e = c0 + e4 + c;
@@ -468,7 +480,7 @@ __global__ void __launch_bounds__(256) qr_apply_update_kernel(const __grid_const
           for (int i = 0; i < B; ++i) t = fmaf(zt[r][i], ys[i][e4 + c], t);
           const int64_t o = (int64_t)row * ld + e;
           float h, l;
-          split_tf32((xh[o] + xl[o]) - t, h, l);
+          split_tf32((hv[c] + lv[c]) - t, h, l);
           xh[o] = h;
           xl[o] = l;
         }
