@@ -63,6 +63,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // 32 values per thread -> lane L of each warp holds the warp's total of v[L]
 // (31 shuffles: each step halves the values a lane keeps).
 __device__ __forceinline__ float warp_transpose_sum(float (&v)[B]) {
@@ -92,26 +98,64 @@ __global__ void qr_init_kernel(const __grid_constant__ QrBatch b) {
   const QrProblem& q = b.p[blockIdx.x];
   const int np = npanels(q.rmax);
   for (int i = threadIdx.x; i < np + 2; i += blockDim.x) q.ctrl[i] = (i == 0) ? -1 : 0;
-  if (threadIdx.x == 0) q.tau[0] = 0.f;
+  if (threadIdx.x == 0) {
+    q.tau[0] = 0.f;
+    q.tau[1] = 0.f;
+  }
 }
 
-// max_j ||a_j|| (rows of `at`), by atomicMax on the float's bits (values >= 0).
+// Range guard.  Q+ of s A is Q+ of A for s > 0 (the reflectors are scale-free
+// and the rank threshold is relative).  When max |a_ij| lies outside
+// [2^-50, 2^50] -- where squared column norms of a p <= 2^15 input could under-
+// or overflow float32 -- the rows the factorisation reads are multiplied by a
+// power of two s with max |a_ij| s < 1 (exact), and the rank threshold with
+// them; inside that range s = 1 and nothing is touched.
+__device__ __forceinline__ float qr_range_scale(float amax) {
+  return (amax >= 8.8817842e-16f && amax <= 1.1258999e15f) ? 1.f : pow2_below(amax, 0);
+}
+
+// max_j ||a_j|| (rows of `at`) into tau[0] and max |a_ij| into tau[1], by
+// atomicMax on the float's bits (values >= 0).  Each column's sum of squares
+// is taken on the column times a power of two c with max |x| c < 1 and then
+// divided by c: the same bits as the plain sum where that does not under- or
+// overflow, the right value where it would.
 __global__ void qr_colnorm_kernel(const __grid_constant__ QrBatch b) {
   const QrProblem& q = b.p[blockIdx.y];
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
-  float best = 0.f;
+  float best = 0.f, amax = 0.f;
   for (int j = blockIdx.x * warps + (threadIdx.x >> 5); j < q.p; j += gridDim.x * warps) {
     const int64_t o = (int64_t)j * q.ld;
+    float cm = 0.f;
+    for (int e = lane; e < q.p; e += 32) cm = fmaxf(cm, fabsf(q.at.hi[o + e] + q.at.lo[o + e]));
+    cm = warp_max(cm);
+    const float c = pow2_below(cm, 0);
     float s = 0.f;
     for (int e = lane; e < q.p; e += 32) {
-      const float x = q.at.hi[o + e] + q.at.lo[o + e];
+      const float x = (q.at.hi[o + e] + q.at.lo[o + e]) * c;
       s = fmaf(x, x, s);
     }
     s = warp_sum(s);
-    best = fmaxf(best, sqrtf(s));
+    best = fmaxf(best, sqrtf(s) * pow2_below_inv(cm, 0));
+    amax = fmaxf(amax, cm);
   }
   if (lane == 0 && best > 0.f) atomicMax(reinterpret_cast<int*>(q.tau), __float_as_int(best));
+  if (lane == 0 && amax > 0.f) atomicMax(reinterpret_cast<int*>(q.tau + 1), __float_as_int(amax));
+}
+
+// s A on the rows the factorisation reads (the first rmax columns of A), when
+// the range guard asks for it.
+__global__ void qr_scale_kernel(const __grid_constant__ QrBatch b) {
+  const QrProblem& q = b.p[blockIdx.y];
+  const float sc = qr_range_scale(q.tau[1]);
+  if (sc == 1.f) return;
+  for (int j = blockIdx.x; j < q.rmax; j += gridDim.x) {
+    const int64_t o = (int64_t)j * q.ld;
+    for (int e = threadIdx.x; e < q.p; e += blockDim.x) {
+      q.at.hi[o + e] *= sc;
+      q.at.lo[o + e] *= sc;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -241,7 +285,7 @@ __global__ void __launch_bounds__(kPanelThreads)
     reduce_and_share(acc, 0);
   }
 
-  const float thr = rtol * q.tau[0];
+  const float thr = rtol * (q.tau[0] * qr_range_scale(q.tau[1]));
   int active = bw;
   for (int j = 0; j < bw; ++j) {
     const int k = k0 + j;
@@ -821,6 +865,10 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
     {
       ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
       qr_colnorm_kernel<<<dim3(std::max(1, std::min(64, pmax / 64)), n), 256, 0, stream>>>(b);
+    }
+    {
+      ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
+      qr_scale_kernel<<<dim3(std::max(1, std::min(512, rmax / 4)), n), 256, 0, stream>>>(b);
     }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
 

@@ -120,26 +120,26 @@ def test_medium_multi_block_parity(precision):
         assert orth(U) <= TOL_ORTH and orth(V) <= TOL_ORTH, (i, orth(U), orth(V))
 
 
-def test_f16_mode_handles_gradients_of_any_scale():
-    """3xF16 scales every operand by a power of two.  Gradients of order 1e-9
-    and 1e5 (outside fp16's range: its smallest subnormal is 6e-8, its largest
-    value 65504), with eps scaled alike so that Adam's step is the same, match
-    the oracle as at the usual scale; a zero gradient leaves W unchanged.
-    (The float32 refresh squares magnitudes -- M M^T U, then column norms --
-    so gradients far below 1e-9 or above 1e5 reach float32's own range limits
-    there, in every mode.)"""
+@pytest.mark.parametrize("precision", FULL)
+def test_gradients_of_any_scale(precision):
+    """Gradients of order 1e-15 and 1e9 -- far outside fp16's range (its
+    smallest subnormal is 6e-8, its largest value 65504), and squared (M M^T U,
+    then the QR's column norms) far outside float32's -- with eps scaled alike
+    so that Adam's step is the same, match the oracle as at the usual scale:
+    3xF16 scales its operands, and the QR its input, by powers of two.  A zero
+    gradient leaves W unchanged."""
     shapes = ((96, 64), (64, 160))
-    for scale in (1e-6, 1e8):
+    for scale in (1e-12, 1e12):
         hyper = inputs.Hyper(eps=float(np.float32(1e-8 * scale)))
         wl = inputs.Workload("scaled", shapes, ("a", "b"), 0.02, 1e-3 * scale, "normal", 4, 2,
                              1 << 30, 31, hyper)
-        W16, _ = run_gpu(wl, F16)
+        Wg, _ = run_gpu(wl, precision)
         ref = orc.run(wl)
         for i in range(wl.count):
             w0 = wl.w0(i).astype(np.float64)
-            e = rel(W16[i].cpu().numpy().astype(np.float64) - w0, ref[i][0] - w0)
-            assert e <= TOL_W[F16], (scale, i, e)
+            e = rel(Wg[i].cpu().numpy().astype(np.float64) - w0, ref[i][0] - w0)
+            assert e <= TOL_W[precision], (scale, i, e)
     wl = inputs.Workload("zero", shapes, ("a", "b"), 0.02, 0.0, "normal", 3, 2, 1 << 30, 32)
-    W16, opt = run_gpu(wl, F16)
+    Wg, opt = run_gpu(wl, precision)
     for i in range(wl.count):
-        np.testing.assert_array_equal(W16[i].cpu().numpy(), wl.w0(i))
+        np.testing.assert_array_equal(Wg[i].cpu().numpy(), wl.w0(i))
