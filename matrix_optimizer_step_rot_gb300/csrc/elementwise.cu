@@ -1,9 +1,12 @@
-// Element-wise kernels of the step: momentum (+ TF32 split of G), the Adam
-// update in rotated coordinates, transposes, fills and exports.
+// Element-wise kernels of the step: momentum (+ the split of G the rotation
+// reads), the Adam update in rotated coordinates, transposes, fills, fp16
+// copies and exports.
 //
 // All of them are HBM-bound.  Each launch covers many matrices: blockIdx.y
-// selects the matrix, blockIdx.x strides over its elements; the per-matrix
-// descriptors travel in the kernel's parameter block.
+// selects the matrix, blockIdx.x strides over its elements (or, for the 3xF16
+// row kernels, over its rows: one block per row, since a row's power-of-two
+// scale needs the row's max first); the per-matrix descriptors travel in the
+// kernel's parameter block.
 #include <algorithm>
 #include <cstring>
 

@@ -25,7 +25,11 @@
 //   * each 256-column block's reflectors form H_k..H_{k+255} = I - Y T Y^T;
 //     the columns after the block (up to rmax) receive a <- (I - Y T^T Y^T) a,
 //     and Q is accumulated backwards block by block, q <- (I - Y T Y^T) q, both
-//     as three tensor-core GEMMs (T^T Y^T or T Y^T, then X (Y T), X -= Z Y^T).
+//     as three tensor-core GEMMs (T^T Y^T or T Y^T, then X (Y T), X -= Z Y^T),
+//     on the precise kernel (K-blocks summed in float32 registers): Q's
+//     orthogonality error adds up over all p^2 entries.
+// A range guard (qr_colnorm_kernel, qr_scale_kernel) rescales inputs whose
+// squared column norms would leave float32's range.
 #include <cooperative_groups.h>
 
 #include <algorithm>

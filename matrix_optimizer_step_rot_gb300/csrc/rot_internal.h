@@ -69,8 +69,8 @@ struct GemmProblem {
   float c0 = 1.f;
 };
 
-// 3xTF32 with each K block accumulated afresh and summed in float32
-// registers, hi*hi kept apart from the cross terms (ROT_PREC_3XTF32_PRECISE);
+// 3xTF32 with each K block of 32 accumulated afresh in TMEM (cross terms
+// first, hi*hi last) and summed in float32 registers (ROT_PREC_3XTF32_PRECISE);
 // used for products whose results cancel.
 constexpr int kPrecPrecise = ROT_PREC_3XTF32_PRECISE;
 
@@ -78,7 +78,8 @@ constexpr int kPrecPrecise = ROT_PREC_3XTF32_PRECISE;
 extern uint64_t g_wait_limit_ns;
 
 // Runs every problem of `probs` (any count; launched in chunks).  precision is
-// ROT_PREC_TF32 or ROT_PREC_3XTF32.  status: device status word (may be
+// ROT_PREC_TF32, ROT_PREC_3XTF32, ROT_PREC_3XF16 (problems marked f16) or
+// kPrecPrecise.  status: device status word (may be
 // nullptr) set to ROT_ETIMEOUT if a bounded wait gives up.
 int gemm_grouped(const std::vector<GemmProblem>& probs, int precision, int* status,
                  cudaStream_t stream);
