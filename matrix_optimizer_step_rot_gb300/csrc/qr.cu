@@ -678,6 +678,7 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
         const int64_t o = (int64_t)r * q.ld_out + c;
         q.ut.hi[o] = h;
         q.ut.lo[o] = l;
+        if (q.ut16_hi) split_f16((h + l) * kF16UnitScale, q.ut16_hi[o], q.ut16_lo[o]);
       }
       tile[i][tx] = v;
     }
@@ -690,6 +691,7 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
         const int64_t o = (int64_t)r * q.ld_out + c;
         q.u.hi[o] = h;
         q.u.lo[o] = l;
+        if (q.u16_hi) split_f16((h + l) * kF16UnitScale, q.u16_hi[o], q.u16_lo[o]);
       }
     }
     __syncthreads();

@@ -226,13 +226,15 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
                          : Split{F(state, L.vt_hi), F(state, L.vt_lo)};
         q.ld_out = ld;
         q.rank_out = ranks + 2 * i + side;
+        // the 3xF16 products' copies of the new basis, written by the QR's last pass
+        q.u16_hi = H(state, side == 0 ? L.u16_hi : L.vb16_hi);
+        q.u16_lo = H(state, side == 0 ? L.u16_lo : L.vb16_lo);
+        q.ut16_hi = H(state, side == 0 ? L.ut16_hi : L.vt16_hi);
+        q.ut16_lo = H(state, side == 0 ? L.ut16_lo : L.vt16_lo);
         qp.push_back(q);
       }
     }
     ROT_TRY(qr_batched(qp, rank_rtol, status, s));
-    std::vector<ToF16Seg> conv;
-    for (size_t k = 0; k < n_items; ++k) push_f16_bases(conv, state, p->items[items[k]]);
-    ROT_TRY(launch_to_f16(conv, s));
   }
 
   // (3) rotation: S_G^T = (G V)^T ; G~ = U^T S_G.  M~ = U^T M V is recomputed

@@ -244,6 +244,11 @@ struct QrProblem {
   Split ut;
   int ld_out;
   int* rank_out;
+  // and, if set, their fp16 splits scaled by 2^14 (ld_out elements per row)
+  unsigned short* u16_hi;
+  unsigned short* u16_lo;
+  unsigned short* ut16_hi;
+  unsigned short* ut16_lo;
 };
 int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status,
                cudaStream_t stream);
