@@ -31,7 +31,8 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
   if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
       precision != ROT_PREC_3XTF32_PRECISE && precision != ROT_PREC_3XF16)
     return ROT_EINVAL;
-  if (precision == ROT_PREC_3XF16 && epi == kEpiApplySplit) return ROT_EINVAL;
+  if (precision == ROT_PREC_3XF16 && (epi == kEpiStoreSplit || epi == kEpiApplySplit))
+    return ROT_EINVAL;  // no fp16 form of the untransposed split outputs
   const bool transposed = epi == kEpiStoreSplitT || epi == kEpiStoreF32T;
   if (ldc < (transposed ? M : N)) return ROT_EINVAL;
   if (work_bytes < rot_test_gemm_work_bytes(M, N, K)) return ROT_EINVAL;
@@ -74,9 +75,7 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
     P.epi = epi == kEpiStoreSplitT ? (int)kEpiStoreF16SplitT : epi;
     P.c_lo = epi == kEpiStoreSplitT
                  ? reinterpret_cast<float*>(reinterpret_cast<unsigned short*>(C) + (int64_t)N * ldc)
-             : epi == kEpiStoreSplit ? C + (int64_t)M * ldc
-                                     : nullptr;
-    if (epi == kEpiStoreSplit) return ROT_EINVAL;  // no untransposed fp16 store
+                 : nullptr;
     P.ldc = ldc;
     P.alpha = alpha;
     P.f16 = 1;

@@ -89,6 +89,12 @@ def test_argument_errors():
                               None) == B.ROT_EINVAL
     assert L.rot_state_export(p.handle, ctypes.c_void_p(256), 0, 7, ctypes.c_void_p(256),
                               None) == B.ROT_EINVAL
+    # the test GEMM validates before any device work: unknown precision, and
+    # the untransposed split outputs, which have no fp16 form
+    vp = ctypes.c_void_p
+    for prec, epi in [(2, 2), (B.ROT_PREC_3XF16, 0), (B.ROT_PREC_3XF16, 5)]:
+        assert L.rot_test_gemm(32, 32, 32, vp(256), 32, vp(256), 32, vp(256), 32, epi, 1.0, prec,
+                               vp(256), 1 << 20, None, None) == B.ROT_EINVAL
     assert B.strerror(B.ROT_EINVAL) == "invalid argument"
 
 
