@@ -52,7 +52,8 @@ extern "C" {
 #define ROT_ENOMEM (-2)      /* host allocation failed */
 #define ROT_ECUDA (-3)       /* a CUDA call or kernel launch failed */
 #define ROT_ETIMEOUT (-4)    /* a device-side wait gave up (see rot_status) */
-#define ROT_ENONFINITE (-5)  /* non-finite value found (see rot_status) */
+#define ROT_ENONFINITE (-5)  /* reserved: non-finite inputs propagate (IEEE) into their own
+                                matrix's results and are not reported */
 #define ROT_ENOTSUP (-6)     /* GPU is not sm_103 or the feature is not built */
 #define ROT_ETOOLARGE (-7)   /* plan needs more scratch than rot_step_noalloc holds */
 
@@ -180,7 +181,10 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream);
  * [1e-6, 1): the QR's numerical-rank threshold relative to the largest
  * column norm.  Non-finite inputs propagate (IEEE).
  * Errors: ROT_EINVAL (null pointers, unknown precision, rank_rtol out of
- * range), ROT_ENOTSUP (device is not sm_103), ROT_ECUDA (launch failure).
+ * range), ROT_ENOTSUP (device is not sm_103, or refresh != 0 for a matrix with
+ * m or n above 24576: the QR holds a panel slice of at most 1536 rows in each
+ * of at most 16 CTAs of a cluster), ROT_ECUDA (launch failure).  An empty plan
+ * returns ROT_OK without touching the device.
  * Device-side problems are reported by rot_status. */
 int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void* state,
              void* work, float beta1, float beta2, float eps, float lr, int32_t refresh,

@@ -109,3 +109,20 @@ def test_empty_plan_and_state_sizes():
     need = sum(4 * (4 * m * n + 4 * m * m + 4 * n * n) + 8 * (m * m + n * n)
                for m, n in wl.shapes)
     assert sb >= need and sb % 256 == 0 and wb > 0
+
+
+def test_host_checked_edge_cases():
+    """Cases the step settles on the host, before any device work."""
+    L = B.lib()
+    vp = ctypes.c_void_p
+    # an empty plan: nothing to do
+    p = B.Plan([], 100)
+    assert L.rot_step(p.handle, None, None, None, None, 0.9, 0.999, 1e-8, 1e-3, 1, 3, 1e-3,
+                      None) == B.ROT_OK
+    # a refresh of a basis larger than the QR takes (16 x 1536 = 24576 rows)
+    p = B.Plan([(24577, 8)], 1 << 40)
+    W = (vp * 1)(vp(256))
+    assert L.rot_step(p.handle, W, W, vp(256), vp(512), 0.9, 0.999, 1e-8, 1e-3, 1, 3, 1e-3,
+                      None) == B.ROT_ENOTSUP
+    # the same matrix without a refresh is not refused on the host (the check
+    # that follows needs a device, so it is not called here)

@@ -143,3 +143,28 @@ def test_gradients_of_any_scale(precision):
     Wg, opt = run_gpu(wl, precision)
     for i in range(wl.count):
         np.testing.assert_array_equal(Wg[i].cpu().numpy(), wl.w0(i))
+
+
+@pytest.mark.parametrize("precision", FULL)
+def test_non_finite_gradient_stays_in_its_matrix(precision):
+    """A NaN in one matrix's gradient (on a refresh step) propagates into that
+    matrix's W (IEEE; nothing is reported) and leaves the other matrices of the
+    same micro-group equal to the oracle's."""
+    wl = inputs.workload("tiny")
+    h = wl.hyper
+    opt = RotatedAdam(wl.shapes, wl.c_max, "cuda", h.beta1, h.beta2, h.eps, h.lr, h.rank_rtol,
+                      precision)
+    W = [torch.from_numpy(wl.w0(i)).cuda() for i in range(wl.count)]
+    for t in range(1, wl.steps + 1):
+        G = [torch.from_numpy(wl.grad(i, t)).cuda() for i in range(wl.count)]
+        if t == wl.refresh_every:
+            G[1][3, 5] = float("nan")
+        opt.step(W, G, wl.refresh(t))
+    torch.cuda.synchronize()
+    assert opt.status() == B.ROT_OK
+    assert torch.isnan(W[1]).any()
+    ref = orc.run(wl, [0, 2, 3])
+    for i in (0, 2, 3):
+        assert torch.isfinite(W[i]).all()
+        e = rel(W[i].cpu().numpy().astype(np.float64), ref[i][0])
+        assert e <= TOL_W[precision], (i, e)
