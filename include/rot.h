@@ -37,6 +37,9 @@
  *   Device work is enqueued on it and the call returns without waiting, except
  *   where stated.
  * - Matrix dimensions: 1 <= m, n <= ROT_MAX_DIM.
+ * - One CUDA device per process: the kernels' launch configuration (shared-
+ *   memory limits, the SM count) is set up once, for the device current at
+ *   the first step.  Data-parallel use runs one process per GPU.
  */
 #ifndef ROT_H_
 #define ROT_H_
