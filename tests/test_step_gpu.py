@@ -168,3 +168,42 @@ def test_non_finite_gradient_stays_in_its_matrix(precision):
         assert torch.isfinite(W[i]).all()
         e = rel(W[i].cpu().numpy().astype(np.float64), ref[i][0])
         assert e <= TOL_W[precision], (i, e)
+
+
+@pytest.mark.parametrize("precision", FULL)
+def test_resume_from_saved_state_is_bit_identical(precision):
+    """Checkpoint/resume: the state blob is caller-owned device memory holding
+    no pointers, so saving it (and W) after step 3 and resuming in a fresh
+    optimizer reproduces the uninterrupted run bit for bit, through a basis
+    refresh (t = 5) and plain steps after it."""
+    wl = inputs.workload("tiny")
+    h = wl.hyper
+
+    def make():
+        return RotatedAdam(wl.shapes, wl.c_max, "cuda", h.beta1, h.beta2, h.eps, h.lr,
+                           h.rank_rtol, precision)
+
+    def grads(t):
+        return [torch.from_numpy(wl.grad(i, t)).cuda() for i in range(wl.count)]
+
+    opt = make()
+    W = [torch.from_numpy(wl.w0(i)).cuda() for i in range(wl.count)]
+    for t in range(1, 4):
+        opt.step(W, grads(t), wl.refresh(t))
+    saved_state = opt.state.clone()
+    saved_W = [w.clone() for w in W]
+    for t in range(4, 8):
+        opt.step(W, grads(t), wl.refresh(t))
+
+    resumed = make()
+    resumed.state.copy_(saved_state)
+    W2 = [w.clone() for w in saved_W]
+    for t in range(4, 8):
+        resumed.step(W2, grads(t), wl.refresh(t))
+    torch.cuda.synchronize()
+    assert opt.status() == B.ROT_OK and resumed.status() == B.ROT_OK
+    for a, b in zip(W, W2):
+        assert torch.equal(a, b)
+    for i in range(wl.count):
+        for which in (B.ROT_WHICH_M, B.ROT_WHICH_V2, B.ROT_WHICH_U, B.ROT_WHICH_V):
+            assert torch.equal(opt.export(i, which), resumed.export(i, which))
