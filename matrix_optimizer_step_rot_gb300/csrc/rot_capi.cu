@@ -10,6 +10,8 @@
 // Every product is C = A * B^T with both operands K-major, so U, V are kept
 // both as-is and transposed, and the intermediates are written in the layout
 // their consumer reads.
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstring>
 #include <vector>
 
@@ -58,6 +60,15 @@ GemmProblem gp(int M, int N, int K, const float* ah, const float* al, int lda, c
 }
 
 constexpr float kF16Inv = 1.f / 16384.f;  // undoes the bases' fixed 2^14 scale
+
+// A named range on the host timeline for profilers (NVTX: no cost unless a
+// tool is attached); closed when the scope ends, early returns included.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
 
 inline unsigned short* H(void* base, uint64_t off) {
   return reinterpret_cast<unsigned short*>(static_cast<char*>(base) + off);
@@ -118,9 +129,11 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   const size_t n_items = items.size();
 
   const bool f16 = precision == ROT_PREC_3XF16;
+  Range group_range("rot: micro-group");
 
   // (1) momentum, and the TF32 split of G (3xF16: its scaled fp16 split)
   if (f16) {
+    Range range("rot: momentum");
     if (cudaMemsetAsync(F(work, WL[0].g_rmax), 0, 12 * n_items, s) != cudaSuccess)
       return ROT_ECUDA;
     std::vector<Momentum16Seg> segs(n_items);
@@ -136,6 +149,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     }
     ROT_TRY(launch_momentum16(segs, beta1, s));
   } else {
+    Range range("rot: momentum");
     std::vector<MomentumSeg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
@@ -149,6 +163,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
 
   // (2) basis refresh
   if (refresh) {
+    Range range("rot: basis refresh");
     std::vector<TransposeSeg> tr(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
@@ -244,6 +259,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // the fp16 splits (G's or M's rows scaled by s_r, U and V by 2^14, S_G or
   // S_M by a power of two below its bound, the largest row norm of G or M).
   {
+    Range range("rot: rotation");
     std::vector<GemmProblem> a, b;
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
@@ -286,6 +302,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
 
   // (3') Adam in rotated coordinates; D's split overwrites G's split
   if (f16) {
+    Range range("rot: adam");
     std::vector<Adam16Seg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
@@ -295,6 +312,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     }
     ROT_TRY(launch_adam16(segs, beta1, beta2, eps, refresh ? 0 : 1, s));
   } else {
+    Range range("rot: adam");
     std::vector<AdamSeg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
@@ -309,6 +327,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // 3xF16 mode D's rows carry their own scales and (D V^T)^T one below the
   // largest row norm of D.
   {
+    Range range("rot: back-rotation and apply");
     std::vector<GemmProblem> a, b;
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
