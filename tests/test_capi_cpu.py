@@ -126,3 +126,14 @@ def test_host_checked_edge_cases():
                       None) == B.ROT_ENOTSUP
     # the same matrix without a refresh is not refused on the host (the check
     # that follows needs a device, so it is not called here)
+
+
+def test_plan_bit_exact_at_scale():
+    """100 000 matrices, many ties and groups, four simulated ranks."""
+    r = np.random.default_rng(77)
+    dims = [64 * k for k in range(1, 33)]
+    shapes = [(int(r.choice(dims)), int(r.choice(dims))) for _ in range(100_000)]
+    p = B.Plan(shapes, 64 << 20, ranks=4)
+    o = orc.plan(shapes, 64 << 20, ranks=4)
+    assert len(o.groups) > 100
+    assert p.groups() == o.groups and p.owners() == o.owners
