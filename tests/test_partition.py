@@ -226,3 +226,16 @@ def test_partition_argument_errors(lib):
         assert e.value.code == E
     assert B.partition_alpha([], [], 3, 1.0) == ([], [0, 0, 0])
     assert B.partition_static([], [0, 0], 3) == []
+
+
+def test_partitions_bit_exact_at_scale(lib):
+    """20 000 items in 2 500 buckets on 64 ranks, several alphas."""
+    r = np.random.default_rng(4242)
+    sizes = [int(x) for x in r.integers(1, 15, 2500)]
+    n = sum(sizes)
+    work = [int(x) for x in r.integers(1, 10 ** 9, n)]
+    elems = [int(x) for x in r.integers(1, 10 ** 7, n)]
+    for alpha in (0.0, 0.8, 1.0):
+        o = orc.alpha_partition(work, sizes, 64, alpha)
+        assert B.partition_alpha(work, sizes, 64, alpha) == (o.owners, o.loads)
+    assert B.partition_static(elems, sizes, 64) == orc.static_partition(elems, sizes, 64)
