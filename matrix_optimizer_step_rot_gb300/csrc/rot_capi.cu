@@ -12,7 +12,9 @@
 // their consumer reads.
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cstring>
+#include <new>
 #include <vector>
 
 #include "plan.h"
@@ -102,17 +104,56 @@ void push_f16_bases(std::vector<ToF16Seg>& segs, void* state, const ItemLayout& 
                   H(state, L.vt16_lo), L.ldn, L.n, L.n});
 }
 
+}  // namespace
+
+// Is the current device an sm_103 part?  The answer is cached per device
+// ordinal (atomics: any host thread may call this); a failing CUDA query
+// (no device, no driver) returns ROT_ECUDA and clears CUDA's last error.
 int check_device() {
-  static int cached = 0;  // 1 ok, -1 not supported
-  if (cached == 0) {
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return ROT_ECUDA;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cached = (major == 10 && minor == 3) ? 1 : -1;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ROT_ECUDA;
   }
-  return cached == 1 ? ROT_OK : ROT_ENOTSUP;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  int verdict = slot ? cached[dev].load(std::memory_order_acquire) : 0;
+  if (verdict == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ROT_ECUDA;
+    }
+    verdict = (major == 10 && minor == 3) ? 1 : -1;
+    if (slot) cached[dev].store(verdict, std::memory_order_release);
+  }
+  return verdict == 1 ? ROT_OK : ROT_ENOTSUP;
 }
+
+// rot_step's host-side argument checks (no device access).
+int check_step_args(const rot_plan* plan, float* const* W, const float* const* G,
+                    const void* state, const void* work, int32_t refresh, int32_t precision,
+                    float rank_rtol) {
+  if (!plan) return ROT_EINVAL;
+  if (plan->count == 0) return ROT_OK;
+  if (!W || !G || !state || !work) return ROT_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(state) & 255) || (reinterpret_cast<uintptr_t>(work) & 255))
+    return ROT_EINVAL;
+  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
+      precision != ROT_PREC_3XTF32_PRECISE && precision != ROT_PREC_3XF16)
+    return ROT_EINVAL;
+  if (!(rank_rtol >= 1e-6f && rank_rtol < 1.f)) return ROT_EINVAL;
+  for (int32_t i = 0; i < plan->count; ++i) {
+    if (!W[i] || !G[i]) return ROT_EINVAL;
+    if (refresh && (plan->shapes[i].m > kQrMaxDim || plan->shapes[i].n > kQrMaxDim))
+      return ROT_ENOTSUP;
+  }
+  return ROT_OK;
+}
+
+namespace {
 
 #define ROT_TRY(x)             \
   do {                         \
@@ -391,27 +432,19 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream) {
 int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void* state,
              void* work, float beta1, float beta2, float eps, float lr, int32_t refresh,
              int32_t precision, float rank_rtol, void* stream) {
-  if (!plan) return ROT_EINVAL;
-  if (plan->count == 0) return ROT_OK;
-  if (!W || !G || !state || !work) return ROT_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(state) & 255) || (reinterpret_cast<uintptr_t>(work) & 255))
-    return ROT_EINVAL;
-  if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
-      precision != ROT_PREC_3XTF32_PRECISE && precision != ROT_PREC_3XF16)
-    return ROT_EINVAL;
-  if (!(rank_rtol >= 1e-6f && rank_rtol < 1.f)) return ROT_EINVAL;
-  for (int32_t i = 0; i < plan->count; ++i) {
-    if (!W[i] || !G[i]) return ROT_EINVAL;
-    if (refresh && (plan->shapes[i].m > kQrMaxDim || plan->shapes[i].n > kQrMaxDim))
-      return ROT_ENOTSUP;
-  }
+  const int args = check_step_args(plan, W, G, state, work, refresh, precision, rank_rtol);
+  if (args != ROT_OK || plan->count == 0) return args;
   const int dev = check_device();
   if (dev != ROT_OK) return dev;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  for (size_t g = 0; g < plan->groups.size(); ++g) {
-    const int e = run_group(plan, g, W, G, state, work, beta1, beta2, eps, lr, refresh != 0,
-                            precision, rank_rtol, s);
-    if (e != ROT_OK) return e;
+  try {
+    for (size_t g = 0; g < plan->groups.size(); ++g) {
+      const int e = run_group(plan, g, W, G, state, work, beta1, beta2, eps, lr, refresh != 0,
+                              precision, rank_rtol, s);
+      if (e != ROT_OK) return e;
+    }
+  } catch (const std::bad_alloc&) {  // the launch descriptors are host vectors
+    return ROT_ENOMEM;
   }
   return ROT_OK;
 }

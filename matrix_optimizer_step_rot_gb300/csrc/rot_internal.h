@@ -261,4 +261,13 @@ void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax);
 // Largest p the QR accepts (panel slices must fit a 16-CTA cluster).
 constexpr int kQrMaxDim = 16 * 1536;
 
+// ROT_OK if the current device is sm_103, ROT_ENOTSUP if it is another GPU,
+// ROT_ECUDA if no device can be queried (CUDA's last error is then cleared).
+int check_device();
+
+// rot_step's host-side argument checks, in its order (no device access).
+int check_step_args(const rot_plan* plan, float* const* W, const float* const* G,
+                    const void* state, const void* work, int32_t refresh, int32_t precision,
+                    float rank_rtol);
+
 }  // namespace rot
