@@ -131,7 +131,8 @@ int rot_partition_static(const uint64_t* elems, int32_t count, const int32_t* bu
 
 /* alpha-balanced greedy LPT partition (Canzona page, section 3.2.1).  Buckets
  * are visited by total work W_b, largest first (ties: lower index first).  For
- * each, with per-rank loads L so far: ideal A = (sum L + W_b) / ranks; deficit
+ * each, with per-rank loads L so far: ideal A = sum L / ranks, the mean load
+ * before the bucket, as the page's code prints it; deficit
  * d_r = max(0, A - L_r); fill share d_r / sum d (1/ranks if every d_r is 0);
  * share s_r = (1 - alpha) / ranks + alpha * fill_r; cut r goes to the item
  * boundary whose prefix work is nearest to W_b (s_0 + ... + s_r) (ties: the
@@ -146,6 +147,20 @@ int rot_partition_static(const uint64_t* elems, int32_t count, const int32_t* bu
 int rot_partition_alpha(const uint64_t* work, int32_t count, const int32_t* bucket_sizes,
                         int32_t n_buckets, int32_t ranks, double alpha, int32_t* owners,
                         uint64_t* loads);
+
+/* rot_partition_alpha with a choice of ideal load.  ROT_ALPHA_IDEAL_BEFORE is
+ * rot_partition_alpha (A = sum L / ranks).  ROT_ALPHA_IDEAL_AFTER takes the
+ * even share once the bucket is placed, A = (sum L + W_b) / ranks: with it,
+ * alpha = 1 levels the loads whenever the bucket covers the deficits, where
+ * the printed rule hands the whole bucket to the ranks below the old mean
+ * (loads (100, 98) and a bucket of 50 unit items end at (100, 148) under it,
+ * at (124, 124) under this one).  Errors as rot_partition_alpha, plus an
+ * unknown `ideal`. */
+#define ROT_ALPHA_IDEAL_BEFORE 0
+#define ROT_ALPHA_IDEAL_AFTER 1
+int rot_partition_alpha_ex(const uint64_t* work, int32_t count, const int32_t* bucket_sizes,
+                           int32_t n_buckets, int32_t ranks, double alpha, int32_t ideal,
+                           int32_t* owners, uint64_t* loads);
 
 /* Free a plan (NULL is accepted). */
 void rot_plan_destroy(rot_plan* plan);

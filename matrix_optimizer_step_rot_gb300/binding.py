@@ -79,6 +79,9 @@ _SIGS = {
                                     ctypes.POINTER(_i32)]),
     "rot_partition_alpha": (_i32, [ctypes.POINTER(_u64), _i32, ctypes.POINTER(_i32), _i32, _i32,
                                    ctypes.c_double, ctypes.POINTER(_i32), ctypes.POINTER(_u64)]),
+    "rot_partition_alpha_ex": (_i32, [ctypes.POINTER(_u64), _i32, ctypes.POINTER(_i32), _i32,
+                                      _i32, ctypes.c_double, _i32, ctypes.POINTER(_i32),
+                                      ctypes.POINTER(_u64)]),
 }
 
 
@@ -189,16 +192,25 @@ def partition_static(elems: Sequence[int], bucket_sizes: Sequence[int], ranks: i
     return [out[i] for i in range(n)]
 
 
+ROT_ALPHA_IDEAL_BEFORE, ROT_ALPHA_IDEAL_AFTER = 0, 1
+
+
 def partition_alpha(work: Sequence[int], bucket_sizes: Sequence[int], ranks: int,
-                    alpha: float) -> Tuple[List[int], List[int]]:
-    """rot_partition_alpha: (owner of every item, total work per rank)."""
+                    alpha: float, ideal: str = "before") -> Tuple[List[int], List[int]]:
+    """rot_partition_alpha (ideal "before", the page's rule) or
+    rot_partition_alpha_ex with ROT_ALPHA_IDEAL_AFTER (ideal "after"):
+    (owner of every item, total work per rank)."""
     n, nb = len(work), len(bucket_sizes)
     w = (_u64 * max(n, 1))(*work)
     b = (_i32 * max(nb, 1))(*bucket_sizes)
     out = (_i32 * max(n, 1))()
     loads = (_u64 * max(ranks, 1))()
-    _check(lib().rot_partition_alpha(w, n, b, nb, ranks, float(alpha), out, loads),
-           "rot_partition_alpha")
+    if ideal == "before":
+        rc = lib().rot_partition_alpha(w, n, b, nb, ranks, float(alpha), out, loads)
+    else:
+        code = {"after": ROT_ALPHA_IDEAL_AFTER}.get(ideal, -1)
+        rc = lib().rot_partition_alpha_ex(w, n, b, nb, ranks, float(alpha), code, out, loads)
+    _check(rc, "rot_partition_alpha")
     return [out[i] for i in range(n)], [loads[r] for r in range(ranks)]
 
 

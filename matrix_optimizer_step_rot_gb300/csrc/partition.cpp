@@ -4,8 +4,10 @@
 // ZeRO-1 bucket.  Section 3.2.1: the alpha-balanced greedy LPT partition --
 // buckets by work, largest first; per-rank deficits against the ideal load;
 // shares mixed between an even split (alpha -> 0) and deficit filling
-// (alpha -> 1); cuts placed on parameter boundaries.  The ideal load is taken
-// as the even share once the bucket is placed, (sum L + W_b) / R.
+// (alpha -> 1); cuts placed on parameter boundaries.  The ideal load is the
+// mean load before the bucket, sum L / R, as the page's code prints it
+// (ROT_ALPHA_IDEAL_BEFORE), or, as an option, the even share once the bucket
+// is placed, (sum L + W_b) / R (ROT_ALPHA_IDEAL_AFTER).
 //
 // The cuts are decided in float64.  This file is compiled without
 // floating-point contraction, and every sum runs in a fixed order, so the
@@ -86,12 +88,13 @@ extern "C" int rot_partition_static(const uint64_t* elems, int32_t count,
   return ROT_OK;
 }
 
-extern "C" int rot_partition_alpha(const uint64_t* work, int32_t count,
-                                   const int32_t* bucket_sizes, int32_t n_buckets,
-                                   int32_t ranks, double alpha, int32_t* owners,
-                                   uint64_t* loads) {
+extern "C" int rot_partition_alpha_ex(const uint64_t* work, int32_t count,
+                                      const int32_t* bucket_sizes, int32_t n_buckets,
+                                      int32_t ranks, double alpha, int32_t ideal,
+                                      int32_t* owners, uint64_t* loads) {
   if (bad_common(count, bucket_sizes, n_buckets, ranks, work, owners)) return ROT_EINVAL;
   if (!(alpha >= 0.0 && alpha <= 1.0)) return ROT_EINVAL;
+  if (ideal != ROT_ALPHA_IDEAL_BEFORE && ideal != ROT_ALPHA_IDEAL_AFTER) return ROT_EINVAL;
   uint64_t total = 0;
   for (int32_t i = 0; i < count; ++i) {
     if (work[i] >= kExactLimit - total) return ROT_EINVAL;
@@ -121,10 +124,11 @@ extern "C" int rot_partition_alpha(const uint64_t* work, int32_t count,
       const int64_t s0 = start[(size_t)b], nb = bucket_sizes[b];
       uint64_t placed = 0;
       for (size_t r = 0; r < R; ++r) placed += L[r];
-      const double ideal = (double)(placed + Wb) / Rd;
+      if (ideal == ROT_ALPHA_IDEAL_AFTER) placed += Wb;
+      const double target_load = (double)placed / Rd;
       double dsum = 0.0;
       for (size_t r = 0; r < R; ++r) {
-        const double d = ideal - (double)L[r];
+        const double d = target_load - (double)L[r];
         deficit[r] = d > 0.0 ? d : 0.0;
         dsum += deficit[r];
       }
@@ -168,4 +172,12 @@ extern "C" int rot_partition_alpha(const uint64_t* work, int32_t count,
     return ROT_ENOMEM;
   }
   return ROT_OK;
+}
+
+extern "C" int rot_partition_alpha(const uint64_t* work, int32_t count,
+                                   const int32_t* bucket_sizes, int32_t n_buckets,
+                                   int32_t ranks, double alpha, int32_t* owners,
+                                   uint64_t* loads) {
+  return rot_partition_alpha_ex(work, count, bucket_sizes, n_buckets, ranks, alpha,
+                                ROT_ALPHA_IDEAL_BEFORE, owners, loads);
 }

@@ -141,15 +141,21 @@ def static_partition(elems: Sequence[int], bucket_sizes: Sequence[int], ranks: i
     return owners
 
 
+IDEAL_BEFORE = "before"  # the page's printed ideal load: sum(L) / R
+IDEAL_AFTER = "after"    # the even share once the bucket is placed: (sum(L) + W_b) / R
+
+
 def alpha_partition(work: Sequence[int], bucket_sizes: Sequence[int], ranks: int,
-                    alpha: float) -> Partition:
+                    alpha: float, ideal: str = IDEAL_BEFORE) -> Partition:
     """α-balanced greedy LPT partition of buckets of items (section 3.2.1).
 
     Items lie in physical order; bucket b is the next bucket_sizes[b] of them
     and its work W_b is the sum of its items' work.
     1. Visit the buckets by W_b, largest first (equal W_b: lower index first).
-    2. For the bucket at hand, with per-rank loads L so far: the ideal load is
-       A = (sum(L) + W_b) / R (the even share once this bucket is placed);
+    2. For the bucket at hand, with per-rank loads L so far: the ideal load A
+       is sum(L) / R, the mean load before the bucket, as the page's code
+       prints it (ideal="before"), or (sum(L) + W_b) / R, the mean once the
+       bucket is placed (ideal="after", this library's alternative reading);
        deficit d_r = max(0, A - L_r); fill shares v_fill = d / sum(d) (1/R each
        if every deficit is zero); even shares 1/R; mixed shares
        v*_r = (1 - alpha) / R + alpha * v_fill_r.
@@ -163,6 +169,8 @@ def alpha_partition(work: Sequence[int], bucket_sizes: Sequence[int], ranks: int
     """
     if ranks < 1:
         raise ValueError("ranks must be >= 1")
+    if ideal not in (IDEAL_BEFORE, IDEAL_AFTER):
+        raise ValueError("ideal must be 'before' or 'after'")
     if sum(bucket_sizes) != len(work):
         raise ValueError("bucket sizes must cover the items")
     starts, s = [], 0
@@ -175,8 +183,9 @@ def alpha_partition(work: Sequence[int], bucket_sizes: Sequence[int], ranks: int
     loads = [0] * ranks
     for b in order:
         items = list(range(starts[b], starts[b] + bucket_sizes[b]))
-        ideal = float(sum(loads) + bwork[b]) / float(ranks)
-        deficit = [max(0.0, ideal - float(l)) for l in loads]
+        placed = sum(loads) + (bwork[b] if ideal == IDEAL_AFTER else 0)
+        target_load = float(placed) / float(ranks)
+        deficit = [max(0.0, target_load - float(l)) for l in loads]
         dsum = 0.0
         for d in deficit:
             dsum += d

@@ -29,7 +29,8 @@ def test_hand_worked_alpha_mix():
 
     Bucket [7]: loads 0, even targets 3.5; boundaries 0 and 7 are equally near,
     the earlier wins: rank 0 takes nothing, rank 1 takes the 7.  Loads (0, 7).
-    Bucket of ones: ideal (7 + 7) / 2 = 7, deficits (7, 0), fill (1, 0).
+    Bucket of ones: ideal 7 / 2 (printed rule) or (7 + 7) / 2 (after the
+    bucket), deficits (3.5, 0) or (7, 0): fill (1, 0) either way.
       alpha = 1: share (1, 0), cut at 7: loads (7, 7).
       alpha = 0: share (0.5, 0.5), target 3.5, boundaries 3 and 4 tie -> 3: (3, 11).
       alpha = 0.5: share (0.75, 0.25), target 5.25 -> 5: (5, 9)."""
@@ -39,16 +40,70 @@ def test_hand_worked_alpha_mix():
         (0.0, [1, 0, 0, 0, 1, 1, 1, 1], [3, 11]),
         (0.5, [1, 0, 0, 0, 0, 0, 1, 1], [5, 9]),
     ]:
-        p = orc.alpha_partition(work, [1, 7], 2, alpha)
-        assert p.owners == owners and p.loads == loads, alpha
+        for ideal in ("before", "after"):  # fill (1, 0) under either ideal here
+            p = orc.alpha_partition(work, [1, 7], 2, alpha, ideal)
+            assert p.owners == owners and p.loads == loads, (alpha, ideal)
 
 
 def test_bucket_order_is_by_work_not_position():
     """Buckets [1, 1] (W = 2) then [6] (W = 6) on two ranks: the 6 is placed
     first (tie at 3 between boundaries 0 and 6 -> rank 1 gets it), then the
     ones fill rank 0 under alpha = 1."""
-    p = orc.alpha_partition([1, 1, 6], [2, 1], 2, 1.0)
-    assert p.owners == [0, 0, 1] and p.loads == [2, 6]
+    for ideal in ("before", "after"):
+        p = orc.alpha_partition([1, 1, 6], [2, 1], 2, 1.0, ideal)
+        assert p.owners == [0, 0, 1] and p.loads == [2, 6]
+
+
+def test_printed_ideal_against_the_post_bucket_ideal():
+    """Buckets [100], [98], fifty ones; two ranks; alpha = 1.
+
+    [100] from zero loads: fill 1/2 under both readings, target 50, boundaries
+    0 and 100 tie, the earlier wins: rank 1 takes it, loads (0, 100).
+    [98]: printed ideal 100 / 2 = 50, deficits (50, 0); post-bucket ideal
+    (100 + 98) / 2 = 99, deficits (99, 0): fill (1, 0) either way, loads
+    (98, 100).
+    Ones: printed ideal 198 / 2 = 99, deficits (1, 0), fill (1, 0): rank 0
+    takes all fifty, loads (148, 100).  Post-bucket ideal 248 / 2 = 124,
+    deficits (26, 24), fill (26/50, 24/50), target 26: loads (124, 124)."""
+    work = [100, 98] + [1] * 50
+    before = orc.alpha_partition(work, [1, 1, 50], 2, 1.0, "before")
+    assert before.owners == [1, 0] + [0] * 50 and before.loads == [148, 100]
+    assert orc.alpha_partition(work, [1, 1, 50], 2, 1.0) == before  # the default
+    after = orc.alpha_partition(work, [1, 1, 50], 2, 1.0, "after")
+    assert after.owners == [1, 0] + [0] * 26 + [1] * 24 and after.loads == [124, 124]
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_printed_ideal_alpha_one_skips_ranks_at_or_above_the_mean(seed):
+    """Printed rule, alpha = 1: a rank whose load is at or above the mean before
+    the bucket has no deficit, hence share 0, and its piece lies between two
+    cuts aimed at the same target: it receives nothing from that bucket
+    (unless no rank is below the mean, when the shares are even)."""
+    r = np.random.default_rng(70 + seed)
+    R = int(r.integers(2, 6))
+    sizes = [int(x) for x in r.integers(1, 12, 7)]
+    work = [int(x) for x in r.integers(1, 50, sum(sizes))]
+    starts = [sum(sizes[:b]) for b in range(len(sizes))]
+    bwork = [sum(work[starts[b]:starts[b] + sizes[b]]) for b in range(len(sizes))]
+    order = sorted(range(len(sizes)), key=lambda b: (-bwork[b], b))
+    loads = [0] * R
+    for k, b in enumerate(order):
+        # the partition of the first k + 1 buckets visited is the state after them
+        keep = set(order[:k + 1])
+        sub_sizes = [sizes[c] if c in keep else 0 for c in range(len(sizes))]
+        sub_work = [work[i] for c in range(len(sizes)) if c in keep
+                    for i in range(starts[c], starts[c] + sizes[c])]
+        p = orc.alpha_partition(sub_work, sub_sizes, R, 1.0, "before")
+        mean = sum(loads) / R
+        if any(l < mean for l in loads):
+            got = [0] * R
+            at = sum(sub_sizes[c] for c in range(b))
+            for j in range(sizes[b]):
+                got[p.owners[at + j]] += work[starts[b] + j]
+            for q in range(R):
+                if loads[q] >= mean:
+                    assert got[q] == 0, (k, q, loads, got)
+        loads = p.loads
 
 
 def test_single_rank_owns_everything():
@@ -74,7 +129,7 @@ def test_alpha_zero_splits_divisible_buckets_evenly():
 
 @pytest.mark.parametrize("seed", range(6))
 def test_alpha_one_keeps_unit_loads_within_one_of_ideal(seed):
-    """alpha = 1 with unit-work items and every bucket holding >= 2R items:
+    """Post-bucket ideal, alpha = 1, with unit-work items and every bucket holding >= 2R items:
     every load stays within 1 of the ideal after every bucket.  (The loads stay
     within 2 of each other, so each bucket's ideal is above every load; the
     fill targets are then the exact deficits and rounding each cut moves a
@@ -84,7 +139,7 @@ def test_alpha_one_keeps_unit_loads_within_one_of_ideal(seed):
     R = int(r.integers(2, 7))
     sizes = sorted((int(x) for x in r.integers(2 * R, 12 * R, 8)), reverse=True)
     for k in range(1, len(sizes) + 1):
-        p = orc.alpha_partition([1] * sum(sizes[:k]), sizes[:k], R, 1.0)
+        p = orc.alpha_partition([1] * sum(sizes[:k]), sizes[:k], R, 1.0, "after")
         ideal = sum(sizes[:k]) / R
         assert max(abs(l - ideal) for l in p.loads) <= 1.0, (k, p.loads, ideal)
 
@@ -101,7 +156,7 @@ def test_single_bucket_cuts_are_nearest_boundaries_by_brute_force(seed):
     work = [int(x) for x in r.integers(0, 9, n)]
     W = sum(work)
     prefix = [0] + list(itertools.accumulate(work))
-    p = orc.alpha_partition(work, [n], R, float(r.uniform(0, 1)))
+    p = orc.alpha_partition(work, [n], R, float(r.uniform(0, 1)), ["before", "after"][seed % 2])
     cuts, at = [], 0
     for q in range(R - 1):
         while at < n and p.owners[at] <= q:
@@ -126,7 +181,7 @@ def test_partition_invariants(seed):
     sizes = [int(x) for x in r.integers(0, 9, int(r.integers(1, 10)))]
     work = [int(x) for x in r.integers(0, 10 ** 6, sum(sizes))]
     R = int(r.integers(1, 9))
-    p = orc.alpha_partition(work, sizes, R, float(r.uniform(0, 1)))
+    p = orc.alpha_partition(work, sizes, R, float(r.uniform(0, 1)), ["before", "after"][seed % 2])
     assert all(0 <= o < R for o in p.owners)
     at = 0
     for c in sizes:
@@ -158,8 +213,9 @@ def test_alpha_one_beats_static_on_the_qwen_stack():
     static_loads = [0] * 8
     for i, o in enumerate(st):
         static_loads[o] += work[i]
-    p = orc.alpha_partition(work, [7] * 28, 8, 1.0)
-    assert orc.imbalance(p.loads) < 1.1 < 2.0 < orc.imbalance(static_loads)
+    for ideal in ("before", "after"):
+        p = orc.alpha_partition(work, [7] * 28, 8, 1.0, ideal)
+        assert orc.imbalance(p.loads) < 1.1 < 2.0 < orc.imbalance(static_loads), ideal
 
 
 # ---------------------------------------------------- C ABI against the oracle
@@ -180,9 +236,10 @@ def test_alpha_partition_bit_exact(lib, seed):
         work = [work[0]] * len(work)
     R = int(r.integers(1, 12))
     alpha = [0.0, 1.0, float(r.uniform(0, 1)), 0.8][seed % 4]
-    o = orc.alpha_partition(work, sizes, R, alpha)
-    owners, loads = B.partition_alpha(work, sizes, R, alpha)
-    assert owners == o.owners and loads == o.loads
+    for ideal in ("before", "after"):
+        o = orc.alpha_partition(work, sizes, R, alpha, ideal)
+        owners, loads = B.partition_alpha(work, sizes, R, alpha, ideal)
+        assert owners == o.owners and loads == o.loads, ideal
 
 
 @pytest.mark.parametrize("name", ["full", "ragged", "slice8b"])
@@ -194,8 +251,9 @@ def test_workload_partitions_bit_exact(lib, name, ranks):
     work = B.item_work(wl.shapes)
     elems = [m * n for m, n in wl.shapes]
     for alpha in (0.0, 0.8, 1.0):
-        o = orc.alpha_partition(work, sizes, ranks, alpha)
-        assert B.partition_alpha(work, sizes, ranks, alpha) == (o.owners, o.loads)
+        for ideal in ("before", "after"):
+            o = orc.alpha_partition(work, sizes, ranks, alpha, ideal)
+            assert B.partition_alpha(work, sizes, ranks, alpha, ideal) == (o.owners, o.loads)
     assert B.partition_static(elems, sizes, ranks) == orc.static_partition(elems, sizes, ranks)
 
 
@@ -217,6 +275,7 @@ def test_partition_argument_errors(lib):
         lambda: B.partition_alpha([1, 2], [2], 2, 1.5),           # alpha
         lambda: B.partition_alpha([1, 2], [2], 2, float("nan")),
         lambda: B.partition_alpha([2 ** 52, 2 ** 52], [2], 2, 1.0),  # total >= 2^53
+        lambda: B.partition_alpha([1, 2], [2], 2, 0.5, "sideways"),  # unknown ideal
         lambda: B.partition_static([1, 2], [1], 2),
         lambda: B.partition_static([2 ** 63, 2 ** 63], [2], 2),   # bucket total overflows
         lambda: B.item_work([(0, 4)]),
@@ -236,6 +295,7 @@ def test_partitions_bit_exact_at_scale(lib):
     work = [int(x) for x in r.integers(1, 10 ** 9, n)]
     elems = [int(x) for x in r.integers(1, 10 ** 7, n)]
     for alpha in (0.0, 0.8, 1.0):
-        o = orc.alpha_partition(work, sizes, 64, alpha)
-        assert B.partition_alpha(work, sizes, 64, alpha) == (o.owners, o.loads)
+        for ideal in ("before", "after"):
+            o = orc.alpha_partition(work, sizes, 64, alpha, ideal)
+            assert B.partition_alpha(work, sizes, 64, alpha, ideal) == (o.owners, o.loads)
     assert B.partition_static(elems, sizes, 64) == orc.static_partition(elems, sizes, 64)
