@@ -55,8 +55,8 @@ extern "C" {
 #define ROT_ENOMEM (-2)      /* host allocation failed */
 #define ROT_ECUDA (-3)       /* a CUDA call or kernel launch failed */
 #define ROT_ETIMEOUT (-4)    /* a device-side wait gave up (see rot_status) */
-#define ROT_ENONFINITE (-5)  /* reserved: non-finite inputs propagate (IEEE) into their own
-                                matrix's results and are not reported */
+#define ROT_ENONFINITE (-5)  /* a non-finite gradient or update was seen (reported by
+                                rot_status while rot_set_nonfinite_check is on) */
 #define ROT_ENOTSUP (-6)     /* GPU is not sm_103 or the feature is not built */
 #define ROT_ETOOLARGE (-7)   /* plan needs more scratch than rot_step_noalloc holds */
 
@@ -229,9 +229,11 @@ int rot_step_noalloc(const rot_plan* plan, float* const* W, const float* const* 
                      int32_t precision, float rank_rtol, void* stream);
 
 /* Synchronise `stream`, then read and clear the device status word of
- * `state`: *status = ROT_OK, or ROT_ETIMEOUT if a device-side wait exceeded its
- * spin limit since the last call.  Returns ROT_ECUDA if the synchronisation
- * fails. */
+ * `state`: *status = ROT_OK; ROT_ETIMEOUT if a device-side wait exceeded its
+ * spin limit since the last call; ROT_ENONFINITE if, while the non-finite
+ * check was on, a gradient element or an element of an update D was NaN or
+ * infinite (the first problem seen is kept).  Returns ROT_ECUDA if the
+ * synchronisation fails. */
 int rot_status(const rot_plan* plan, void* state, int32_t* status, void* stream);
 
 /* Copy one state matrix of input item `item` as float32 row-major into the
@@ -245,6 +247,16 @@ int rot_state_export(const rot_plan* plan, const void* state, int32_t item, int3
  * refresh).  Errors: ROT_EINVAL, ROT_ECUDA. */
 int rot_state_ranks(const rot_plan* plan, const void* state, int32_t item, int32_t* rank_u,
                     int32_t* rank_v, void* stream);
+
+/* Non-finite check (a diagnostic in the spirit of the ZeRO essay's section
+ * 4.4 checks on gradients and the second moment): with on != 0, later steps'
+ * element-wise kernels test every gradient element and every element of the
+ * rotated update D = M~ / (sqrt(v) + eps), and rot_status then reports
+ * ROT_ENONFINITE if one was not finite.  The values themselves still
+ * propagate (IEEE) into their own matrix's results.  Off by default; the test
+ * costs no extra memory traffic.  Returns the previous setting.  Host-side
+ * setting shared by all plans. */
+int32_t rot_set_nonfinite_check(int32_t on);
 
 /* Set the upper bound, in nanoseconds, on every device-side wait of later
  * launches (default 2 000 000 000 = 2 s); returns the previous bound.  A wait

@@ -37,6 +37,15 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
  * ROT_ETIMEOUT; the context stays usable.  Errors: ROT_EINVAL, ROT_ECUDA. */
 int rot_test_wait_timeout(uint64_t limit_ns, int32_t* status, void* stream);
 
+/* Host allocation failure injection.  The library's host containers (plan,
+ * partitions, the step's launch descriptors) allocate through one allocator;
+ * with after >= 0, the allocation that follows `after` more successful ones
+ * fails once, and the entry point that made it returns ROT_ENOMEM (rot_step
+ * then has stepped the micro-groups before the failing one, and none after
+ * it).  after < 0 cancels a planned failure.  Host-side, no device work;
+ * returns ROT_OK. */
+int rot_test_fail_host_alloc(int64_t after);
+
 /* Workspace bytes rot_test_gemm needs for these sizes. */
 uint64_t rot_test_gemm_work_bytes(int32_t M, int32_t N, int32_t K);
 

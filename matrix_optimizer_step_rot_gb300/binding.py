@@ -68,12 +68,19 @@ _SIGS = {
     "rot_state_ranks": (_i32, [_vp, _vp, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp]),
     "rot_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "rot_set_wait_timeout_ns": (_u64, [_u64]),
+    "rot_set_nonfinite_check": (_i32, [_i32]),
+    "rot_launch_count": (_u64, []),
+    "rot_profile_enable": (_i32, [_i32]),
+    "rot_profile_reset": (_i32, []),
+    "rot_profile_read": (_i32, [_i32, ctypes.POINTER(_u64), ctypes.POINTER(ctypes.c_double),
+                                ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "rot_step_noalloc": (_i32, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _f32, _f32,
                                 _f32, _f32, _i32, _i32, _f32, _vp]),
     "rot_test_gemm": (_i32, [_i32, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _i32,
                              _vp, _u64, _vp, _vp]),
     "rot_test_gemm_work_bytes": (_u64, [_i32, _i32, _i32]),
     "rot_test_wait_timeout": (_i32, [_u64, _vp, _vp]),
+    "rot_test_fail_host_alloc": (_i32, [ctypes.c_int64]),
     "rot_item_work": (_i32, [ctypes.POINTER(rot_shape), _i32, ctypes.POINTER(_u64)]),
     "rot_partition_static": (_i32, [ctypes.POINTER(_u64), _i32, ctypes.POINTER(_i32), _i32, _i32,
                                     ctypes.POINTER(_i32)]),

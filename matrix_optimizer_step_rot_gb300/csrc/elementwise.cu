@@ -33,7 +33,7 @@ inline unsigned grid_x_for(int64_t elems) {
 
 // bytes_per_elem: algorithmic bytes each element moves (for instrumentation)
 template <class Seg, class Kernel, class... Args>
-int launch_segs(const std::vector<Seg>& segs, double bytes_per_elem, Kernel kernel,
+int launch_segs(const hvec<Seg>& segs, double bytes_per_elem, Kernel kernel,
                 cudaStream_t stream, Args... args) {
   for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
     SegBatch<Seg> b;
@@ -55,16 +55,28 @@ int launch_segs(const std::vector<Seg>& segs, double bytes_per_elem, Kernel kern
   return ROT_OK;
 }
 
+// Optional non-finite check (rot_set_nonfinite_check): `flag` is the status
+// word or null.  A thread that saw a non-finite value sets it to
+// ROT_ENONFINITE once (unless another status is already there); the values
+// themselves propagate untouched.
+__device__ __forceinline__ void report_nonfinite(int* flag, bool seen) {
+  if (flag && seen) atomicCAS(flag, 0, ROT_ENONFINITE);
+}
+
 // M <- beta1 M + (1 - beta1) G, with M held as a split; also writes G's split.
-__global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b, float beta1) {
+__global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b, float beta1,
+                                int* flag) {
   const MomentumSeg& s = b.seg[blockIdx.y];
   const int64_t total = (int64_t)s.rows * s.cols;
   const float one_minus = 1.0f - beta1;
+  const bool check = flag != nullptr;
+  bool bad = false;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
     const int64_t o = (int64_t)r * s.ldm + c;
     const float g = s.g[e];
+    bad |= check && !isfinite(g);
     const float m = beta1 * (s.m_hi[o] + s.m_lo[o]) + one_minus * g;
     float h, l;
     split_tf32(m, h, l);
@@ -74,13 +86,16 @@ __global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b,
     s.g_hi[o] = h;
     s.g_lo[o] = l;
   }
+  report_nonfinite(flag, bad);
 }
 
 // [M~ <- beta1 M~ + (1 - beta1) G~;]  v <- beta2 v + (1 - beta2) G~^2 ;
 // D = M~ / (sqrt(v) + eps)  (D as a split)
 __global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float beta1, float beta2,
-                            float eps, int incremental) {
+                            float eps, int incremental, int* flag) {
   const AdamSeg& s = b.seg[blockIdx.y];
+  const bool check = flag != nullptr;
+  bool bad = false;
   const int64_t total = (int64_t)s.rows * s.cols;
   const float one_minus1 = 1.0f - beta1;
   const float one_minus = 1.0f - beta2;
@@ -97,11 +112,13 @@ __global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float b
     const float v = beta2 * s.v[o] + one_minus * (g * g);
     s.v[o] = v;
     const float d = m / (sqrtf(v) + eps);
+    bad |= check && !isfinite(d);
     float h, l;
     split_tf32_mma(d, h, l);
     s.d_hi[o] = h;
     s.d_lo[o] = l;
   }
+  report_nonfinite(flag, bad);
 }
 
 // Sum and max over the block (256 threads); every thread gets both.
@@ -154,7 +171,7 @@ __device__ __forceinline__ void momentum_elem(float x, float& hi, float& lo, flo
 }
 
 __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg> b,
-                                  float beta1) {
+                                  float beta1, int* flag) {
   const Momentum16Seg& s = b.seg[blockIdx.y];
   const float one_minus = 1.0f - beta1;
   const int nv = ((s.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(s.g) & 15) == 0)
@@ -184,6 +201,8 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
     if (threadIdx.x == 0) {
       s.g_rinv[r] = pow2_below_inv(mx, kF16ScaleExp);
       atomic_max_nonneg(s.g_rmax, row_norm_bound(sum, mx, s.cols));
+      // the row's sum of squares is finite iff every g of the row is
+      report_nonfinite(flag, !isfinite(sum) && !(sum > 3.402823466e38f && isfinite(mx)));
     }
     if (s.m16_hi) {
       // M's new row (this thread's own writes above), its scale and split
@@ -235,7 +254,7 @@ __device__ __forceinline__ float adam_elem(float g, float& m, float& v, float be
 }
 
 __global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, float beta1,
-                              float beta2, float eps, int incremental) {
+                              float beta2, float eps, int incremental, int* flag) {
   const Adam16Seg& s = b.seg[blockIdx.y];
   const float one_minus1 = 1.0f - beta1;
   const float one_minus = 1.0f - beta2;
@@ -269,6 +288,7 @@ __global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, flo
     if (threadIdx.x == 0) {
       s.d_rinv[r] = pow2_below_inv(mx, kF16ScaleExp);
       atomic_max_nonneg(s.d_rmax, row_norm_bound(sum, mx, s.cols));
+      report_nonfinite(flag, !isfinite(sum) && !(sum > 3.402823466e38f && isfinite(mx)));
     }
     for (int q = threadIdx.x; q < nv; q += blockDim.x) {
       const float4 m = reinterpret_cast<const float4*>(mt)[q];
@@ -408,21 +428,22 @@ __global__ void combine_kernel(const float* hi, const float* lo, int ld_src, flo
 
 }  // namespace
 
-int launch_momentum(const std::vector<MomentumSeg>& segs, float beta1, cudaStream_t stream) {
+int launch_momentum(const hvec<MomentumSeg>& segs, float beta1, int* flag,
+                    cudaStream_t stream) {
   // read G (4) and M's split (8); write M's split (8) and G's split (8)
-  return launch_segs(segs, 28.0, momentum_kernel, stream, beta1);
+  return launch_segs(segs, 28.0, momentum_kernel, stream, beta1, flag);
 }
 
-int launch_adam(const std::vector<AdamSeg>& segs, float beta1, float beta2, float eps,
-                int incremental, cudaStream_t stream) {
+int launch_adam(const hvec<AdamSeg>& segs, float beta1, float beta2, float eps,
+                int incremental, int* flag, cudaStream_t stream) {
   // read G~, M~, v (12); write v (4) and D's split (8); incremental: write M~ (4)
   return launch_segs(segs, incremental ? 28.0 : 24.0, adam_kernel, stream, beta1, beta2, eps,
-                     incremental);
+                     incremental, flag);
 }
 
 // One block per row: grid.x covers the rows (up to 1024 blocks per matrix).
 template <class Seg, class Kernel, class... Args>
-int launch_rows(const std::vector<Seg>& segs, double bytes_per_elem, Kernel kernel,
+int launch_rows(const hvec<Seg>& segs, double bytes_per_elem, Kernel kernel,
                 cudaStream_t stream, Args... args) {
   for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
     SegBatch<Seg> b;
@@ -444,27 +465,28 @@ int launch_rows(const std::vector<Seg>& segs, double bytes_per_elem, Kernel kern
   return ROT_OK;
 }
 
-int launch_momentum16(const std::vector<Momentum16Seg>& segs, float beta1, cudaStream_t stream) {
+int launch_momentum16(const hvec<Momentum16Seg>& segs, float beta1, int* flag,
+                      cudaStream_t stream) {
   // read G (4) and M's split (8); write M's split (8) and G's fp16 split (4)
-  return launch_rows(segs, 24.0, momentum16_kernel, stream, beta1);
+  return launch_rows(segs, 24.0, momentum16_kernel, stream, beta1, flag);
 }
 
-int launch_adam16(const std::vector<Adam16Seg>& segs, float beta1, float beta2, float eps,
-                  int incremental, cudaStream_t stream) {
+int launch_adam16(const hvec<Adam16Seg>& segs, float beta1, float beta2, float eps,
+                  int incremental, int* flag, cudaStream_t stream) {
   // read G~, M~, v (12); write v (4) and D's fp16 split (4); incremental: write M~ (4)
   return launch_rows(segs, incremental ? 24.0 : 20.0, adam16_kernel, stream, beta1, beta2, eps,
-                     incremental);
+                     incremental, flag);
 }
 
-int launch_split16(const std::vector<Split16Seg>& segs, cudaStream_t stream) {
+int launch_split16(const hvec<Split16Seg>& segs, cudaStream_t stream) {
   return launch_rows(segs, 8.0, split16_kernel, stream);
 }
 
-int launch_to_f16(const std::vector<ToF16Seg>& segs, cudaStream_t stream) {
+int launch_to_f16(const hvec<ToF16Seg>& segs, cudaStream_t stream) {
   return launch_segs(segs, 12.0, to_f16_kernel, stream);
 }
 
-int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream) {
+int launch_transpose(const hvec<TransposeSeg>& segs, cudaStream_t stream) {
   for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
     SegBatch<TransposeSeg> b;
     std::memset(&b, 0, sizeof(b));
@@ -487,11 +509,11 @@ int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream)
   return ROT_OK;
 }
 
-int launch_fill(const std::vector<FillSeg>& segs, cudaStream_t stream) {
+int launch_fill(const hvec<FillSeg>& segs, cudaStream_t stream) {
   return launch_segs(segs, 8.0, fill_kernel, stream);
 }
 
-int launch_split(const std::vector<SplitSeg>& segs, cudaStream_t stream) {
+int launch_split(const hvec<SplitSeg>& segs, cudaStream_t stream) {
   return launch_segs(segs, 12.0, split_kernel, stream);
 }
 

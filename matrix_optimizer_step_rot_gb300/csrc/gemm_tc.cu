@@ -729,7 +729,7 @@ int num_sms() {
 }
 
 template <int BN, int STAGES, bool SPLIT3, bool PRECISE = false, bool F16 = false>
-int launch(const std::vector<GemmProblem>& probs, int* status, cudaStream_t stream) {
+int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
   using C = Cfg<BN, STAGES, SPLIT3>;
   static_assert(!PRECISE || (BN == 128 && SPLIT3 && !F16), "precise variant is 3xTF32, BN = 128");
   auto kernel =
@@ -818,7 +818,7 @@ int launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? ROT_OK : ROT_ECUDA;
 }
 
-int gemm_tc(const std::vector<GemmProblem>& probs, int precision, int* status,
+int gemm_tc(const hvec<GemmProblem>& probs, int precision, int* status,
             cudaStream_t stream) {
   if (precision == kPrecPrecise) return launch<128, 3, true, true>(probs, status, stream);
   if (precision == ROT_PREC_3XF16) {

@@ -22,13 +22,15 @@
 #include "plan.h"
 #include "rot.h"
 
+using rot::hvec;
+
 namespace {
 
 constexpr uint64_t kExactLimit = 1ull << 53;  // integers exact in a double
 
 // Checks the bucket sizes against `count`; fills the start index of each.
 bool bucket_starts(const int32_t* sizes, int32_t n_buckets, int32_t count,
-                   std::vector<int64_t>& start) {
+                   hvec<int64_t>& start) {
   start.resize((size_t)n_buckets);
   int64_t at = 0;
   for (int32_t b = 0; b < n_buckets; ++b) {
@@ -64,7 +66,7 @@ extern "C" int rot_partition_static(const uint64_t* elems, int32_t count,
                                     int32_t ranks, int32_t* owners) {
   if (bad_common(count, bucket_sizes, n_buckets, ranks, elems, owners)) return ROT_EINVAL;
   try {
-    std::vector<int64_t> start;
+    hvec<int64_t> start;
     if (!bucket_starts(bucket_sizes, n_buckets, count, start)) return ROT_EINVAL;
     for (int32_t b = 0; b < n_buckets; ++b) {
       const int64_t s0 = start[(size_t)b], s1 = s0 + bucket_sizes[b];
@@ -101,13 +103,13 @@ extern "C" int rot_partition_alpha_ex(const uint64_t* work, int32_t count,
     total += work[i];
   }
   try {
-    std::vector<int64_t> start;
+    hvec<int64_t> start;
     if (!bucket_starts(bucket_sizes, n_buckets, count, start)) return ROT_EINVAL;
-    std::vector<uint64_t> bwork((size_t)n_buckets, 0);
+    hvec<uint64_t> bwork((size_t)n_buckets, 0);
     for (int32_t b = 0; b < n_buckets; ++b)
       for (int64_t i = start[(size_t)b]; i < start[(size_t)b] + bucket_sizes[b]; ++i)
         bwork[(size_t)b] += work[i];
-    std::vector<int32_t> order((size_t)n_buckets);
+    hvec<int32_t> order((size_t)n_buckets);
     std::iota(order.begin(), order.end(), 0);
     std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
       return bwork[(size_t)a] != bwork[(size_t)b] ? bwork[(size_t)a] > bwork[(size_t)b] : a < b;
@@ -115,10 +117,10 @@ extern "C" int rot_partition_alpha_ex(const uint64_t* work, int32_t count,
 
     const size_t R = (size_t)ranks;
     const double Rd = (double)ranks;
-    std::vector<uint64_t> L(R, 0);
-    std::vector<double> deficit(R), share(R);
-    std::vector<uint64_t> prefix;
-    std::vector<int64_t> cut(R);
+    hvec<uint64_t> L(R, 0);
+    hvec<double> deficit(R), share(R);
+    hvec<uint64_t> prefix;
+    hvec<int64_t> cut(R);
     for (const int32_t b : order) {
       const uint64_t Wb = bwork[(size_t)b];
       const int64_t s0 = start[(size_t)b], nb = bucket_sizes[b];

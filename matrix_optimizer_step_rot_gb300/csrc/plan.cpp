@@ -35,7 +35,7 @@ struct MoreLoaded {
     return a.cost != b.cost ? a.cost > b.cost : a.rank > b.rank;
   }
 };
-using Heap = std::priority_queue<Load, std::vector<Load>, MoreLoaded>;
+using Heap = std::priority_queue<Load, hvec<Load>, MoreLoaded>;
 
 Heap fresh_heap(int32_t ranks) {
   Heap h;
@@ -47,20 +47,20 @@ Heap fresh_heap(int32_t ranks) {
 
 void build_groups(rot_plan* p) {
   const int32_t count = p->count;
-  std::vector<uint64_t> cost(count), bytes(count);
+  hvec<uint64_t> cost(count), bytes(count);
   for (int32_t i = 0; i < count; ++i) {
     cost[i] = item_cost(p->shapes[i].m, p->shapes[i].n);
     bytes[i] = item_bytes(p->shapes[i].m, p->shapes[i].n);
   }
-  std::vector<int32_t> order(count);
+  hvec<int32_t> order(count);
   std::iota(order.begin(), order.end(), 0);
   std::stable_sort(order.begin(), order.end(),
                    [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
 
   p->owners.assign(count, -1);
-  std::vector<int32_t> current;
+  hvec<int32_t> current;
   Heap heap = fresh_heap(p->ranks);
-  std::vector<uint64_t> held(p->ranks, 0);  // bytes per rank in the current group
+  hvec<uint64_t> held(p->ranks, 0);  // bytes per rank in the current group
   uint64_t held_max = 0;
 
   auto close_group = [&]() {
@@ -155,7 +155,7 @@ void build_layout(rot_plan* p) {
   uint64_t most = 256;
   for (size_t g = 0; g < p->groups.size(); ++g) {
     Cursor w;
-    std::vector<WorkLayout>& WL = p->work[g];
+    hvec<WorkLayout>& WL = p->work[g];
     WL.resize(p->groups[g].size());
     for (size_t k = 0; k < p->groups[g].size(); ++k) {
       const ItemLayout& L = p->items[p->groups[g][k]];

@@ -65,15 +65,15 @@ struct rot_plan {
   int32_t count = 0;
   int32_t ranks = 1;
   uint64_t c_max = 0;
-  std::vector<rot_shape> shapes;
-  std::vector<std::vector<int32_t>> groups;
-  std::vector<uint64_t> group_bytes, group_cost;
-  std::vector<int32_t> owners;
+  rot::hvec<rot_shape> shapes;
+  rot::hvec<rot::hvec<int32_t>> groups;
+  rot::hvec<uint64_t> group_bytes, group_cost;
+  rot::hvec<int32_t> owners;
   // layout
   uint64_t state_bytes = 0, work_bytes = 0;
   uint64_t ranks_off = 0;  // int32 pairs (rank_u, rank_v) per item
-  std::vector<rot::ItemLayout> items;
-  std::vector<std::vector<rot::WorkLayout>> work;  // [group][position in group]
+  rot::hvec<rot::ItemLayout> items;
+  rot::hvec<rot::hvec<rot::WorkLayout>> work;  // [group][position in group]
 };
 
 namespace rot {

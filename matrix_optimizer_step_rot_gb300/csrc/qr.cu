@@ -838,7 +838,7 @@ void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax) {
   q.part = reinterpret_cast<float*>(take(((uint64_t)p / kChunk + 1) * kRowTiles * kRows * B * 4));
 }
 
-int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status,
+int qr_batched(const hvec<QrProblem>& probs, float rank_rtol, int* status,
                cudaStream_t stream) {
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
@@ -903,7 +903,7 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
         }
       }
       // block factor T from the Gram of the block's reflectors
-      std::vector<GemmProblem> gram;
+      hvec<GemmProblem> gram;
       for (int i = 0; i < b.count; ++i) {
         const QrProblem& q = b.p[i];
         if (kb0 >= q.rmax) continue;
@@ -918,8 +918,8 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
         qr_tblock_kernel<<<n, kTThreads, 3 * TH * (TH + 1) * sizeof(float), stream>>>(b, kb0);
       }
       // trailing columns kb0+NB .. rmax-1: a <- a - Y (T^T (Y^T a))
-      std::vector<TransposeSeg> tr;
-      std::vector<GemmProblem> f1, f2, f3;
+      hvec<TransposeSeg> tr;
+      hvec<GemmProblem> f1, f2, f3;
       for (int i = 0; i < b.count; ++i) {
         const QrProblem& q = b.p[i];
         const int kend = kb0 + NB;
@@ -952,8 +952,8 @@ int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status
                       stream>>>(b);
     }
     for (int kb0 = ((rmax - 1) / NB) * NB; kb0 >= 0; kb0 -= NB) {
-      std::vector<TransposeSeg> tr;
-      std::vector<GemmProblem> q1, q2, q3;
+      hvec<TransposeSeg> tr;
+      hvec<GemmProblem> q1, q2, q3;
       for (int i = 0; i < b.count; ++i) {
         const QrProblem& q = b.p[i];
         if (kb0 >= q.rmax) continue;

@@ -22,10 +22,12 @@
 
 namespace rot {
 
-int gemm_tc(const std::vector<GemmProblem>& probs, int precision, int* status,
+std::atomic<int> g_nonfinite_check{0};
+
+int gemm_tc(const hvec<GemmProblem>& probs, int precision, int* status,
             cudaStream_t stream);
 
-int gemm_grouped(const std::vector<GemmProblem>& probs, int precision, int* status,
+int gemm_grouped(const hvec<GemmProblem>& probs, int precision, int* status,
                  cudaStream_t stream) {
   return gemm_tc(probs, precision, status, stream);
 }
@@ -93,7 +95,7 @@ GemmProblem gp16(int M, int N, int K, const unsigned short* ah, const unsigned s
 }
 
 // fp16 copies (scaled by 2^14) of U, U^T, V, V^T for the 3xF16 products.
-void push_f16_bases(std::vector<ToF16Seg>& segs, void* state, const ItemLayout& L) {
+void push_f16_bases(hvec<ToF16Seg>& segs, void* state, const ItemLayout& L) {
   segs.push_back({F(state, L.u_hi), F(state, L.u_lo), L.ldm, H(state, L.u16_hi),
                   H(state, L.u16_lo), L.ldm, L.m, L.m});
   segs.push_back({F(state, L.ut_hi), F(state, L.ut_lo), L.ldm, H(state, L.ut16_hi),
@@ -164,9 +166,10 @@ namespace {
 int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* G, void* state,
               void* work, float beta1, float beta2, float eps, float lr, int refresh,
               int precision, float rank_rtol, cudaStream_t s) {
-  const std::vector<int32_t>& items = p->groups[g];
-  const std::vector<WorkLayout>& WL = p->work[g];
+  const hvec<int32_t>& items = p->groups[g];
+  const hvec<WorkLayout>& WL = p->work[g];
   int* status = static_cast<int*>(state);
+  int* nonfinite = g_nonfinite_check.load(std::memory_order_relaxed) ? status : nullptr;
   const size_t n_items = items.size();
 
   const bool f16 = precision == ROT_PREC_3XF16;
@@ -177,7 +180,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     Range range("rot: momentum");
     if (cudaMemsetAsync(F(work, WL[0].g_rmax), 0, 12 * n_items, s) != cudaSuccess)
       return ROT_ECUDA;
-    std::vector<Momentum16Seg> segs(n_items);
+    hvec<Momentum16Seg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
       const ItemLayout& L = p->items[i];
@@ -188,10 +191,10 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
                  refresh ? H(work, x.m16_hi) : nullptr, H(work, x.m16_lo), F(work, x.m_rinv),
                  F(work, x.m_rmax)};
     }
-    ROT_TRY(launch_momentum16(segs, beta1, s));
+    ROT_TRY(launch_momentum16(segs, beta1, nonfinite, s));
   } else {
     Range range("rot: momentum");
-    std::vector<MomentumSeg> segs(n_items);
+    hvec<MomentumSeg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
       const ItemLayout& L = p->items[i];
@@ -199,13 +202,13 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       segs[k] = {G[i], F(state, L.m_hi), F(state, L.m_lo), F(work, WL[k].g_hi),
                  F(work, WL[k].g_lo), L.m, L.n, L.ldn};
     }
-    ROT_TRY(launch_momentum(segs, beta1, s));
+    ROT_TRY(launch_momentum(segs, beta1, nonfinite, s));
   }
 
   // (2) basis refresh
   if (refresh) {
     Range range("rot: basis refresh");
-    std::vector<TransposeSeg> tr(n_items);
+    hvec<TransposeSeg> tr(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
@@ -214,7 +217,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     }
     ROT_TRY(launch_transpose(tr, s));
 
-    std::vector<GemmProblem> first, second;
+    hvec<GemmProblem> first, second;
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
@@ -255,7 +258,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     ROT_TRY(gemm_grouped(first, kPrecPrecise, status, s));
     ROT_TRY(gemm_grouped(second, kPrecPrecise, status, s));
 
-    std::vector<QrProblem> qp;
+    hvec<QrProblem> qp;
     int32_t* ranks = reinterpret_cast<int32_t*>(static_cast<char*>(state) + p->ranks_off);
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
@@ -301,7 +304,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // S_M by a power of two below its bound, the largest row norm of G or M).
   {
     Range range("rot: rotation");
-    std::vector<GemmProblem> a, b;
+    hvec<GemmProblem> a, b;
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
@@ -344,24 +347,24 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // (3') Adam in rotated coordinates; D's split overwrites G's split
   if (f16) {
     Range range("rot: adam");
-    std::vector<Adam16Seg> segs(n_items);
+    hvec<Adam16Seg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       segs[k] = {F(work, x.gt), F(state, L.mt), F(state, L.v), H(work, x.g_hi), H(work, x.g_lo),
                  F(work, x.d_rinv), F(work, x.d_rmax), L.m, L.n, L.ldn};
     }
-    ROT_TRY(launch_adam16(segs, beta1, beta2, eps, refresh ? 0 : 1, s));
+    ROT_TRY(launch_adam16(segs, beta1, beta2, eps, refresh ? 0 : 1, nonfinite, s));
   } else {
     Range range("rot: adam");
-    std::vector<AdamSeg> segs(n_items);
+    hvec<AdamSeg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       segs[k] = {F(work, x.gt), F(state, L.mt), F(state, L.v), F(work, x.g_hi), F(work, x.g_lo),
                  L.m, L.n, L.ldn};
     }
-    ROT_TRY(launch_adam(segs, beta1, beta2, eps, refresh ? 0 : 1, s));
+    ROT_TRY(launch_adam(segs, beta1, beta2, eps, refresh ? 0 : 1, nonfinite, s));
   }
 
   // (4) back-rotation: (D V^T)^T into S_G's buffer; W -= lr U (D V^T).  In
@@ -369,7 +372,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // largest row norm of D.
   {
     Range range("rot: back-rotation and apply");
-    std::vector<GemmProblem> a, b;
+    hvec<GemmProblem> a, b;
     for (size_t k = 0; k < n_items; ++k) {
       const int i = items[k];
       const ItemLayout& L = p->items[i];
@@ -404,7 +407,9 @@ using namespace rot;
 
 extern "C" {
 
-int rot_state_init(const rot_plan* plan, void* state, void* stream) {
+namespace {
+
+int state_init(const rot_plan* plan, void* state, void* stream) {
   if (!plan || !state) return ROT_EINVAL;
   if ((reinterpret_cast<uintptr_t>(state) & 255) != 0) return ROT_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -412,7 +417,7 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream) {
   if (cudaMemsetAsync(static_cast<char*>(state) + plan->ranks_off, 0xff,
                       8ull * (uint64_t)(plan->count > 0 ? plan->count : 1), s) != cudaSuccess)
     return ROT_ECUDA;
-  std::vector<FillSeg> segs;
+  hvec<FillSeg> segs;
   for (int32_t i = 0; i < plan->count; ++i) {
     const ItemLayout& L = plan->items[i];
     segs.push_back({F(state, L.m_hi), F(state, L.m_lo), L.m, L.n, L.ldn, 0});
@@ -424,9 +429,19 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream) {
     segs.push_back({F(state, L.vt_hi), F(state, L.vt_lo), L.n, L.n, L.ldn, 1});
   }
   ROT_TRY(launch_fill(segs, s));
-  std::vector<ToF16Seg> conv;
+  hvec<ToF16Seg> conv;
   for (int32_t i = 0; i < plan->count; ++i) push_f16_bases(conv, state, plan->items[i]);
   return launch_to_f16(conv, s);
+}
+
+}  // namespace
+
+int rot_state_init(const rot_plan* plan, void* state, void* stream) {
+  try {
+    return state_init(plan, state, stream);
+  } catch (const std::bad_alloc&) {
+    return ROT_ENOMEM;
+  }
 }
 
 int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void* state,
@@ -447,6 +462,10 @@ int rot_step(const rot_plan* plan, float* const* W, const float* const* G, void*
     return ROT_ENOMEM;
   }
   return ROT_OK;
+}
+
+int32_t rot_set_nonfinite_check(int32_t on) {
+  return g_nonfinite_check.exchange(on != 0 ? 1 : 0);
 }
 
 int rot_status(const rot_plan* plan, void* state, int32_t* status, void* stream) {

@@ -5,11 +5,47 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <cstddef>
+#include <new>
 #include <vector>
 
 #include "rot.h"
 
 namespace rot {
+
+// ---------------------------------------------------------------------------
+// Host allocations.  The library's host containers (plan, partition, launch
+// descriptors) allocate through host_alloc, which throws std::bad_alloc on
+// failure; every entry point turns that into ROT_ENOMEM.  A test can make the
+// n-th later allocation fail (rot_test_fail_host_alloc).
+// ---------------------------------------------------------------------------
+
+void* host_alloc(std::size_t bytes);
+void host_free(void* p) noexcept;
+// after >= 0: the allocation after `after` more successful ones fails (once);
+// after < 0: no failure.
+void set_host_alloc_failure(int64_t after);
+
+template <class T>
+struct HostAlloc {
+  using value_type = T;
+  HostAlloc() noexcept = default;
+  template <class U>
+  HostAlloc(const HostAlloc<U>&) noexcept {}
+  T* allocate(std::size_t n) {
+    if (n > static_cast<std::size_t>(-1) / sizeof(T)) throw std::bad_alloc();
+    return static_cast<T*>(host_alloc(n * sizeof(T)));
+  }
+  void deallocate(T* p, std::size_t) noexcept { host_free(p); }
+};
+template <class T, class U>
+bool operator==(const HostAlloc<T>&, const HostAlloc<U>&) noexcept { return true; }
+template <class T, class U>
+bool operator!=(const HostAlloc<T>&, const HostAlloc<U>&) noexcept { return false; }
+
+template <class T>
+using hvec = std::vector<T, HostAlloc<T>>;
 
 // ---------------------------------------------------------------------------
 // Layout helpers
@@ -77,11 +113,15 @@ constexpr int kPrecPrecise = ROT_PREC_3XTF32_PRECISE;
 // Upper bound on every device-side wait, in nanoseconds.
 extern uint64_t g_wait_limit_ns;
 
+// Whether the element-wise kernels report non-finite gradients and updates
+// (rot_set_nonfinite_check).
+extern std::atomic<int> g_nonfinite_check;
+
 // Runs every problem of `probs` (any count; launched in chunks).  precision is
 // ROT_PREC_TF32, ROT_PREC_3XTF32, ROT_PREC_3XF16 (problems marked f16) or
 // kPrecPrecise.  status: device status word (may be
 // nullptr) set to ROT_ETIMEOUT if a bounded wait gives up.
-int gemm_grouped(const std::vector<GemmProblem>& probs, int precision, int* status,
+int gemm_grouped(const hvec<GemmProblem>& probs, int precision, int* status,
                  cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
@@ -96,7 +136,9 @@ struct MomentumSeg {
   float* g_lo;
   int rows, cols, ldm;
 };
-int launch_momentum(const std::vector<MomentumSeg>& segs, float beta1, cudaStream_t stream);
+// flag: the status word when the non-finite check is on (non-finite G or D
+// sets it to ROT_ENONFINITE), else null.
+int launch_momentum(const hvec<MomentumSeg>& segs, float beta1, int* flag, cudaStream_t stream);
 
 struct AdamSeg {
   const float* gt;  // G~ float32, ld
@@ -108,8 +150,8 @@ struct AdamSeg {
 };
 // incremental != 0: M~ <- beta1 M~ + (1 - beta1) G~ first (bases unchanged
 // since the last step); else M~ was just recomputed as U^T M V.
-int launch_adam(const std::vector<AdamSeg>& segs, float beta1, float beta2, float eps,
-                int incremental, cudaStream_t stream);
+int launch_adam(const hvec<AdamSeg>& segs, float beta1, float beta2, float eps,
+                int incremental, int* flag, cudaStream_t stream);
 
 // 3xF16 variants, one block per row.  Momentum as above, and G's scaled fp16
 // split: row r gets the power-of-two scale s_r with max|G_r| s_r < 2^14,
@@ -130,7 +172,8 @@ struct Momentum16Seg {
   float* m_rinv;
   float* m_rmax;
 };
-int launch_momentum16(const std::vector<Momentum16Seg>& segs, float beta1, cudaStream_t stream);
+int launch_momentum16(const hvec<Momentum16Seg>& segs, float beta1, int* flag,
+                      cudaStream_t stream);
 
 // Adam as above with D written as a scaled fp16 split (per-row scales into
 // d_rinv, largest row 2-norm into *d_rmax).
@@ -144,8 +187,8 @@ struct Adam16Seg {
   float* d_rmax;
   int rows, cols, ld;
 };
-int launch_adam16(const std::vector<Adam16Seg>& segs, float beta1, float beta2, float eps,
-                  int incremental, cudaStream_t stream);
+int launch_adam16(const hvec<Adam16Seg>& segs, float beta1, float beta2, float eps,
+                  int incremental, int* flag, cudaStream_t stream);
 
 // hi/lo (fp16, rows x cols, ld_dst) = fp16 split of 2^14 (s_hi + s_lo), for
 // the bases (|entries| <= 1).
@@ -158,7 +201,7 @@ struct ToF16Seg {
   int ld_dst;
   int rows, cols;
 };
-int launch_to_f16(const std::vector<ToF16Seg>& segs, cudaStream_t stream);
+int launch_to_f16(const hvec<ToF16Seg>& segs, cudaStream_t stream);
 
 // Scaled fp16 split of a float32 matrix (test entry point): per-row scales
 // (rinv != nullptr) or one scale from *bound; rmax (if set) grows to the
@@ -174,7 +217,7 @@ struct Split16Seg {
   float* rmax;
   const float* bound;
 };
-int launch_split16(const std::vector<Split16Seg>& segs, cudaStream_t stream);
+int launch_split16(const hvec<Split16Seg>& segs, cudaStream_t stream);
 
 // dst (cols x rows, ld_dst) = src^T, where src (rows x cols, ld_src) is a split;
 // dst is written as a split.  src_is_split = 0 reads float32 from src.hi.
@@ -190,7 +233,7 @@ struct TransposeSeg {
   int dst_is_split;
   int dst_mma_only = 0;  // the split output feeds only tensor cores
 };
-int launch_transpose(const std::vector<TransposeSeg>& segs, cudaStream_t stream);
+int launch_transpose(const hvec<TransposeSeg>& segs, cudaStream_t stream);
 
 // Fill a p x p split with the identity (lo = 0), or a rows x cols split with 0.
 struct FillSeg {
@@ -199,7 +242,7 @@ struct FillSeg {
   int rows, cols, ld;
   int identity;
 };
-int launch_fill(const std::vector<FillSeg>& segs, cudaStream_t stream);
+int launch_fill(const hvec<FillSeg>& segs, cudaStream_t stream);
 
 // hi/lo (rows x cols, ld_dst) = TF32 split of src (float32, ld_src).
 struct SplitSeg {
@@ -210,7 +253,7 @@ struct SplitSeg {
   int ld_dst;
   int rows, cols;
 };
-int launch_split(const std::vector<SplitSeg>& segs, cudaStream_t stream);
+int launch_split(const hvec<SplitSeg>& segs, cudaStream_t stream);
 
 // dst (rows x cols, ld_dst, float32) = hi + lo (or hi alone when lo == nullptr).
 int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,
@@ -250,7 +293,7 @@ struct QrProblem {
   unsigned short* ut16_hi;
   unsigned short* ut16_lo;
 };
-int qr_batched(const std::vector<QrProblem>& probs, float rank_rtol, int* status,
+int qr_batched(const hvec<QrProblem>& probs, float rank_rtol, int* status,
                cudaStream_t stream);
 
 // Bytes of QR scratch besides `at` and `qt` for one problem (256-aligned

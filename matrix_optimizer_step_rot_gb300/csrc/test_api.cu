@@ -22,10 +22,13 @@ uint64_t rot_test_gemm_work_bytes(int32_t M, int32_t N, int32_t K) {
   return 2 * split_bytes(M, ldk) + 2 * split_bytes(N, ldk) + 1024;
 }
 
-int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
-                  int32_t ldb, float* C, int32_t ldc, int32_t epi, float alpha,
-                  int32_t precision, void* work, uint64_t work_bytes, int32_t* status,
-                  void* stream) {
+}  // extern "C"
+
+namespace {
+
+int test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
+              int32_t ldb, float* C, int32_t ldc, int32_t epi, float alpha, int32_t precision,
+              void* work, uint64_t work_bytes, int32_t* status, void* stream) {
   if (M < 1 || N < 1 || K < 1 || !A || !B || !C || !work) return ROT_EINVAL;
   if (lda < K || ldb < K || epi < kEpiStoreSplit || epi > kEpiApplySplit) return ROT_EINVAL;
   if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
@@ -52,11 +55,11 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
     float* rinv = reinterpret_cast<float*>(w + 2 * ha + 2 * hb);
     float* bnorm = reinterpret_cast<float*>(w + 2 * ha + 2 * hb + align256(4ull * M));
     if (cudaMemsetAsync(bnorm, 0, 4, s) != cudaSuccess) return ROT_ECUDA;
-    std::vector<Split16Seg> pass1 = {{A, lda, a16h, a16l, ldk, M, K, rinv, nullptr, nullptr},
+    hvec<Split16Seg> pass1 = {{A, lda, a16h, a16l, ldk, M, K, rinv, nullptr, nullptr},
                                      {B, ldb, nullptr, nullptr, ldk, N, K, nullptr, bnorm, nullptr}};
     int e = launch_split16(pass1, s);
     if (e != ROT_OK) return e;
-    std::vector<Split16Seg> pass2 = {{B, ldb, b16h, b16l, ldk, N, K, nullptr, nullptr, bnorm}};
+    hvec<Split16Seg> pass2 = {{B, ldb, b16h, b16l, ldk, N, K, nullptr, nullptr, bnorm}};
     e = launch_split16(pass2, s);
     if (e != ROT_OK) return e;
     GemmProblem P;
@@ -87,7 +90,7 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
   float* a_lo = reinterpret_cast<float*>(w + split_bytes(M, ldk));
   float* b_hi = reinterpret_cast<float*>(w + 2 * split_bytes(M, ldk));
   float* b_lo = reinterpret_cast<float*>(w + 2 * split_bytes(M, ldk) + split_bytes(N, ldk));
-  std::vector<SplitSeg> segs = {{A, lda, a_hi, a_lo, ldk, M, K}, {B, ldb, b_hi, b_lo, ldk, N, K}};
+  hvec<SplitSeg> segs = {{A, lda, a_hi, a_lo, ldk, M, K}, {B, ldb, b_hi, b_lo, ldk, N, K}};
   int e = launch_split(segs, s);
   if (e != ROT_OK) return e;
   GemmProblem P;
@@ -109,6 +112,27 @@ int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, 
   P.epi = epi;
   P.alpha = alpha;
   return gemm_grouped({P}, precision, reinterpret_cast<int*>(status), s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
+                  int32_t ldb, float* C, int32_t ldc, int32_t epi, float alpha,
+                  int32_t precision, void* work, uint64_t work_bytes, int32_t* status,
+                  void* stream) {
+  try {
+    return test_gemm(M, N, K, A, lda, B, ldb, C, ldc, epi, alpha, precision, work, work_bytes,
+                     status, stream);
+  } catch (const std::bad_alloc&) {
+    return ROT_ENOMEM;
+  }
+}
+
+int rot_test_fail_host_alloc(int64_t after) {
+  set_host_alloc_failure(after < 0 ? -1 : after);
+  return ROT_OK;
 }
 
 int rot_test_wait_timeout(uint64_t limit_ns, int32_t* status, void* stream) {

@@ -137,3 +137,55 @@ def test_plan_bit_exact_at_scale():
     o = orc.plan(shapes, 64 << 20, ranks=4)
     assert len(o.groups) > 100
     assert p.groups() == o.groups and p.owners() == o.owners
+
+
+def _fail_each_allocation_in_turn(call, cleanup=None, limit=400):
+    """Make the k-th host allocation of `call` fail for k = 0, 1, ... until the
+    call gets through; every failing run must return ROT_ENOMEM (no exception
+    across the C ABI, no crash).  Returns how many allocations were failed."""
+    L = B.lib()
+    for k in range(limit):
+        L.rot_test_fail_host_alloc(k)
+        try:
+            rc, res = call()
+        finally:
+            L.rot_test_fail_host_alloc(-1)
+        if rc == B.ROT_OK:
+            if cleanup:
+                cleanup(res)
+            return k
+        assert rc == B.ROT_ENOMEM, (k, rc)
+    raise AssertionError("the call never succeeded")
+
+
+def test_plan_create_reports_host_allocation_failure():
+    wl = inputs.workload("block")
+    arr = (B.rot_shape * wl.count)(*[B.rot_shape(m, n) for m, n in wl.shapes])
+
+    def call():
+        out = ctypes.c_void_p()
+        rc = B.lib().rot_plan_create_ex(arr, wl.count, 64 << 20, 2, ctypes.byref(out))
+        if rc != B.ROT_OK:
+            assert not out.value  # *out is NULL on error
+        return rc, out
+
+    failed = _fail_each_allocation_in_turn(call, lambda out: B.lib().rot_plan_destroy(out))
+    assert failed >= 5  # shapes, groups, owners, layouts: each failed in turn
+
+
+def test_partitions_report_host_allocation_failure():
+    work = [int(x) for x in np.random.default_rng(5).integers(1, 1000, 30)]
+    sizes = [7, 8, 15]
+    w = (ctypes.c_uint64 * 30)(*work)
+    b = (ctypes.c_int32 * 3)(*sizes)
+    owners = (ctypes.c_int32 * 30)()
+    loads = (ctypes.c_uint64 * 4)()
+    for fn in ("rot_partition_alpha", "rot_partition_static"):
+        def call():
+            if fn == "rot_partition_alpha":
+                return B.lib().rot_partition_alpha(w, 30, b, 3, 4, 1.0, owners, loads), None
+            return B.lib().rot_partition_static(w, 30, b, 3, 4, owners), None
+        assert _fail_each_allocation_in_turn(call) >= 1, fn
+    # and the results are unaffected by the earlier failures
+    o = orc.alpha_partition(work, sizes, 4, 1.0)
+    assert B.partition_alpha(work, sizes, 4, 1.0) == (o.owners, o.loads)
