@@ -42,6 +42,8 @@ import os
 from typing import Callable, Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
+import scipy.linalg
+import scipy.linalg.lapack
 
 
 # ---------------------------------------------------------------------------
@@ -307,8 +309,60 @@ def hqr_plus_c(A: np.ndarray, rank_rtol: float) -> Tuple[np.ndarray, int, np.nda
     return np.ascontiguousarray(Q), int(r), beta[:r].copy()
 
 
+def hqr_plus_lapack(A: np.ndarray, rank_rtol: float,
+                    ncols: Optional[int] = None) -> Tuple[np.ndarray, int, np.ndarray]:
+    """hqr_plus() with LAPACK's Householder routines as its two library steps:
+    dgeqrf finds the reflectors of A's columns, dorgqr multiplies them out,
+    Q = H_0 H_1 ... H_{r-1} I.
+
+    The same definition as hqr_plus: LAPACK's reflector generator (dlarfg)
+    takes beta = -sgn(x_0) ||x|| as well, and |R_kk| = ||x|| at step k, so
+    the rank r is the first k with |R_kk| <= tau.  One case differs: when the
+    part of x below x_0 is exactly zero, dlarfg takes H_k = I (tau_k = 0,
+    R_kk = x_0) where hqr_plus reflects with w = 2 x_0 e_0 (beta_k = -x_0).
+    That reflector is put back here (tau_k = 2, v = e_k, beta_k = -R_kk), so
+    the completion columns match too.
+
+    ncols: only the first ncols columns are factored (the reflectors of the
+    first k columns do not depend on later ones, so the result is the same
+    whenever the stop comes by column ncols - 1, as it does when
+    ncols > rank(A)); default: all.  Returns (Q, r, beta[0:r]).
+    """
+    A = np.asarray(A, dtype=np.float64)
+    p, q = A.shape
+    assert p == q, "square input expected"
+    if p == 0:
+        return np.eye(0), 0, np.zeros(0)
+    tau_abs = rank_rtol * float(np.max(np.linalg.norm(A, axis=0)))
+    c = p if ncols is None else max(1, min(p, int(ncols)))
+    (qr, tau), R = scipy.linalg.qr(A[:, :c], mode="raw")
+    diag = np.diag(R)
+    r = c
+    for k in range(c):
+        if abs(float(diag[k])) <= tau_abs:
+            r = k
+            break
+    beta = np.array(diag[:r], dtype=np.float64)
+    t = np.array(tau[:r], dtype=np.float64)
+    flat = t == 0.0  # zero sub-column: restore the reflection hqr_plus makes
+    t[flat] = 2.0
+    beta[flat] = -beta[flat]
+    if r == 0:
+        return np.eye(p), 0, beta
+    a = np.zeros((p, p), dtype=np.float64, order="F")
+    a[:, :r] = qr[:, :r]
+    Q, _, info = scipy.linalg.lapack.dorgqr(a, t, lwork=max(1, 64 * p))
+    if info != 0:
+        raise RuntimeError(f"dorgqr failed ({info})")
+    Q = np.array(Q)
+    Q[:, :r][:, beta < 0.0] *= -1.0
+    return Q, r, beta
+
+
 def default_qr():
-    return hqr_plus_c if _c_lib() is not None else hqr_plus
+    """The QR+ the oracle's runs use: the LAPACK-step version (fast at the
+    12288-sized bases); hqr_plus and hqr_plus_c are its hand-written checks."""
+    return hqr_plus_lapack
 
 
 # ---------------------------------------------------------------------------
@@ -334,16 +388,24 @@ def refresh_basis(M: np.ndarray, U: np.ndarray, V: np.ndarray, rank_rtol: float,
                   qr: Optional[Callable] = None, perturb: Optional[Callable] = None):
     """One subspace-iteration step on each side: U <- QR+(M M^T U), V <- QR+(M^T M V).
 
-    `qr` picks the QR+ implementation (default: the C build if present);
-    `perturb`, used only to measure the method's sensitivity, maps each QR
-    input to a perturbed copy."""
+    `qr` picks the QR+ implementation (default: default_qr()); `perturb`, used
+    only to measure the method's sensitivity, maps (name, array) to a
+    perturbed copy of each stored quantity (see run())."""
     qr = qr or default_qr()
+    m, n = M.shape
     A_U = M @ (M.T @ U)
     A_V = M.T @ (M @ V)
     if perturb is not None:
-        A_U, A_V = perturb(A_U), perturb(A_V)
-    U_new, r_u, _ = qr(A_U, rank_rtol)
-    V_new, r_v, _ = qr(A_V, rank_rtol)
+        A_U, A_V = perturb("A_U", A_U), perturb("A_V", A_V)
+    if qr is hqr_plus_lapack:
+        # rank(A_U), rank(A_V) <= min(m, n): the stop comes by column min(m, n)
+        U_new, r_u, _ = qr(A_U, rank_rtol, ncols=min(m, n) + 1)
+        V_new, r_v, _ = qr(A_V, rank_rtol, ncols=min(m, n) + 1)
+    else:
+        U_new, r_u, _ = qr(A_U, rank_rtol)
+        V_new, r_v, _ = qr(A_V, rank_rtol)
+    if perturb is not None:
+        U_new, V_new = perturb("U", U_new), perturb("V", V_new)
     return U_new, V_new, r_u, r_v
 
 
@@ -356,16 +418,21 @@ def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: flo
     (2) if refresh: U, V <- subspace-iteration step + QR+
     (3) G~ = U^T G V, M~ = U^T M V, v <- beta2 v + (1 - beta2) G~^2, D = M~ / (sqrt(v) + eps)
     (4) W <- W - lr U D V^T
+
+    `perturb` (sensitivity runs only) maps (name, array) to a perturbed copy of
+    each quantity a float32 implementation stores: M, the QR inputs A_U and
+    A_V, the new U and V, G~, M~, v and D.
     """
+    p = perturb or (lambda name, X: X)
     G = np.asarray(G, dtype=np.float64)
-    st.M = beta1 * st.M + (1.0 - beta1) * G
+    st.M = p("M", beta1 * st.M + (1.0 - beta1) * G)
     if refresh:
         st.U, st.V, st.rank_u, st.rank_v = refresh_basis(st.M, st.U, st.V, rank_rtol,
                                                          perturb=perturb)
-    Gt = (st.U.T @ G) @ st.V
-    Mt = (st.U.T @ st.M) @ st.V
-    st.v = beta2 * st.v + (1.0 - beta2) * (Gt * Gt)
-    D = Mt / (np.sqrt(st.v) + eps)
+    Gt = p("Gt", (st.U.T @ G) @ st.V)
+    Mt = p("Mt", (st.U.T @ st.M) @ st.V)
+    st.v = p("v", beta2 * st.v + (1.0 - beta2) * (Gt * Gt))
+    D = p("D", Mt / (np.sqrt(st.v) + eps))
     return np.asarray(W, dtype=np.float64) - lr * ((st.U @ D) @ st.V.T)
 
 
@@ -373,18 +440,23 @@ def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: flo
 # A whole run of a workload (matrices are independent, so any subset can run)
 # ---------------------------------------------------------------------------
 
+FLOOR_REL = 2.0 ** -24  # float32 unit roundoff
+FLOOR_SEEDS = (1, 2, 3, 4, 5)
+
+
 def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         first_step: int = 1, perturb_seed: Optional[int] = None,
-        perturb_rel: float = 2.0 ** -22) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
+        perturb_rel: float = FLOOR_REL) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
     """Run `steps` steps (default: the workload's) for the chosen matrices.
 
     `wl` is a workload object exposing shapes, hyper, refresh(t), w0(i) and
     grad(i, t).  Returns {i: (W, state)} with W in float64.
 
-    With perturb_seed set, every QR input is multiplied element-wise by
-    (1 + perturb_rel * xi), xi ~ N(0, 1): the same method run on inputs that
-    differ at float32 rounding level.  How far that moves W is the method's
-    own sensitivity (its floor for any float32 implementation).
+    With perturb_seed set, every quantity a float32 implementation stores (see
+    step()) is multiplied element-wise by (1 + perturb_rel * xi), xi ~ N(0, 1),
+    each time it is formed: the same method on values that differ at float32
+    rounding level.  How far that moves the final W is the method's own
+    sensitivity, the floor any float32 implementation faces.
     """
     items = list(range(wl.count)) if items is None else list(items)
     steps = wl.steps if steps is None else steps
@@ -397,7 +469,8 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         perturb = None
         if perturb_seed is not None:
             rng = np.random.default_rng([perturb_seed, i])
-            perturb = lambda A, rng=rng: A * (1.0 + perturb_rel * rng.standard_normal(A.shape))
+            perturb = (lambda name, X, rng=rng:
+                       X * (1.0 + perturb_rel * rng.standard_normal(X.shape)))
         for t in range(first_step, first_step + steps):
             W = step(W, wl.grad(i, t), st, h.beta1, h.beta2, h.eps, h.lr, wl.refresh(t),
                      h.rank_rtol, perturb=perturb)
@@ -405,13 +478,15 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     return out
 
 
-def floor(wl, item: int, W_ref: np.ndarray, seeds: Sequence[int] = (1, 2, 3),
-          steps: Optional[int] = None) -> float:
-    """Largest relative change of the final W over runs whose QR inputs are
-    perturbed at float32 level (see run())."""
+def floor(wl, item: int, W_ref: np.ndarray, seeds: Sequence[int] = FLOOR_SEEDS,
+          steps: Optional[int] = None, rel: float = FLOOR_REL) -> float:
+    """The method's float32 floor for one matrix: the largest relative change
+    of the final W over runs (one per seed) whose stored quantities are
+    perturbed at relative size `rel` (float32 unit roundoff by default; see
+    run())."""
     worst = 0.0
     for s in seeds:
-        Wp, _ = run(wl, [item], steps=steps, perturb_seed=s)[item]
+        Wp, _ = run(wl, [item], steps=steps, perturb_seed=s, perturb_rel=rel)[item]
         worst = max(worst, float(np.linalg.norm(Wp - W_ref) / np.linalg.norm(W_ref)))
     return worst
 

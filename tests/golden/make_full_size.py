@@ -1,0 +1,122 @@
+"""Writes tests/golden/full_size/<workload>.npz: the float64 oracle's results
+for sampled matrices of the full-size workloads, for the GPU parity tests
+(tests/test_configs_gpu.py).  Calls only the oracle (oracle/rot_oracle.py)
+and the seeded input generator; nothing here comes from the CUDA path.
+
+For each sampled matrix i of a workload, after the workload's steps:
+  idx      S flat indices into W (m x n, row-major), drawn once from a
+           seeded generator and stored (so the test does not depend on the
+           generator's stream)
+  w        the oracle's final W at those indices (float64)
+  norm     ||W||_F of the oracle's whole final W
+  wsamp    ||W[idx]||  (the sample's own norm, for the relative error)
+  floor    the method's float32 floor: the largest relative change of the
+           final W over five runs whose stored quantities are perturbed at
+           2^-24 (oracle.floor)
+  rank_u, rank_v   the numerical ranks at the last refresh
+
+The matrices are independent, so each sampled one is run on its own.  The
+samples cover every distinct shape of each Qwen3-shaped workload (one
+matrix per shape, spread over the layers) and one matrix per distinct
+(m, n) of the ragged workload.
+
+    python tests/golden/make_full_size.py [workload ...]   # default: all four
+"""
+
+import argparse
+import os
+import sys
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(os.path.dirname(HERE))
+sys.path.insert(0, ROOT)
+
+from matrix_optimizer_step_rot_gb300 import inputs  # noqa: E402
+from oracle import rot_oracle as orc  # noqa: E402
+
+OUT = os.path.join(HERE, "full_size")
+
+# (workload, sampled items, samples per matrix)
+PLAN = {
+    # every matrix of the block
+    "block": (list(range(7)), 8192),
+    # one per shape kind, spread over the 28 layers: L0.k, L13.v, L27.q,
+    # L5.o, L20.gate, L9.up, L14.down
+    "full": ([1, 7 * 13 + 2, 7 * 27 + 0, 7 * 5 + 3, 7 * 20 + 4, 7 * 9 + 5, 7 * 14 + 6], 8192),
+    # L0.k, L1.v, L3.q, L2.o, L0.gate, L1.up, L3.down
+    "slice8b": ([1, 7 + 2, 21 + 0, 14 + 3, 4, 7 + 5, 21 + 6], 8192),
+    # filled in by ragged_items(): first matrix of each distinct (m, n)
+    "ragged": (None, 1024),
+}
+
+
+def ragged_items(wl):
+    seen, items = set(), []
+    for i, shp in enumerate(wl.shapes):
+        if shp not in seen:
+            seen.add(shp)
+            items.append(i)
+    return items
+
+
+class CachedInputs:
+    """The workload with its gradients memoised, so the six runs of a matrix
+    (reference + five floor seeds) draw them once."""
+
+    def __init__(self, wl):
+        self._wl = wl
+        self._g = {}
+
+    def __getattr__(self, name):
+        return getattr(self._wl, name)
+
+    def grad(self, i, t):
+        if (i, t) not in self._g:
+            self._g[(i, t)] = self._wl.grad(i, t)
+        return self._g[(i, t)]
+
+    def forget(self):
+        self._g.clear()
+
+
+def one(wl, i, samples):
+    m, n = wl.shapes[i]
+    W, st = orc.run(wl, [i])[i]
+    fl = orc.floor(wl, i, W)
+    rng = np.random.default_rng([20260, wl.seed, i])
+    s = min(samples, m * n)
+    idx = np.sort(rng.choice(m * n, size=s, replace=False)).astype(np.uint32)
+    w = W.ravel()[idx]
+    return dict(idx=idx, w=w, norm=float(np.linalg.norm(W)), wsamp=float(np.linalg.norm(w)),
+                floor=fl, rank_u=int(st.rank_u), rank_v=int(st.rank_v))
+
+
+def make(name):
+    wl0 = inputs.workload(name)
+    items, samples = PLAN[name]
+    if items is None:
+        items = ragged_items(wl0)
+    wl = CachedInputs(wl0)
+    rec = {"items": np.array(items, dtype=np.int32), "steps": wl0.steps,
+           "refresh_every": wl0.refresh_every, "seed": wl0.seed}
+    t0 = time.time()
+    for k, i in enumerate(items):
+        r = one(wl, i, samples)
+        wl.forget()
+        for key, val in r.items():
+            rec[f"{i}.{key}"] = val
+        print(f"{name}[{i}] {wl0.shapes[i]}: floor {r['floor']:.2e} ranks "
+              f"({r['rank_u']}, {r['rank_v']})  [{k + 1}/{len(items)}, "
+              f"{time.time() - t0:.0f} s]", flush=True)
+    os.makedirs(OUT, exist_ok=True)
+    np.savez_compressed(os.path.join(OUT, f"{name}.npz"), **rec)
+
+
+if __name__ == "__main__":
+    ap = argparse.ArgumentParser()
+    ap.add_argument("names", nargs="*", default=["ragged", "block", "full", "slice8b"])
+    for nm in ap.parse_args().names:
+        make(nm)

@@ -11,7 +11,7 @@ from oracle import rot_oracle as orc
 from matrix_optimizer_step_rot_gb300 import inputs
 
 build_oracle.build()
-QR_IMPLS = [orc.hqr_plus, orc.hqr_plus_c]
+QR_IMPLS = [orc.hqr_plus, orc.hqr_plus_c, orc.hqr_plus_lapack]
 
 H = inputs.Hyper()
 B1, B2, EPS, LR = H.beta1, H.beta2, H.eps, H.lr
@@ -171,6 +171,38 @@ def test_c_qr_matches_numpy_definition_on_refresh_inputs():
             assert rn == rc
             np.testing.assert_allclose(Qc, Qn, rtol=0, atol=1e-11)
             np.testing.assert_allclose(bc, bn, rtol=1e-12, atol=0)
+
+
+def test_lapack_qr_matches_hand_written_householder_on_refresh_inputs():
+    """The oracle's runs take QR+ through LAPACK's Householder routines; the
+    plain Householder loop (hqr_plus) checks it, completion columns included,
+    on Gram-type inputs with a rank stop inside, with and without the column
+    limit the refresh passes."""
+    for m, n, seed in [(70, 40, 1), (40, 70, 2), (96, 96, 3), (130, 9, 4)]:
+        M = rng(seed).normal(size=(m, n))
+        for A in (M @ M.T, M.T @ M):
+            Qn, rn, bn = orc.hqr_plus(A, 1e-3)
+            for ncols in (None, min(m, n) + 1):
+                Ql, rl, bl = orc.hqr_plus_lapack(A, 1e-3, ncols=ncols)
+                assert rl == rn
+                np.testing.assert_allclose(Ql, Qn, rtol=0, atol=1e-11)
+                np.testing.assert_allclose(bl, bn, rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("qr", QR_IMPLS)
+def test_hqr_zero_subcolumns_hand_worked(qr):
+    """A = diag(3, -2, 0, 0): each factored column has nothing below its
+    diagonal, so x = x_0 e_0.  By the definition beta = -sgn(x_0)|x_0| and
+    w = 2 x_0 e_0, H_k = I - 2 e_k e_k^T: H_0 = diag(-1, 1, 1, 1) (beta_0 = -3),
+    H_1 = diag(1, -1, 1, 1) (beta_1 = 2), then the stop (r = 2).  Q = H_0 H_1 I
+    = diag(-1, -1, 1, 1); the sign fix negates column 0: diag(1, -1, 1, 1).
+    (LAPACK's generator takes H = I here; the LAPACK-step version restores the
+    reflection.)"""
+    A = np.diag([3.0, -2.0, 0.0, 0.0])
+    Q, r, beta = qr(A, 1e-3)
+    assert r == 2
+    np.testing.assert_array_equal(beta, [-3.0, 2.0])
+    np.testing.assert_array_equal(Q, np.diag([1.0, -1.0, 1.0, 1.0]))
 
 
 # --------------------------------------------------------------------------
@@ -347,3 +379,47 @@ def test_ragged_shapes():
     wl = inputs.workload("ragged")
     dims = {d for s in wl.shapes for d in s}
     assert wl.count == 256 and dims <= set(range(64, 1025, 64)) and len(dims) == 16
+
+
+# --------------------------------------------------------------------------
+# P9: the float32 floor (oracle against itself, perturbed)
+# --------------------------------------------------------------------------
+
+def _small_workload(steps, K, shapes=((24, 16), (16, 24))):
+    return inputs.Workload("floorpin", shapes, ("a", "b"), 0.02, 1e-2, "normal", steps, K,
+                           1 << 20, 11)
+
+
+def test_floor_is_zero_without_perturbation():
+    wl = _small_workload(4, 2)
+    W, _ = orc.run(wl, [0])[0]
+    assert orc.floor(wl, 0, W, rel=0.0) == 0.0
+
+
+def test_floor_is_first_order_in_the_perturbation_where_the_step_is_smooth():
+    """No refresh (Adam's D is smooth in its inputs away from G~ = 0, and the
+    identity bases rotate nothing): the change of W is linear in the
+    perturbation size, so 16 times the size gives 16 times the floor (to
+    first order).  Its size: W_T = W_0 - lr sum_t D_t, and each D_t moves by
+    about 1.5 u relative (D itself, M~, and half of v's perturbation;
+    u = 2^-24), so |dW| ~ lr |D| 1.5 u sqrt(T), with |D| ~ 4.5 over the first
+    five steps of Adam without bias correction: relative to |W| = 0.02, about
+    0.75 u."""
+    wl = _small_workload(5, 100)  # K > steps: plain Adam, U = V = I
+    W, _ = orc.run(wl, [1])[1]
+    u = 2.0 ** -24
+    f24 = orc.floor(wl, 1, W, rel=u)
+    f20 = orc.floor(wl, 1, W, rel=16 * u)
+    assert 0.25 * u < f24 < 4.0 * u
+    assert 14.0 < f20 / f24 < 18.0
+
+
+def test_floor_large_when_the_first_step_refreshes():
+    """Refresh on step 1 (K = 1): v = 0 before the step, so D = M~ / (|G~|
+    sqrt(1 - beta2) + eps) ~ 3.16 sgn(G~) is discontinuous in G~ and the rotated
+    G~ has entries near zero; rounding-level changes flip some signs and move
+    W by far more than the perturbation (the survey's measured 5e-4 .. 2e-3 at
+    larger sizes)."""
+    wl = _small_workload(3, 1)
+    W, _ = orc.run(wl, [0])[0]
+    assert orc.floor(wl, 0, W) > 1e3 * 2.0 ** -24
