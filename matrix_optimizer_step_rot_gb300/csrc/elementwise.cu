@@ -63,7 +63,8 @@ __device__ __forceinline__ void report_nonfinite(int* flag, bool seen) {
   if (flag && seen) atomicCAS(flag, 0, ROT_ENONFINITE);
 }
 
-// M <- beta1 M + (1 - beta1) G, with M held as a split; also writes G's split.
+// M <- beta1 M + (1 - beta1) G (float32); also writes G's split and, on
+// refresh steps, M's exact TF32 split.
 __global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b, float beta1,
                                 int* flag) {
   const MomentumSeg& s = b.seg[blockIdx.y];
@@ -77,11 +78,14 @@ __global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b,
     const int64_t o = (int64_t)r * s.ldm + c;
     const float g = s.g[e];
     bad |= check && !isfinite(g);
-    const float m = beta1 * (s.m_hi[o] + s.m_lo[o]) + one_minus * g;
+    const float m = beta1 * s.m[o] + one_minus * g;
+    s.m[o] = m;
     float h, l;
-    split_tf32(m, h, l);
-    s.m_hi[o] = h;
-    s.m_lo[o] = l;
+    if (s.m_hi) {
+      split_tf32(m, h, l);
+      s.m_hi[o] = h;
+      s.m_lo[o] = l;
+    }
     split_tf32_mma(g, h, l);
     s.g_hi[o] = h;
     s.g_lo[o] = l;
@@ -162,10 +166,9 @@ __device__ __forceinline__ void atomic_max_nonneg(float* slot, float x) {
 // pass: M's update and the row's max |g| and sum g^2; second pass (G re-read,
 // from L2): the scaled fp16 split of G.  Four columns per thread and access
 // (16-byte loads) where the row allows, single columns for the rest.
-__device__ __forceinline__ void momentum_elem(float x, float& hi, float& lo, float beta1,
-                                              float one_minus, float& sum, float& mx) {
-  const float m = beta1 * (hi + lo) + one_minus * x;
-  split_tf32(m, hi, lo);
+__device__ __forceinline__ void momentum_elem(float x, float& m, float beta1, float one_minus,
+                                              float& sum, float& mx) {
+  m = beta1 * m + one_minus * x;
   sum = fmaf(x, x, sum);
   mx = fmaxf(mx, fabsf(x));
 }
@@ -178,24 +181,21 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
                      ? s.cols / 4 : 0;
   for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
     const float* g = s.g + (int64_t)r * s.cols;
-    float* mh = s.m_hi + (int64_t)r * s.ldm;
-    float* ml = s.m_lo + (int64_t)r * s.ldm;
+    float* mr = s.m + (int64_t)r * s.ldm;
     unsigned short* gh = s.g_hi + (int64_t)r * s.ldm;
     unsigned short* gl = s.g_lo + (int64_t)r * s.ldm;
     float sum = 0.f, mx = 0.f;
     for (int q = threadIdx.x; q < nv; q += blockDim.x) {
       const float4 x = reinterpret_cast<const float4*>(g)[q];
-      float4 h = reinterpret_cast<float4*>(mh)[q];
-      float4 l = reinterpret_cast<float4*>(ml)[q];
-      momentum_elem(x.x, h.x, l.x, beta1, one_minus, sum, mx);
-      momentum_elem(x.y, h.y, l.y, beta1, one_minus, sum, mx);
-      momentum_elem(x.z, h.z, l.z, beta1, one_minus, sum, mx);
-      momentum_elem(x.w, h.w, l.w, beta1, one_minus, sum, mx);
-      reinterpret_cast<float4*>(mh)[q] = h;
-      reinterpret_cast<float4*>(ml)[q] = l;
+      float4 mm = reinterpret_cast<float4*>(mr)[q];
+      momentum_elem(x.x, mm.x, beta1, one_minus, sum, mx);
+      momentum_elem(x.y, mm.y, beta1, one_minus, sum, mx);
+      momentum_elem(x.z, mm.z, beta1, one_minus, sum, mx);
+      momentum_elem(x.w, mm.w, beta1, one_minus, sum, mx);
+      reinterpret_cast<float4*>(mr)[q] = mm;
     }
     for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x)
-      momentum_elem(g[c], mh[c], ml[c], beta1, one_minus, sum, mx);
+      momentum_elem(g[c], mr[c], beta1, one_minus, sum, mx);
     block_sum_max(sum, mx);
     const float scale = pow2_below(mx, kF16ScaleExp);
     if (threadIdx.x == 0) {
@@ -205,10 +205,10 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
       report_nonfinite(flag, !isfinite(sum) && !(sum > 3.402823466e38f && isfinite(mx)));
     }
     if (s.m16_hi) {
-      // M's new row (this thread's own writes above), its scale and split
+      // M's new row (this thread's own writes above), its scale and splits
       float msum = 0.f, mmx = 0.f;
       for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-        const float m = mh[c] + ml[c];
+        const float m = mr[c];
         msum = fmaf(m, m, msum);
         mmx = fmaxf(mmx, fabsf(m));
       }
@@ -220,8 +220,13 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
       }
       unsigned short* m16h = s.m16_hi + (int64_t)r * s.ldm;
       unsigned short* m16l = s.m16_lo + (int64_t)r * s.ldm;
-      for (int c = threadIdx.x; c < s.cols; c += blockDim.x)
-        split_f16((mh[c] + ml[c]) * mscale, m16h[c], m16l[c]);
+      float* mth = s.m_hi + (int64_t)r * s.ldm;
+      float* mtl = s.m_lo + (int64_t)r * s.ldm;
+      for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+        const float m = mr[c];
+        split_f16(m * mscale, m16h[c], m16l[c]);
+        split_tf32(m, mth[c], mtl[c]);
+      }
     }
     for (int q = threadIdx.x; q < nv; q += blockDim.x) {
       const float4 x = reinterpret_cast<const float4*>(g)[q];
@@ -332,6 +337,65 @@ __global__ void split16_kernel(const __grid_constant__ SegBatch<Split16Seg> b) {
   }
 }
 
+// TF32 split (lo rounded to TF32: tensor-core operands only) of a basis held
+// as a 2^14-scaled fp16 split, optionally transposed (32 x 32 tiles through
+// shared memory).
+template <bool TRANSPOSE>
+__global__ void to_tf32_kernel(const __grid_constant__ SegBatch<ToTf32Seg> b) {
+  __shared__ float tile[32][33];
+  const ToTf32Seg& s = b.seg[blockIdx.y];
+  const int tiles_r = (s.rows + 31) / 32, tiles_c = (s.cols + 31) / 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+    for (int i = ty; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + tx;
+      float x = 0.f;
+      if (r < s.rows && c < s.cols) {
+        const int64_t o = (int64_t)r * s.ld_src + c;
+        x = (__half2float(__ushort_as_half(s.s_hi[o])) +
+             __half2float(__ushort_as_half(s.s_lo[o]))) * kF16UnitScaleInv;
+      }
+      if (TRANSPOSE) {
+        tile[i][tx] = x;
+      } else if (r < s.rows && c < s.cols) {
+        float h, l;
+        split_tf32_mma(x, h, l);
+        const int64_t o = (int64_t)r * s.ld_dst + c;
+        s.d_hi[o] = h;
+        s.d_lo[o] = l;
+      }
+    }
+    if (TRANSPOSE) {
+      __syncthreads();
+      for (int i = ty; i < 32; i += 8) {
+        const int c = c0 + i, r = r0 + tx;  // output row c, column r
+        if (r < s.rows && c < s.cols) {
+          float h, l;
+          split_tf32_mma(tile[tx][i], h, l);
+          const int64_t o = (int64_t)c * s.ld_dst + r;
+          s.d_hi[o] = h;
+          s.d_lo[o] = l;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void combine16_kernel(const unsigned short* hi, const unsigned short* lo, int ld_src,
+                                 float* dst, int ld_dst, int rows, int cols) {
+  const int64_t total = (int64_t)rows * cols;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / cols), c = (int)(e - (int64_t)r * cols);
+    const int64_t o = (int64_t)r * ld_src + c;
+    dst[(int64_t)r * ld_dst + c] =
+        (__half2float(__ushort_as_half(hi[o])) + __half2float(__ushort_as_half(lo[o]))) *
+        kF16UnitScaleInv;
+  }
+}
+
 __global__ void to_f16_kernel(const __grid_constant__ SegBatch<ToF16Seg> b) {
   const ToF16Seg& s = b.seg[blockIdx.y];
   const int64_t total = (int64_t)s.rows * s.cols;
@@ -396,8 +460,14 @@ __global__ void fill_kernel(const __grid_constant__ SegBatch<FillSeg> b) {
        e += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
     const int64_t o = (int64_t)r * s.ld + c;
-    s.hi[o] = (s.identity && r == c) ? 1.0f : 0.0f;
-    if (s.lo) s.lo[o] = 0.0f;
+    if (s.f16) {  // fp16 split scaled by 2^14: the identity's 1 is 2^14, lo 0
+      reinterpret_cast<unsigned short*>(s.hi)[o] =
+          __half_as_ushort(__float2half_rn((s.identity && r == c) ? kF16UnitScale : 0.0f));
+      if (s.lo) reinterpret_cast<unsigned short*>(s.lo)[o] = __half_as_ushort(__float2half_rn(0.f));
+    } else {
+      s.hi[o] = (s.identity && r == c) ? 1.0f : 0.0f;
+      if (s.lo) s.lo[o] = 0.0f;
+    }
   }
 }
 
@@ -430,8 +500,10 @@ __global__ void combine_kernel(const float* hi, const float* lo, int ld_src, flo
 
 int launch_momentum(const hvec<MomentumSeg>& segs, float beta1, int* flag,
                     cudaStream_t stream) {
-  // read G (4) and M's split (8); write M's split (8) and G's split (8)
-  return launch_segs(segs, 28.0, momentum_kernel, stream, beta1, flag);
+  // read G (4) and M (4); write M (4) and G's split (8) (refresh steps: and
+  // M's split, 8)
+  const bool split_m = !segs.empty() && segs[0].m_hi;
+  return launch_segs(segs, split_m ? 28.0 : 20.0, momentum_kernel, stream, beta1, flag);
 }
 
 int launch_adam(const hvec<AdamSeg>& segs, float beta1, float beta2, float eps,
@@ -467,8 +539,58 @@ int launch_rows(const hvec<Seg>& segs, double bytes_per_elem, Kernel kernel,
 
 int launch_momentum16(const hvec<Momentum16Seg>& segs, float beta1, int* flag,
                       cudaStream_t stream) {
-  // read G (4) and M's split (8); write M's split (8) and G's fp16 split (4)
-  return launch_rows(segs, 24.0, momentum16_kernel, stream, beta1, flag);
+  // read G (4) and M (4); write M (4) and G's fp16 split (4) (refresh steps:
+  // and M's fp16 split, 4, and TF32 split, 8)
+  const bool split_m = !segs.empty() && segs[0].m16_hi;
+  return launch_rows(segs, split_m ? 28.0 : 16.0, momentum16_kernel, stream, beta1, flag);
+}
+
+namespace {
+
+int to_tf32_segs(const hvec<ToTf32Seg>& segs, bool transpose, cudaStream_t stream) {
+  // read the fp16 split (4), write the TF32 split (8)
+  for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
+    SegBatch<ToTf32Seg> b;
+    std::memset(&b, 0, sizeof(b));
+    b.count = (int)std::min<size_t>(kMaxSegs, segs.size() - base);
+    int64_t most = 0;
+    double elems = 0.0;
+    for (int i = 0; i < b.count; ++i) {
+      b.seg[i] = segs[base + i];
+      most = std::max<int64_t>(most, (int64_t)((b.seg[i].rows + 31) / 32) * ((b.seg[i].cols + 31) / 32));
+      elems += (double)b.seg[i].rows * b.seg[i].cols;
+    }
+    if (most == 0) continue;
+    dim3 grid((unsigned)std::min<int64_t>(most, 4096), b.count);
+    ProfScope prof(ROT_PROF_ELEMENTWISE, elems * 12.0, stream);
+    if (transpose) {
+      to_tf32_kernel<true><<<grid, kThreads, 0, stream>>>(b);
+    } else {
+      to_tf32_kernel<false><<<grid, kThreads, 0, stream>>>(b);
+    }
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+  }
+  return ROT_OK;
+}
+
+}  // namespace
+
+int launch_to_tf32(const hvec<ToTf32Seg>& segs, cudaStream_t stream) {
+  return to_tf32_segs(segs, false, stream);
+}
+
+int launch_to_tf32_t(const hvec<ToTf32Seg>& segs, cudaStream_t stream) {
+  return to_tf32_segs(segs, true, stream);
+}
+
+int launch_combine16(const unsigned short* hi, const unsigned short* lo, int ld_src, float* dst,
+                     int ld_dst, int rows, int cols, cudaStream_t stream) {
+  const int64_t total = (int64_t)rows * cols;
+  if (total == 0) return ROT_OK;
+  ProfScope prof(ROT_PROF_ELEMENTWISE, (double)total * 8, stream);
+  combine16_kernel<<<grid_x_for(total), kThreads, 0, stream>>>(hi, lo, ld_src, dst, ld_dst,
+                                                               rows, cols);
+  return cudaGetLastError() == cudaSuccess ? ROT_OK : ROT_ECUDA;
 }
 
 int launch_adam16(const hvec<Adam16Seg>& segs, float beta1, float beta2, float eps,

@@ -125,18 +125,9 @@ void build_layout(rot_plan* p) {
     L.n = (int)n;
     L.ldm = (int)pad_ld(m);
     L.ldn = (int)pad_ld(n);
-    L.m_hi = s.floats(m, L.ldn);
-    L.m_lo = s.floats(m, L.ldn);
+    L.mom = s.floats(m, L.ldn);
     L.v = s.floats(m, L.ldn);
     L.mt = s.floats(m, L.ldn);
-    L.u_hi = s.floats(m, L.ldm);
-    L.u_lo = s.floats(m, L.ldm);
-    L.ut_hi = s.floats(m, L.ldm);
-    L.ut_lo = s.floats(m, L.ldm);
-    L.vb_hi = s.floats(n, L.ldn);
-    L.vb_lo = s.floats(n, L.ldn);
-    L.vt_hi = s.floats(n, L.ldn);
-    L.vt_lo = s.floats(n, L.ldn);
     L.u16_hi = s.halves(m, L.ldm);
     L.u16_lo = s.halves(m, L.ldm);
     L.ut16_hi = s.halves(m, L.ldm);
@@ -148,9 +139,10 @@ void build_layout(rot_plan* p) {
   }
   p->state_bytes = s.at;
 
-  // Workspace: per group, a rotation region followed by a refresh region.
-  // The gradient split written by the momentum kernel stays live across the
-  // refresh, so the two regions do not overlap.
+  // Workspace: per group, a rotation region, the TF32 splits of the bases
+  // and of M, then a refresh region.  The gradient split written by the
+  // momentum kernel stays live across the refresh, so the regions do not
+  // overlap.
   p->work.resize(p->groups.size());
   uint64_t most = 256;
   for (size_t g = 0; g < p->groups.size(); ++g) {
@@ -181,6 +173,20 @@ void build_layout(rot_plan* p) {
         WL[k].d_rmax = norms + 12 * k + 4;
         WL[k].m_rmax = norms + 12 * k + 8;
       }
+    }
+    for (size_t k = 0; k < p->groups[g].size(); ++k) {
+      const ItemLayout& L = p->items[p->groups[g][k]];
+      WorkLayout& x = WL[k];
+      x.u_hi = w.floats(L.m, L.ldm);
+      x.u_lo = w.floats(L.m, L.ldm);
+      x.ut_hi = w.floats(L.m, L.ldm);
+      x.ut_lo = w.floats(L.m, L.ldm);
+      x.vb_hi = w.floats(L.n, L.ldn);
+      x.vb_lo = w.floats(L.n, L.ldn);
+      x.vt_hi = w.floats(L.n, L.ldn);
+      x.vt_lo = w.floats(L.n, L.ldn);
+      x.m_hi = w.floats(L.m, L.ldn);
+      x.m_lo = w.floats(L.m, L.ldn);
     }
     for (size_t k = 0; k < p->groups[g].size(); ++k) {
       const ItemLayout& L = p->items[p->groups[g][k]];

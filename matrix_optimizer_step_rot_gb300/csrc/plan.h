@@ -11,16 +11,18 @@
 
 namespace rot {
 
-// Offsets (bytes from the state blob's base) of one matrix's state.
+// Offsets (bytes from the state blob's base) of one matrix's state.  Each
+// quantity is kept once: M, v and M~ in float32; each basis in the two
+// orientations the 3xF16 products read, as scaled fp16 splits
+// (hi + lo = 2^14 x, 22 significant bits, the same as the TF32 splits the
+// tensor cores read).  TF32 splits are made from them in the workspace where
+// a product needs them.
 struct ItemLayout {
   int m, n, ldm, ldn;                 // ldm = pad(m), ldn = pad(n)
-  uint64_t m_hi, m_lo;                // momentum split, m x ldn
+  uint64_t mom;                       // momentum M (float32), m x ldn
   uint64_t v;                         // second moment, m x ldn
   uint64_t mt;                        // M~ = U^T M V (float32), m x ldn
-  uint64_t u_hi, u_lo, ut_hi, ut_lo;  // U and U^T splits, m x ldm
-  uint64_t vb_hi, vb_lo, vt_hi, vt_lo;  // V and V^T splits, n x ldn
-  // fp16 splits of U, U^T (m x ldm) and V, V^T (n x ldn), scaled by 2^14, for
-  // the 3xF16 rotation products; rewritten whenever the bases change
+  // fp16 splits of U, U^T (m x ldm) and V, V^T (n x ldn), scaled by 2^14
   uint64_t u16_hi, u16_lo, ut16_hi, ut16_lo;
   uint64_t vb16_hi, vb16_lo, vt16_hi, vt16_lo;
 };
@@ -43,6 +45,12 @@ struct WorkLayout {
   // refresh steps in 3xF16: M's row-scaled fp16 split (m x ldn), its rows'
   // inverse scales and row-norm bound (third float of the item's slots)
   uint64_t m16_hi, m16_lo, m_rinv, m_rmax;
+  // TF32 splits of the bases (made from the fp16 state copies): U^T and
+  // V^T for the refresh products; all four for the TF32-class rotation
+  // modes.  M's TF32 split on refresh steps.
+  uint64_t u_hi, u_lo, ut_hi, ut_lo;  // m x ldm
+  uint64_t vb_hi, vb_lo, vt_hi, vt_lo;  // n x ldn
+  uint64_t m_hi, m_lo;                // m x ldn
   // refresh region
   uint64_t mT_hi, mT_lo;  // M^T split (n x ldm)
   int zu_rows, zu_ld;

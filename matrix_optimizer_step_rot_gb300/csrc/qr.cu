@@ -643,7 +643,9 @@ __global__ void __launch_bounds__(kTThreads) qr_tblock_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Q^T = I (split), then the sign fix and the split outputs U^T and U
+// Q^T = I (split), then the sign fix and the outputs U^T and U, as the
+// 2^14-scaled fp16 splits the state keeps (22 significant bits, the
+// precision of the TF32 splits the tensor cores read)
 // ---------------------------------------------------------------------------
 
 __global__ void qr_eye_kernel(const __grid_constant__ QrBatch b) {
@@ -673,12 +675,8 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
         const int64_t oi = (int64_t)r * q.ld + c;
         v = q.qt.hi[oi] + q.qt.lo[oi];
         if (r < rank && q.beta[r] < 0.f) v = -v;  // row r of Q^T = column r of Q
-        float h, l;
-        split_tf32_mma(v, h, l);  // the bases feed only tensor cores
         const int64_t o = (int64_t)r * q.ld_out + c;
-        q.ut.hi[o] = h;
-        q.ut.lo[o] = l;
-        if (q.ut16_hi) split_f16((h + l) * kF16UnitScale, q.ut16_hi[o], q.ut16_lo[o]);
+        split_f16(v * kF16UnitScale, q.ut16_hi[o], q.ut16_lo[o]);
       }
       tile[i][tx] = v;
     }
@@ -686,12 +684,8 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
     for (int i = ty; i < 32; i += 8) {
       const int r = c0 + i, c = r0 + tx;  // U[r][c] = Q^T[c][r]
       if (r < q.p && c < q.p) {
-        float h, l;
-        split_tf32_mma(tile[tx][i], h, l);
         const int64_t o = (int64_t)r * q.ld_out + c;
-        q.u.hi[o] = h;
-        q.u.lo[o] = l;
-        if (q.u16_hi) split_f16((h + l) * kF16UnitScale, q.u16_hi[o], q.u16_lo[o]);
+        split_f16(tile[tx][i] * kF16UnitScale, q.u16_hi[o], q.u16_lo[o]);
       }
     }
     __syncthreads();

@@ -77,6 +77,9 @@ struct Range {
 inline unsigned short* H(void* base, uint64_t off) {
   return reinterpret_cast<unsigned short*>(static_cast<char*>(base) + off);
 }
+inline const unsigned short* H(const void* base, uint64_t off) {
+  return reinterpret_cast<const unsigned short*>(static_cast<const char*>(base) + off);
+}
 
 // A 3xF16 problem: a_*, b_* (and c_* for kEpiStoreF16SplitT) are fp16 arrays.
 GemmProblem gp16(int M, int N, int K, const unsigned short* ah, const unsigned short* al, int lda,
@@ -92,18 +95,6 @@ GemmProblem gp16(int M, int N, int K, const unsigned short* ah, const unsigned s
   P.in_r = in_r;
   P.out_r = out_r;
   return P;
-}
-
-// fp16 copies (scaled by 2^14) of U, U^T, V, V^T for the 3xF16 products.
-void push_f16_bases(hvec<ToF16Seg>& segs, void* state, const ItemLayout& L) {
-  segs.push_back({F(state, L.u_hi), F(state, L.u_lo), L.ldm, H(state, L.u16_hi),
-                  H(state, L.u16_lo), L.ldm, L.m, L.m});
-  segs.push_back({F(state, L.ut_hi), F(state, L.ut_lo), L.ldm, H(state, L.ut16_hi),
-                  H(state, L.ut16_lo), L.ldm, L.m, L.m});
-  segs.push_back({F(state, L.vb_hi), F(state, L.vb_lo), L.ldn, H(state, L.vb16_hi),
-                  H(state, L.vb16_lo), L.ldn, L.n, L.n});
-  segs.push_back({F(state, L.vt_hi), F(state, L.vt_lo), L.ldn, H(state, L.vt16_hi),
-                  H(state, L.vt16_lo), L.ldn, L.n, L.n});
 }
 
 }  // namespace
@@ -186,10 +177,10 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const ItemLayout& L = p->items[i];
       const WorkLayout& x = WL[k];
       if (!W[i] || !G[i]) return ROT_EINVAL;
-      segs[k] = {G[i], F(state, L.m_hi), F(state, L.m_lo), H(work, x.g_hi), H(work, x.g_lo),
+      segs[k] = {G[i], F(state, L.mom), H(work, x.g_hi), H(work, x.g_lo),
                  F(work, x.g_rinv), F(work, x.g_rmax), L.m, L.n, L.ldn,
                  refresh ? H(work, x.m16_hi) : nullptr, H(work, x.m16_lo), F(work, x.m_rinv),
-                 F(work, x.m_rmax)};
+                 F(work, x.m_rmax), F(work, x.m_hi), F(work, x.m_lo)};
     }
     ROT_TRY(launch_momentum16(segs, beta1, nonfinite, s));
   } else {
@@ -199,8 +190,8 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const int i = items[k];
       const ItemLayout& L = p->items[i];
       if (!W[i] || !G[i]) return ROT_EINVAL;
-      segs[k] = {G[i], F(state, L.m_hi), F(state, L.m_lo), F(work, WL[k].g_hi),
-                 F(work, WL[k].g_lo), L.m, L.n, L.ldn};
+      segs[k] = {G[i], F(state, L.mom), F(work, WL[k].g_hi), F(work, WL[k].g_lo), L.m, L.n,
+                 L.ldn, refresh ? F(work, WL[k].m_hi) : nullptr, F(work, WL[k].m_lo)};
     }
     ROT_TRY(launch_momentum(segs, beta1, nonfinite, s));
   }
@@ -209,20 +200,27 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   if (refresh) {
     Range range("rot: basis refresh");
     hvec<TransposeSeg> tr(n_items);
+    hvec<ToTf32Seg> old_bases;
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
-      tr[k] = {F(state, L.m_hi), F(state, L.m_lo), L.ldn, F(work, x.mT_hi), F(work, x.mT_lo),
+      tr[k] = {F(work, x.m_hi), F(work, x.m_lo), L.ldn, F(work, x.mT_hi), F(work, x.mT_lo),
                L.ldm, L.m, L.n, 1, 1, 1};
+      // the products' TF32 operands U^T and V^T (the bases before the refresh)
+      old_bases.push_back({H(state, L.ut16_hi), H(state, L.ut16_lo), L.ldm, F(work, x.ut_hi),
+                           F(work, x.ut_lo), L.ldm, L.m, L.m});
+      old_bases.push_back({H(state, L.vt16_hi), H(state, L.vt16_lo), L.ldn, F(work, x.vt_hi),
+                           F(work, x.vt_lo), L.ldn, L.n, L.n});
     }
     ROT_TRY(launch_transpose(tr, s));
+    ROT_TRY(launch_to_tf32(old_bases, s));
 
     hvec<GemmProblem> first, second;
     for (size_t k = 0; k < n_items; ++k) {
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       const int m = L.m, n = L.n;
-      const float *Mh = F(state, L.m_hi), *Ml = F(state, L.m_lo);
+      const float *Mh = F(work, x.m_hi), *Ml = F(work, x.m_lo);
       const float *MTh = F(work, x.mT_hi), *MTl = F(work, x.mT_lo);
       float *Zuh = F(work, x.zu_hi), *Zul = F(work, x.zu_lo);
       float *Zvh = F(work, x.zv_hi), *Zvl = F(work, x.zv_lo);
@@ -230,7 +228,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       float *Avh = F(work, x.avt_hi), *Avl = F(work, x.avt_lo);
       if (n < m) {
         // Z_U = M^T U (n x m), stored transposed (m x n);  A_U = M Z_U
-        first.push_back(gp(n, m, m, MTh, MTl, L.ldm, F(state, L.ut_hi), F(state, L.ut_lo), L.ldm,
+        first.push_back(gp(n, m, m, MTh, MTl, L.ldm, F(work, x.ut_hi), F(work, x.ut_lo), L.ldm,
                            Zuh, Zul, x.zu_ld, kEpiStoreSplitT, 0.f, 1));
         second.push_back(gp(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, Auh, Aul, L.ldm,
                             kEpiStoreSplitT));
@@ -238,12 +236,12 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         // Gram M M^T (m x m);  A_U = Gram U
         first.push_back(gp(m, m, n, Mh, Ml, L.ldn, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld,
                            kEpiStoreSplit, 0.f, 1));
-        second.push_back(gp(m, m, m, Zuh, Zul, x.zu_ld, F(state, L.ut_hi), F(state, L.ut_lo),
+        second.push_back(gp(m, m, m, Zuh, Zul, x.zu_ld, F(work, x.ut_hi), F(work, x.ut_lo),
                             L.ldm, Auh, Aul, L.ldm, kEpiStoreSplitT));
       }
       if (m < n) {
         // Z_V = M V (m x n), stored transposed (n x m);  A_V = M^T Z_V
-        first.push_back(gp(m, n, n, Mh, Ml, L.ldn, F(state, L.vt_hi), F(state, L.vt_lo), L.ldn,
+        first.push_back(gp(m, n, n, Mh, Ml, L.ldn, F(work, x.vt_hi), F(work, x.vt_lo), L.ldn,
                            Zvh, Zvl, x.zv_ld, kEpiStoreSplitT, 0.f, 1));
         second.push_back(gp(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, Avh, Avl, L.ldn,
                             kEpiStoreSplitT));
@@ -251,7 +249,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         // Gram M^T M (n x n);  A_V = Gram V
         first.push_back(gp(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
                            kEpiStoreSplit, 0.f, 1));
-        second.push_back(gp(n, n, n, Zvh, Zvl, x.zv_ld, F(state, L.vt_hi), F(state, L.vt_lo),
+        second.push_back(gp(n, n, n, Zvh, Zvl, x.zv_ld, F(work, x.vt_hi), F(work, x.vt_lo),
                             L.ldn, Avh, Avl, L.ldn, kEpiStoreSplitT));
       }
     }
@@ -279,13 +277,9 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         q.p = pdim;
         q.ld = ld;
         q.rmax = rmax;
-        q.u = side == 0 ? Split{F(state, L.u_hi), F(state, L.u_lo)}
-                        : Split{F(state, L.vb_hi), F(state, L.vb_lo)};
-        q.ut = side == 0 ? Split{F(state, L.ut_hi), F(state, L.ut_lo)}
-                         : Split{F(state, L.vt_hi), F(state, L.vt_lo)};
         q.ld_out = ld;
         q.rank_out = ranks + 2 * i + side;
-        // the 3xF16 products' copies of the new basis, written by the QR's last pass
+        // the new basis, written by the QR's last pass as the state's fp16 copies
         q.u16_hi = H(state, side == 0 ? L.u16_hi : L.vb16_hi);
         q.u16_lo = H(state, side == 0 ? L.u16_lo : L.vb16_lo);
         q.ut16_hi = H(state, side == 0 ? L.ut16_hi : L.vt16_hi);
@@ -302,6 +296,25 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // quantity since U and V are unchanged.  In 3xF16 mode both sides run on
   // the fp16 splits (G's or M's rows scaled by s_r, U and V by 2^14, S_G or
   // S_M by a power of two below its bound, the largest row norm of G or M).
+  if (!f16) {
+    // the TF32-class modes read TF32 splits of the four basis orientations,
+    // made from the state's fp16 copies
+    Range range("rot: TF32 bases");
+    hvec<ToTf32Seg> cv;
+    for (size_t k = 0; k < n_items; ++k) {
+      const ItemLayout& L = p->items[items[k]];
+      const WorkLayout& x = WL[k];
+      cv.push_back({H(state, L.u16_hi), H(state, L.u16_lo), L.ldm, F(work, x.u_hi),
+                    F(work, x.u_lo), L.ldm, L.m, L.m});
+      cv.push_back({H(state, L.ut16_hi), H(state, L.ut16_lo), L.ldm, F(work, x.ut_hi),
+                    F(work, x.ut_lo), L.ldm, L.m, L.m});
+      cv.push_back({H(state, L.vb16_hi), H(state, L.vb16_lo), L.ldn, F(work, x.vb_hi),
+                    F(work, x.vb_lo), L.ldn, L.n, L.n});
+      cv.push_back({H(state, L.vt16_hi), H(state, L.vt16_lo), L.ldn, F(work, x.vt_hi),
+                    F(work, x.vt_lo), L.ldn, L.n, L.n});
+    }
+    ROT_TRY(launch_to_tf32(cv, s));
+  }
   {
     Range range("rot: rotation");
     hvec<GemmProblem> a, b;
@@ -309,8 +322,8 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       const int m = L.m, n = L.n;
-      const float *Vth = F(state, L.vt_hi), *Vtl = F(state, L.vt_lo);
-      const float *Uth = F(state, L.ut_hi), *Utl = F(state, L.ut_lo);
+      const float *Vth = F(work, x.vt_hi), *Vtl = F(work, x.vt_lo);
+      const float *Uth = F(work, x.ut_hi), *Utl = F(work, x.ut_lo);
       if (f16) {
         a.push_back(gp16(m, n, n, H(work, x.g_hi), H(work, x.g_lo), L.ldn, H(state, L.vt16_hi),
                          H(state, L.vt16_lo), L.ldn, H(work, x.sg_hi), H(work, x.sg_lo), L.ldm,
@@ -334,7 +347,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
                          H(work, x.sm_hi), H(work, x.sm_lo), L.ldm, F(state, L.mt), nullptr,
                          L.ldn, kEpiStoreF32, kF16Inv, nullptr, F(work, x.m_rmax), nullptr));
       } else if (refresh) {
-        a.push_back(gp(m, n, n, F(state, L.m_hi), F(state, L.m_lo), L.ldn, Vth, Vtl, L.ldn,
+        a.push_back(gp(m, n, n, F(work, x.m_hi), F(work, x.m_lo), L.ldn, Vth, Vtl, L.ldn,
                        F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
         b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
                        F(state, L.mt), nullptr, L.ldn, kEpiStoreF32));
@@ -387,10 +400,10 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
                          H(work, x.sg_hi), H(work, x.sg_lo), L.ldm, W[i], nullptr, n, kEpiApply,
                          kF16Inv, nullptr, F(work, x.d_rmax), nullptr, lr));
       } else {
-        a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, F(state, L.vb_hi),
-                       F(state, L.vb_lo), L.ldn, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
+        a.push_back(gp(m, n, n, F(work, x.g_hi), F(work, x.g_lo), L.ldn, F(work, x.vb_hi),
+                       F(work, x.vb_lo), L.ldn, F(work, x.sg_hi), F(work, x.sg_lo), L.ldm,
                        kEpiStoreSplitT, 0.f, 1));
-        b.push_back(gp(m, n, m, F(state, L.u_hi), F(state, L.u_lo), L.ldm, F(work, x.sg_hi),
+        b.push_back(gp(m, n, m, F(work, x.u_hi), F(work, x.u_lo), L.ldm, F(work, x.sg_hi),
                        F(work, x.sg_lo), L.ldm, W[i], nullptr, n, kEpiApply, lr));
       }
     }
@@ -420,18 +433,20 @@ int state_init(const rot_plan* plan, void* state, void* stream) {
   hvec<FillSeg> segs;
   for (int32_t i = 0; i < plan->count; ++i) {
     const ItemLayout& L = plan->items[i];
-    segs.push_back({F(state, L.m_hi), F(state, L.m_lo), L.m, L.n, L.ldn, 0});
+    segs.push_back({F(state, L.mom), nullptr, L.m, L.n, L.ldn, 0});
     segs.push_back({F(state, L.v), nullptr, L.m, L.n, L.ldn, 0});
     segs.push_back({F(state, L.mt), nullptr, L.m, L.n, L.ldn, 0});
-    segs.push_back({F(state, L.u_hi), F(state, L.u_lo), L.m, L.m, L.ldm, 1});
-    segs.push_back({F(state, L.ut_hi), F(state, L.ut_lo), L.m, L.m, L.ldm, 1});
-    segs.push_back({F(state, L.vb_hi), F(state, L.vb_lo), L.n, L.n, L.ldn, 1});
-    segs.push_back({F(state, L.vt_hi), F(state, L.vt_lo), L.n, L.n, L.ldn, 1});
+    // U = U^T = I, V = V^T = I as 2^14-scaled fp16 splits
+    const uint64_t bases[4][2] = {{L.u16_hi, L.u16_lo}, {L.ut16_hi, L.ut16_lo},
+                                  {L.vb16_hi, L.vb16_lo}, {L.vt16_hi, L.vt16_lo}};
+    for (int j = 0; j < 4; ++j) {
+      const int p = j < 2 ? L.m : L.n, ld = j < 2 ? L.ldm : L.ldn;
+      FillSeg f{F(state, bases[j][0]), F(state, bases[j][1]), p, p, ld, 1};
+      f.f16 = 1;
+      segs.push_back(f);
+    }
   }
-  ROT_TRY(launch_fill(segs, s));
-  hvec<ToF16Seg> conv;
-  for (int32_t i = 0; i < plan->count; ++i) push_f16_bases(conv, state, plan->items[i]);
-  return launch_to_f16(conv, s);
+  return launch_fill(segs, s);
 }
 
 }  // namespace
@@ -490,13 +505,15 @@ int rot_state_export(const rot_plan* plan, const void* state, int32_t item, int3
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (which) {
     case ROT_WHICH_M:
-      return launch_combine(F(state, L.m_hi), F(state, L.m_lo), L.ldn, dst, L.n, L.m, L.n, s);
+      return launch_combine(F(state, L.mom), nullptr, L.ldn, dst, L.n, L.m, L.n, s);
     case ROT_WHICH_V2:
       return launch_combine(F(state, L.v), nullptr, L.ldn, dst, L.n, L.m, L.n, s);
     case ROT_WHICH_U:
-      return launch_combine(F(state, L.u_hi), F(state, L.u_lo), L.ldm, dst, L.m, L.m, L.m, s);
+      return launch_combine16(H(state, L.u16_hi), H(state, L.u16_lo), L.ldm, dst, L.m, L.m, L.m,
+                              s);
     case ROT_WHICH_V:
-      return launch_combine(F(state, L.vb_hi), F(state, L.vb_lo), L.ldn, dst, L.n, L.n, L.n, s);
+      return launch_combine16(H(state, L.vb16_hi), H(state, L.vb16_lo), L.ldn, dst, L.n, L.n,
+                              L.n, s);
     default:
       return ROT_EINVAL;
   }

@@ -130,11 +130,12 @@ int gemm_grouped(const hvec<GemmProblem>& probs, int precision, int* status,
 
 struct MomentumSeg {
   const float* g;  // caller's gradient, row-major, ld = cols
-  float* m_hi;     // state momentum split (exact), ld = ldm
-  float* m_lo;
+  float* m;        // state momentum (float32), ld = ldm
   float* g_hi;     // workspace gradient split (tensor-core operand), ld = ldm
   float* g_lo;
   int rows, cols, ldm;
+  float* m_hi;     // refresh steps: M's exact TF32 split (workspace), else null
+  float* m_lo;
 };
 // flag: the status word when the non-finite check is on (non-finite G or D
 // sets it to ROT_ENONFINITE), else null.
@@ -159,18 +160,20 @@ int launch_adam(const hvec<AdamSeg>& segs, float beta1, float beta2, float eps,
 // be 0 or smaller beforehand).  g_hi / g_lo are fp16 arrays (ld = ldm).
 struct Momentum16Seg {
   const float* g;
-  float* m_hi;
-  float* m_lo;
+  float* m;  // state momentum (float32)
   unsigned short* g_hi;
   unsigned short* g_lo;
   float* g_rinv;
   float* g_rmax;
   int rows, cols, ldm;
-  // refresh steps: M's row-scaled fp16 split too (m16_hi == nullptr: not)
+  // refresh steps: M's row-scaled fp16 split and its exact TF32 split too
+  // (m16_hi == nullptr: neither)
   unsigned short* m16_hi;
   unsigned short* m16_lo;
   float* m_rinv;
   float* m_rmax;
+  float* m_hi;
+  float* m_lo;
 };
 int launch_momentum16(const hvec<Momentum16Seg>& segs, float beta1, int* flag,
                       cudaStream_t stream);
@@ -235,12 +238,32 @@ struct TransposeSeg {
 };
 int launch_transpose(const hvec<TransposeSeg>& segs, cudaStream_t stream);
 
+// TF32 split (hi, lo: float32 arrays, lo rounded to TF32 as well) of a basis
+// held as a 2^14-scaled fp16 split; dst is src (transpose == 0) or src^T.
+struct ToTf32Seg {
+  const unsigned short* s_hi;
+  const unsigned short* s_lo;
+  int ld_src;
+  float* d_hi;
+  float* d_lo;
+  int ld_dst;
+  int rows, cols;  // of src
+};
+int launch_to_tf32(const hvec<ToTf32Seg>& segs, cudaStream_t stream);    // dst = src
+int launch_to_tf32_t(const hvec<ToTf32Seg>& segs, cudaStream_t stream);  // dst = src^T
+
+// dst (float32, rows x cols, ld_dst) = (hi + lo) / 2^14 of a 2^14-scaled fp16
+// split (basis export).
+int launch_combine16(const unsigned short* hi, const unsigned short* lo, int ld_src, float* dst,
+                     int ld_dst, int rows, int cols, cudaStream_t stream);
+
 // Fill a p x p split with the identity (lo = 0), or a rows x cols split with 0.
 struct FillSeg {
   float* hi;
   float* lo;
   int rows, cols, ld;
   int identity;
+  int f16 = 0;  // hi, lo are fp16 arrays; the identity is written as 2^14
 };
 int launch_fill(const hvec<FillSeg>& segs, cudaStream_t stream);
 
@@ -282,12 +305,10 @@ struct QrProblem {
   int* ctrl;    // [0] rank, [1] stopped flag, [2..] per-panel active counts
   float* tau;   // largest column norm of A
   int p, ld, rmax;
-  // outputs (state): U (row-major) and U^T as splits, ld_out; and the rank.
-  Split u;
-  Split ut;
+  // outputs (state): U (row-major) and U^T as fp16 splits scaled by 2^14
+  // (ld_out elements per row), and the rank
   int ld_out;
   int* rank_out;
-  // and, if set, their fp16 splits scaled by 2^14 (ld_out elements per row)
   unsigned short* u16_hi;
   unsigned short* u16_lo;
   unsigned short* ut16_hi;
