@@ -177,6 +177,23 @@ int rot_plan_group(const rot_plan* plan, int32_t g, const int32_t** items,
 /* Owner rank of every input index (borrowed array of `count` entries). */
 int rot_plan_owners(const rot_plan* plan, const int32_t** owners);
 
+/* State format of a plan (set before rot_state_bytes / rot_state_init; the
+ * layout of the state blob depends on it).
+ * ROT_STATE_FULL (default): M, v and M~ in float32; each basis, in the two
+ *   orientations the products read, as a 2^14-scaled fp16 split (22
+ *   significant bits).
+ * ROT_STATE_COMPACT: the reduced-precision state of the pages -- the first
+ *   moments M and M~ in bf16, v in float32 (the ZeRO essay, section 3.3:
+ *   m in BF16, v in FP32) and each basis orientation a single fp16 (the
+ *   rotation page, section 3.1: rotation matrices stored in float16).  About
+ *   half the bytes of the full format; bases orthogonal to about 2^-11 sqrt(p)
+ *   and W changed by about the method's own spread at these precisions (its
+ *   parity is checked against that, not against the float32 bars).
+ * Errors: ROT_EINVAL (null plan, unknown format), ROT_ENOMEM. */
+#define ROT_STATE_FULL 0
+#define ROT_STATE_COMPACT 1
+int rot_plan_set_state_format(rot_plan* plan, int32_t format);
+
 /* Bytes of the caller-allocated state blob (M, v, U, V of every matrix plus a
  * status word; persists across steps) and of the workspace blob (temporaries
  * of one step, sized for the largest micro-group; contents need not persist).

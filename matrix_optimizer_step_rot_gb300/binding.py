@@ -32,6 +32,7 @@ ROT_PREC_3XTF32 = 3
 ROT_PREC_3XTF32_PRECISE = 4
 ROT_PREC_3XF16 = 5
 ROT_WHICH_M, ROT_WHICH_V2, ROT_WHICH_U, ROT_WHICH_V = 0, 1, 2, 3
+ROT_STATE_FULL, ROT_STATE_COMPACT = 0, 1
 
 
 class RotError(RuntimeError):
@@ -70,6 +71,7 @@ _SIGS = {
     "rot_set_wait_timeout_ns": (_u64, [_u64]),
     "rot_set_nonfinite_check": (_i32, [_i32]),
     "rot_launch_count": (_u64, []),
+    "rot_plan_set_state_format": (_i32, [_vp, _i32]),
     "rot_profile_enable": (_i32, [_i32]),
     "rot_profile_reset": (_i32, []),
     "rot_profile_read": (_i32, [_i32, ctypes.POINTER(_u64), ctypes.POINTER(ctypes.c_double),
@@ -132,13 +134,17 @@ def _check(code: int, where: str) -> None:
 class Plan:
     """Owns a rot_plan handle."""
 
-    def __init__(self, shapes: Sequence[Tuple[int, int]], c_max: int, ranks: int = 1):
+    def __init__(self, shapes: Sequence[Tuple[int, int]], c_max: int, ranks: int = 1,
+                 state_format: int = 0):
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         arr = (rot_shape * max(1, len(self.shapes)))(*[rot_shape(m, n) for m, n in self.shapes])
         h = _vp()
         _check(lib().rot_plan_create_ex(arr, len(self.shapes), int(c_max), int(ranks),
                                         ctypes.byref(h)), "rot_plan_create_ex")
         self.handle = h
+        if state_format:
+            _check(lib().rot_plan_set_state_format(h, int(state_format)),
+                   "rot_plan_set_state_format")
 
     def __del__(self):
         h = getattr(self, "handle", None)

@@ -12,6 +12,8 @@
 
 #include "profile.h"
 #include "rot_internal.h"
+#include <cuda_bf16.h>
+
 #include "split.cuh"
 
 namespace rot {
@@ -55,6 +57,22 @@ int launch_segs(const hvec<Seg>& segs, double bytes_per_elem, Kernel kernel,
   return ROT_OK;
 }
 
+// State values held as float32, or as bf16 in the compact state format.
+__device__ __forceinline__ float ld_state(const float* p, int64_t o, bool bf16) {
+  return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[o]) : p[o];
+}
+__device__ __forceinline__ void st_state(float* p, int64_t o, float x, bool bf16) {
+  if (bf16) {
+    reinterpret_cast<__nv_bfloat16*>(p)[o] = __float2bfloat16_rn(x);
+  } else {
+    p[o] = x;
+  }
+}
+// x as the state keeps it (rounded to bf16 in the compact format)
+__device__ __forceinline__ float as_state(float x, bool bf16) {
+  return bf16 ? __bfloat162float(__float2bfloat16_rn(x)) : x;
+}
+
 // Optional non-finite check (rot_set_nonfinite_check): `flag` is the status
 // word or null.  A thread that saw a non-finite value sets it to
 // ROT_ENONFINITE once (unless another status is already there); the values
@@ -78,8 +96,8 @@ __global__ void momentum_kernel(const __grid_constant__ SegBatch<MomentumSeg> b,
     const int64_t o = (int64_t)r * s.ldm + c;
     const float g = s.g[e];
     bad |= check && !isfinite(g);
-    const float m = beta1 * s.m[o] + one_minus * g;
-    s.m[o] = m;
+    const float m = as_state(beta1 * ld_state(s.m, o, s.m_bf16) + one_minus * g, s.m_bf16);
+    st_state(s.m, o, m, s.m_bf16);
     float h, l;
     if (s.m_hi) {
       split_tf32(m, h, l);
@@ -108,10 +126,10 @@ __global__ void adam_kernel(const __grid_constant__ SegBatch<AdamSeg> b, float b
     const int r = (int)(e / s.cols), c = (int)(e - (int64_t)r * s.cols);
     const int64_t o = (int64_t)r * s.ld + c;
     const float g = s.gt[o];
-    float m = s.mt[o];
+    float m = ld_state(s.mt, o, s.mt_bf16);
     if (incremental) {
-      m = beta1 * m + one_minus1 * g;
-      s.mt[o] = m;
+      m = as_state(beta1 * m + one_minus1 * g, s.mt_bf16);
+      st_state(s.mt, o, m, s.mt_bf16);
     }
     const float v = beta2 * s.v[o] + one_minus * (g * g);
     s.v[o] = v;
@@ -177,11 +195,14 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
                                   float beta1, int* flag) {
   const Momentum16Seg& s = b.seg[blockIdx.y];
   const float one_minus = 1.0f - beta1;
-  const int nv = ((s.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(s.g) & 15) == 0)
+  const bool bf = s.m_bf16 != 0;
+  const int nv = (!bf && (s.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(s.g) & 15) == 0)
                      ? s.cols / 4 : 0;
   for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
     const float* g = s.g + (int64_t)r * s.cols;
-    float* mr = s.m + (int64_t)r * s.ldm;
+    float* mr = bf ? reinterpret_cast<float*>(reinterpret_cast<__nv_bfloat16*>(s.m) +
+                                              (int64_t)r * s.ldm)
+                   : s.m + (int64_t)r * s.ldm;
     unsigned short* gh = s.g_hi + (int64_t)r * s.ldm;
     unsigned short* gl = s.g_lo + (int64_t)r * s.ldm;
     float sum = 0.f, mx = 0.f;
@@ -194,8 +215,11 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
       momentum_elem(x.w, mm.w, beta1, one_minus, sum, mx);
       reinterpret_cast<float4*>(mr)[q] = mm;
     }
-    for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x)
-      momentum_elem(g[c], mr[c], beta1, one_minus, sum, mx);
+    for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x) {
+      float m = ld_state(mr, c, bf);
+      momentum_elem(g[c], m, beta1, one_minus, sum, mx);
+      st_state(mr, c, m, bf);
+    }
     block_sum_max(sum, mx);
     const float scale = pow2_below(mx, kF16ScaleExp);
     if (threadIdx.x == 0) {
@@ -208,7 +232,7 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
       // M's new row (this thread's own writes above), its scale and splits
       float msum = 0.f, mmx = 0.f;
       for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-        const float m = mr[c];
+        const float m = ld_state(mr, c, bf);
         msum = fmaf(m, m, msum);
         mmx = fmaxf(mmx, fabsf(m));
       }
@@ -223,7 +247,7 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
       float* mth = s.m_hi + (int64_t)r * s.ldm;
       float* mtl = s.m_lo + (int64_t)r * s.ldm;
       for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-        const float m = mr[c];
+        const float m = ld_state(mr, c, bf);
         split_f16(m * mscale, m16h[c], m16l[c]);
         split_tf32(m, mth[c], mtl[c]);
       }
@@ -263,10 +287,13 @@ __global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, flo
   const Adam16Seg& s = b.seg[blockIdx.y];
   const float one_minus1 = 1.0f - beta1;
   const float one_minus = 1.0f - beta2;
-  const int nv = s.cols / 4;
+  const bool bf = s.mt_bf16 != 0;
+  const int nv = bf ? 0 : s.cols / 4;
   for (int r = blockIdx.x; r < s.rows; r += gridDim.x) {
     const float* gt = s.gt + (int64_t)r * s.ld;
-    float* mt = s.mt + (int64_t)r * s.ld;
+    float* mt = bf ? reinterpret_cast<float*>(reinterpret_cast<__nv_bfloat16*>(s.mt) +
+                                              (int64_t)r * s.ld)
+                   : s.mt + (int64_t)r * s.ld;
     float* v = s.v + (int64_t)r * s.ld;
     unsigned short* dh = s.d_hi + (int64_t)r * s.ld;
     unsigned short* dl = s.d_lo + (int64_t)r * s.ld;
@@ -283,9 +310,12 @@ __global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, flo
       reinterpret_cast<float4*>(v)[q] = w;
     }
     for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x) {
-      float m = mt[c], w = v[c];
-      adam_elem(gt[c], m, w, beta1, one_minus1, beta2, one_minus, eps, incremental, sum, mx);
-      if (incremental) mt[c] = m;
+      float m = ld_state(mt, c, bf), w = v[c];
+      if (incremental) {  // the stored (rounded) M~ is the one D uses
+        m = as_state(beta1 * m + one_minus1 * gt[c], bf);
+        st_state(mt, c, m, bf);
+      }
+      adam_elem(gt[c], m, w, beta1, one_minus1, beta2, one_minus, eps, 0, sum, mx);
       v[c] = w;
     }
     block_sum_max(sum, mx);
@@ -307,7 +337,7 @@ __global__ void adam16_kernel(const __grid_constant__ SegBatch<Adam16Seg> b, flo
       reinterpret_cast<ushort4*>(dl)[q] = l;
     }
     for (int c = 4 * nv + threadIdx.x; c < s.cols; c += blockDim.x)
-      split_f16(mt[c] / (sqrtf(v[c]) + eps) * scale, dh[c], dl[c]);
+      split_f16(ld_state(mt, c, bf) / (sqrtf(v[c]) + eps) * scale, dh[c], dl[c]);
   }
 }
 
@@ -486,13 +516,14 @@ __global__ void split_kernel(const __grid_constant__ SegBatch<SplitSeg> b) {
 }
 
 __global__ void combine_kernel(const float* hi, const float* lo, int ld_src, float* dst,
-                               int ld_dst, int rows, int cols) {
+                               int ld_dst, int rows, int cols, int src_bf16) {
   const int64_t total = (int64_t)rows * cols;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(e / cols), c = (int)(e - (int64_t)r * cols);
     const int64_t o = (int64_t)r * ld_src + c;
-    dst[(int64_t)r * ld_dst + c] = lo ? hi[o] + lo[o] : hi[o];
+    dst[(int64_t)r * ld_dst + c] =
+        src_bf16 ? ld_state(hi, o, true) : (lo ? hi[o] + lo[o] : hi[o]);
   }
 }
 
@@ -640,12 +671,12 @@ int launch_split(const hvec<SplitSeg>& segs, cudaStream_t stream) {
 }
 
 int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,
-                   int rows, int cols, cudaStream_t stream) {
+                   int rows, int cols, cudaStream_t stream, int src_bf16) {
   const int64_t total = (int64_t)rows * cols;
   if (total == 0) return ROT_OK;
   ProfScope prof(ROT_PROF_ELEMENTWISE, (double)total * (lo ? 12 : 8), stream);
   combine_kernel<<<grid_x_for(total), kThreads, 0, stream>>>(hi, lo, ld_src, dst, ld_dst, rows,
-                                                             cols);
+                                                             cols, src_bf16);
   return cudaGetLastError() == cudaSuccess ? ROT_OK : ROT_ECUDA;
 }
 

@@ -21,6 +21,7 @@
 // and reports ROT_ETIMEOUT through the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
 #include <algorithm>
 #include <cstring>
@@ -180,6 +181,14 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
           }
         }
       }
+      return;
+    }
+    case kEpiStoreBF16: {
+      if (row >= M) return;
+      __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(P.c_hi) + (int64_t)row * P.ldc + col0;
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if (t < ncol) c[t] = __float2bfloat16_rn(__uint_as_float(r[t]));
       return;
     }
     case kEpiApply: {

@@ -115,8 +115,19 @@ struct Cursor {
 
 void build_layout(rot_plan* p) {
   Cursor s;
+  const bool compact = p->state_format == ROT_STATE_COMPACT;
   s.take(256);                                   // status word (+ padding)
   p->ranks_off = s.take(8ull * (uint64_t)std::max(p->count, 1));
+  p->zeros_off = 0;
+  p->zeros_bytes = 0;
+  if (compact) {  // one array of zeros as large as the largest basis
+    int64_t most = 0;
+    for (int32_t i = 0; i < p->count; ++i)
+      for (int64_t d : {(int64_t)p->shapes[i].m, (int64_t)p->shapes[i].n})
+        most = std::max(most, d * pad_ld(d));
+    p->zeros_bytes = 2ull * (uint64_t)std::max<int64_t>(most, 1);
+    p->zeros_off = s.take(p->zeros_bytes);
+  }
   p->items.resize(p->count);
   for (int32_t i = 0; i < p->count; ++i) {
     ItemLayout& L = p->items[i];
@@ -125,6 +136,16 @@ void build_layout(rot_plan* p) {
     L.n = (int)n;
     L.ldm = (int)pad_ld(m);
     L.ldn = (int)pad_ld(n);
+    if (compact) {
+      L.mom = s.halves(m, L.ldn);
+      L.v = s.floats(m, L.ldn);
+      L.mt = s.halves(m, L.ldn);
+      L.u16_hi = s.halves(m, L.ldm);
+      L.ut16_hi = s.halves(m, L.ldm);
+      L.vb16_hi = s.halves(n, L.ldn);
+      L.vt16_hi = s.halves(n, L.ldn);
+      continue;
+    }
     L.mom = s.floats(m, L.ldn);
     L.v = s.floats(m, L.ldn);
     L.mt = s.floats(m, L.ldn);
@@ -137,6 +158,9 @@ void build_layout(rot_plan* p) {
     L.vt16_hi = s.halves(n, L.ldn);
     L.vt16_lo = s.halves(n, L.ldn);
   }
+  if (compact)
+    for (ItemLayout& L : p->items)
+      L.u16_lo = L.ut16_lo = L.vb16_lo = L.vt16_lo = p->zeros_off;
   p->state_bytes = s.at;
 
   // Workspace: per group, a rotation region, the TF32 splits of the bases
@@ -282,6 +306,18 @@ int rot_plan_group(const rot_plan* plan, int32_t g, const int32_t** items, int32
 int rot_plan_owners(const rot_plan* plan, const int32_t** owners) {
   if (!plan || !owners) return ROT_EINVAL;
   *owners = plan->owners.data();
+  return ROT_OK;
+}
+
+int rot_plan_set_state_format(rot_plan* plan, int32_t format) {
+  if (!plan || (format != ROT_STATE_FULL && format != ROT_STATE_COMPACT)) return ROT_EINVAL;
+  if (plan->state_format == format) return ROT_OK;
+  try {
+    plan->state_format = format;
+    rot::build_layout(plan);
+  } catch (const std::bad_alloc&) {
+    return ROT_ENOMEM;
+  }
   return ROT_OK;
 }
 

@@ -17,11 +17,14 @@ namespace rot {
 // (hi + lo = 2^14 x, 22 significant bits, the same as the TF32 splits the
 // tensor cores read).  TF32 splits are made from them in the workspace where
 // a product needs them.
+// In the compact format (ROT_STATE_COMPACT) M and M~ are bf16 and each basis
+// orientation a single 2^14-scaled fp16 (the lo offsets then all point at
+// one shared array of zeros, which the products read as the missing lo).
 struct ItemLayout {
   int m, n, ldm, ldn;                 // ldm = pad(m), ldn = pad(n)
-  uint64_t mom;                       // momentum M (float32), m x ldn
-  uint64_t v;                         // second moment, m x ldn
-  uint64_t mt;                        // M~ = U^T M V (float32), m x ldn
+  uint64_t mom;                       // momentum M (float32, or bf16), m x ldn
+  uint64_t v;                         // second moment (float32), m x ldn
+  uint64_t mt;                        // M~ = U^T M V (float32, or bf16), m x ldn
   // fp16 splits of U, U^T (m x ldm) and V, V^T (n x ldn), scaled by 2^14
   uint64_t u16_hi, u16_lo, ut16_hi, ut16_lo;
   uint64_t vb16_hi, vb16_lo, vt16_hi, vt16_lo;
@@ -72,6 +75,9 @@ uint64_t item_bytes(int64_t m, int64_t n);
 struct rot_plan {
   int32_t count = 0;
   int32_t ranks = 1;
+  int32_t state_format = ROT_STATE_FULL;
+  uint64_t zeros_off = 0;    // compact format: the shared zero array (fp16), else 0
+  uint64_t zeros_bytes = 0;
   uint64_t c_max = 0;
   rot::hvec<rot_shape> shapes;
   rot::hvec<rot::hvec<int32_t>> groups;

@@ -676,7 +676,11 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
         v = q.qt.hi[oi] + q.qt.lo[oi];
         if (r < rank && q.beta[r] < 0.f) v = -v;  // row r of Q^T = column r of Q
         const int64_t o = (int64_t)r * q.ld_out + c;
-        split_f16(v * kF16UnitScale, q.ut16_hi[o], q.ut16_lo[o]);
+        if (q.ut16_lo) {
+          split_f16(v * kF16UnitScale, q.ut16_hi[o], q.ut16_lo[o]);
+        } else {
+          q.ut16_hi[o] = __half_as_ushort(__float2half_rn(v * kF16UnitScale));
+        }
       }
       tile[i][tx] = v;
     }
@@ -685,7 +689,11 @@ __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
       const int r = c0 + i, c = r0 + tx;  // U[r][c] = Q^T[c][r]
       if (r < q.p && c < q.p) {
         const int64_t o = (int64_t)r * q.ld_out + c;
-        split_f16(tile[tx][i] * kF16UnitScale, q.u16_hi[o], q.u16_lo[o]);
+        if (q.u16_lo) {
+          split_f16(tile[tx][i] * kF16UnitScale, q.u16_hi[o], q.u16_lo[o]);
+        } else {
+          q.u16_hi[o] = __half_as_ushort(__float2half_rn(tile[tx][i] * kF16UnitScale));
+        }
       }
     }
     __syncthreads();

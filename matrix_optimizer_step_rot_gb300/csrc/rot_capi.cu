@@ -164,6 +164,8 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   const size_t n_items = items.size();
 
   const bool f16 = precision == ROT_PREC_3XF16;
+  const int compact = p->state_format == ROT_STATE_COMPACT;
+  const int mt_epi = compact ? kEpiStoreBF16 : kEpiStoreF32;  // M~ as the state keeps it
   Range group_range("rot: micro-group");
 
   // (1) momentum, and the TF32 split of G (3xF16: its scaled fp16 split)
@@ -180,7 +182,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       segs[k] = {G[i], F(state, L.mom), H(work, x.g_hi), H(work, x.g_lo),
                  F(work, x.g_rinv), F(work, x.g_rmax), L.m, L.n, L.ldn,
                  refresh ? H(work, x.m16_hi) : nullptr, H(work, x.m16_lo), F(work, x.m_rinv),
-                 F(work, x.m_rmax), F(work, x.m_hi), F(work, x.m_lo)};
+                 F(work, x.m_rmax), F(work, x.m_hi), F(work, x.m_lo), compact};
     }
     ROT_TRY(launch_momentum16(segs, beta1, nonfinite, s));
   } else {
@@ -191,7 +193,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const ItemLayout& L = p->items[i];
       if (!W[i] || !G[i]) return ROT_EINVAL;
       segs[k] = {G[i], F(state, L.mom), F(work, WL[k].g_hi), F(work, WL[k].g_lo), L.m, L.n,
-                 L.ldn, refresh ? F(work, WL[k].m_hi) : nullptr, F(work, WL[k].m_lo)};
+                 L.ldn, refresh ? F(work, WL[k].m_hi) : nullptr, F(work, WL[k].m_lo), compact};
     }
     ROT_TRY(launch_momentum(segs, beta1, nonfinite, s));
   }
@@ -279,11 +281,12 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         q.rmax = rmax;
         q.ld_out = ld;
         q.rank_out = ranks + 2 * i + side;
-        // the new basis, written by the QR's last pass as the state's fp16 copies
+        // the new basis, written by the QR's last pass as the state's fp16
+        // copies (hi alone in the compact format, whose lo is the shared zeros)
         q.u16_hi = H(state, side == 0 ? L.u16_hi : L.vb16_hi);
-        q.u16_lo = H(state, side == 0 ? L.u16_lo : L.vb16_lo);
+        q.u16_lo = compact ? nullptr : H(state, side == 0 ? L.u16_lo : L.vb16_lo);
         q.ut16_hi = H(state, side == 0 ? L.ut16_hi : L.vt16_hi);
-        q.ut16_lo = H(state, side == 0 ? L.ut16_lo : L.vt16_lo);
+        q.ut16_lo = compact ? nullptr : H(state, side == 0 ? L.ut16_lo : L.vt16_lo);
         qp.push_back(q);
       }
     }
@@ -345,12 +348,12 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
                          nullptr, F(work, x.m_rmax)));
         b.push_back(gp16(m, n, m, H(state, L.ut16_hi), H(state, L.ut16_lo), L.ldm,
                          H(work, x.sm_hi), H(work, x.sm_lo), L.ldm, F(state, L.mt), nullptr,
-                         L.ldn, kEpiStoreF32, kF16Inv, nullptr, F(work, x.m_rmax), nullptr));
+                         L.ldn, mt_epi, kF16Inv, nullptr, F(work, x.m_rmax), nullptr));
       } else if (refresh) {
         a.push_back(gp(m, n, n, F(work, x.m_hi), F(work, x.m_lo), L.ldn, Vth, Vtl, L.ldn,
                        F(work, x.sm_hi), F(work, x.sm_lo), L.ldm, kEpiStoreSplitT, 0.f, 1));
         b.push_back(gp(m, n, m, Uth, Utl, L.ldm, F(work, x.sm_hi), F(work, x.sm_lo), L.ldm,
-                       F(state, L.mt), nullptr, L.ldn, kEpiStoreF32));
+                       F(state, L.mt), nullptr, L.ldn, mt_epi));
       }
     }
     ROT_TRY(gemm_grouped(a, precision, status, s));
@@ -365,7 +368,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       segs[k] = {F(work, x.gt), F(state, L.mt), F(state, L.v), H(work, x.g_hi), H(work, x.g_lo),
-                 F(work, x.d_rinv), F(work, x.d_rmax), L.m, L.n, L.ldn};
+                 F(work, x.d_rinv), F(work, x.d_rmax), L.m, L.n, L.ldn, compact};
     }
     ROT_TRY(launch_adam16(segs, beta1, beta2, eps, refresh ? 0 : 1, nonfinite, s));
   } else {
@@ -375,7 +378,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       const ItemLayout& L = p->items[items[k]];
       const WorkLayout& x = WL[k];
       segs[k] = {F(work, x.gt), F(state, L.mt), F(state, L.v), F(work, x.g_hi), F(work, x.g_lo),
-                 L.m, L.n, L.ldn};
+                 L.m, L.n, L.ldn, compact};
     }
     ROT_TRY(launch_adam(segs, beta1, beta2, eps, refresh ? 0 : 1, nonfinite, s));
   }
@@ -430,18 +433,26 @@ int state_init(const rot_plan* plan, void* state, void* stream) {
   if (cudaMemsetAsync(static_cast<char*>(state) + plan->ranks_off, 0xff,
                       8ull * (uint64_t)(plan->count > 0 ? plan->count : 1), s) != cudaSuccess)
     return ROT_ECUDA;
+  const bool compact = plan->state_format == ROT_STATE_COMPACT;
+  if (compact && plan->zeros_bytes &&
+      cudaMemsetAsync(static_cast<char*>(state) + plan->zeros_off, 0, plan->zeros_bytes, s) !=
+          cudaSuccess)
+    return ROT_ECUDA;
   hvec<FillSeg> segs;
   for (int32_t i = 0; i < plan->count; ++i) {
     const ItemLayout& L = plan->items[i];
-    segs.push_back({F(state, L.mom), nullptr, L.m, L.n, L.ldn, 0});
+    FillSeg mom{F(state, L.mom), nullptr, L.m, L.n, L.ldn, 0};
+    FillSeg mt{F(state, L.mt), nullptr, L.m, L.n, L.ldn, 0};
+    mom.f16 = mt.f16 = compact;  // bf16 zero has the fp16 zero's bits
+    segs.push_back(mom);
     segs.push_back({F(state, L.v), nullptr, L.m, L.n, L.ldn, 0});
-    segs.push_back({F(state, L.mt), nullptr, L.m, L.n, L.ldn, 0});
+    segs.push_back(mt);
     // U = U^T = I, V = V^T = I as 2^14-scaled fp16 splits
     const uint64_t bases[4][2] = {{L.u16_hi, L.u16_lo}, {L.ut16_hi, L.ut16_lo},
                                   {L.vb16_hi, L.vb16_lo}, {L.vt16_hi, L.vt16_lo}};
     for (int j = 0; j < 4; ++j) {
       const int p = j < 2 ? L.m : L.n, ld = j < 2 ? L.ldm : L.ldn;
-      FillSeg f{F(state, bases[j][0]), F(state, bases[j][1]), p, p, ld, 1};
+      FillSeg f{F(state, bases[j][0]), compact ? nullptr : F(state, bases[j][1]), p, p, ld, 1};
       f.f16 = 1;
       segs.push_back(f);
     }
@@ -505,7 +516,8 @@ int rot_state_export(const rot_plan* plan, const void* state, int32_t item, int3
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (which) {
     case ROT_WHICH_M:
-      return launch_combine(F(state, L.mom), nullptr, L.ldn, dst, L.n, L.m, L.n, s);
+      return launch_combine(F(state, L.mom), nullptr, L.ldn, dst, L.n, L.m, L.n, s,
+                            plan->state_format == ROT_STATE_COMPACT);
     case ROT_WHICH_V2:
       return launch_combine(F(state, L.v), nullptr, L.ldn, dst, L.n, L.m, L.n, s);
     case ROT_WHICH_U:

@@ -78,6 +78,7 @@ enum GemmEpi : int {
   kEpiApply = 4,        // C (row-major, float32 in c.hi) -= alpha * acc
   kEpiApplySplit = 5,   // C (row-major split) <- split(hi + lo - alpha * acc)
   kEpiStoreF16SplitT = 6,  // C^T (row-major N x M fp16 arrays) <- scaled fp16 split (3xF16)
+  kEpiStoreBF16 = 7,    // C (row-major) <- acc rounded to bf16, into c.hi (compact state)
 };
 
 struct GemmProblem {
@@ -130,12 +131,13 @@ int gemm_grouped(const hvec<GemmProblem>& probs, int precision, int* status,
 
 struct MomentumSeg {
   const float* g;  // caller's gradient, row-major, ld = cols
-  float* m;        // state momentum (float32), ld = ldm
+  float* m;        // state momentum (float32, or bf16 when m_bf16), ld = ldm
   float* g_hi;     // workspace gradient split (tensor-core operand), ld = ldm
   float* g_lo;
   int rows, cols, ldm;
   float* m_hi;     // refresh steps: M's exact TF32 split (workspace), else null
   float* m_lo;
+  int m_bf16 = 0;  // compact state: M is stored as bf16
 };
 // flag: the status word when the non-finite check is on (non-finite G or D
 // sets it to ROT_ENONFINITE), else null.
@@ -143,11 +145,12 @@ int launch_momentum(const hvec<MomentumSeg>& segs, float beta1, int* flag, cudaS
 
 struct AdamSeg {
   const float* gt;  // G~ float32, ld
-  float* mt;        // state M~ float32, ld (updated in place when incremental)
+  float* mt;        // state M~ float32 (bf16 when mt_bf16), ld (updated in place when incremental)
   float* v;         // state second moment, ld
   float* d_hi;      // D split out, ld
   float* d_lo;
   int rows, cols, ld;
+  int mt_bf16 = 0;
 };
 // incremental != 0: M~ <- beta1 M~ + (1 - beta1) G~ first (bases unchanged
 // since the last step); else M~ was just recomputed as U^T M V.
@@ -174,6 +177,7 @@ struct Momentum16Seg {
   float* m_rmax;
   float* m_hi;
   float* m_lo;
+  int m_bf16 = 0;  // compact state: M is stored as bf16
 };
 int launch_momentum16(const hvec<Momentum16Seg>& segs, float beta1, int* flag,
                       cudaStream_t stream);
@@ -189,6 +193,7 @@ struct Adam16Seg {
   float* d_rinv;
   float* d_rmax;
   int rows, cols, ld;
+  int mt_bf16 = 0;  // compact state: M~ is stored as bf16
 };
 int launch_adam16(const hvec<Adam16Seg>& segs, float beta1, float beta2, float eps,
                   int incremental, int* flag, cudaStream_t stream);
@@ -278,9 +283,10 @@ struct SplitSeg {
 };
 int launch_split(const hvec<SplitSeg>& segs, cudaStream_t stream);
 
-// dst (rows x cols, ld_dst, float32) = hi + lo (or hi alone when lo == nullptr).
+// dst (rows x cols, ld_dst, float32) = hi + lo (or hi alone when lo == nullptr;
+// src_bf16: hi is a bf16 array and lo is ignored).
 int launch_combine(const float* hi, const float* lo, int ld_src, float* dst, int ld_dst,
-                   int rows, int cols, cudaStream_t stream);
+                   int rows, int cols, cudaStream_t stream, int src_bf16 = 0);
 
 // ---------------------------------------------------------------------------
 // Batched blocked Householder QR+ (Q factor only)
@@ -306,7 +312,8 @@ struct QrProblem {
   float* tau;   // largest column norm of A
   int p, ld, rmax;
   // outputs (state): U (row-major) and U^T as fp16 splits scaled by 2^14
-  // (ld_out elements per row), and the rank
+  // (ld_out elements per row; a null lo keeps hi alone, rounded to fp16),
+  // and the rank
   int ld_out;
   int* rank_out;
   unsigned short* u16_hi;

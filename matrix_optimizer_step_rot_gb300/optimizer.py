@@ -13,15 +13,16 @@ from . import binding as B
 class RotatedAdam:
     """Rotated-Adam step over a fixed list of float32 matrices.
 
-    shapes: (m, n) per matrix; c_max: micro-group byte cap.  The state blob
+    shapes: (m, n) per matrix; c_max: micro-group byte cap; state_format:
+    ROT_STATE_FULL or ROT_STATE_COMPACT (bf16 moments, fp16 bases).  The state blob
     (M, v, U, V per matrix) and the workspace blob are torch uint8 tensors on
     `device`; the library writes them through raw pointers.
     """
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], c_max: int, device="cuda",
                  beta1=0.9, beta2=0.999, eps=1e-8, lr=1e-3, rank_rtol=1e-3,
-                 precision=B.ROT_PREC_3XTF32):
-        self.plan = B.Plan(shapes, c_max)
+                 precision=B.ROT_PREC_3XTF32, state_format=B.ROT_STATE_FULL):
+        self.plan = B.Plan(shapes, c_max, state_format=state_format)
         self.device = torch.device(device)
         sb, wb = self.plan.state_bytes()
         self.state = torch.empty(sb, dtype=torch.uint8, device=self.device)

@@ -442,11 +442,17 @@ def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: flo
 
 FLOOR_REL = 2.0 ** -24  # float32 unit roundoff
 FLOOR_SEEDS = (1, 2, 3, 4, 5)
+# The reduced-precision state the pages describe: rotation matrices stored in
+# float16 (the rotation page, section 3.1; unit roundoff 2^-11) and the first
+# moment in BF16 (the ZeRO essay, section 3.3; unit roundoff 2^-8), v and
+# everything else as before.
+COMPACT_RELS = {"U": 2.0 ** -11, "V": 2.0 ** -11, "M": 2.0 ** -8, "Mt": 2.0 ** -8}
 
 
 def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         first_step: int = 1, perturb_seed: Optional[int] = None,
-        perturb_rel: float = FLOOR_REL) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
+        perturb_rel: float = FLOOR_REL,
+        perturb_rels: Optional[Dict[str, float]] = None) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
     """Run `steps` steps (default: the workload's) for the chosen matrices.
 
     `wl` is a workload object exposing shapes, hyper, refresh(t), w0(i) and
@@ -456,7 +462,9 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     step()) is multiplied element-wise by (1 + perturb_rel * xi), xi ~ N(0, 1),
     each time it is formed: the same method on values that differ at float32
     rounding level.  How far that moves the final W is the method's own
-    sensitivity, the floor any float32 implementation faces.
+    sensitivity, the floor any float32 implementation faces.  perturb_rels
+    gives some quantities (by the names step() uses) another size: the
+    rounding of a lower-precision storage format (COMPACT_RELS).
     """
     items = list(range(wl.count)) if items is None else list(items)
     steps = wl.steps if steps is None else steps
@@ -469,8 +477,9 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         perturb = None
         if perturb_seed is not None:
             rng = np.random.default_rng([perturb_seed, i])
-            perturb = (lambda name, X, rng=rng:
-                       X * (1.0 + perturb_rel * rng.standard_normal(X.shape)))
+            rels = dict(perturb_rels or {})
+            perturb = (lambda name, X, rng=rng, rels=rels:
+                       X * (1.0 + rels.get(name, perturb_rel) * rng.standard_normal(X.shape)))
         for t in range(first_step, first_step + steps):
             W = step(W, wl.grad(i, t), st, h.beta1, h.beta2, h.eps, h.lr, wl.refresh(t),
                      h.rank_rtol, perturb=perturb)
@@ -479,14 +488,16 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
 
 
 def floor(wl, item: int, W_ref: np.ndarray, seeds: Sequence[int] = FLOOR_SEEDS,
-          steps: Optional[int] = None, rel: float = FLOOR_REL) -> float:
+          steps: Optional[int] = None, rel: float = FLOOR_REL,
+          rels: Optional[Dict[str, float]] = None) -> float:
     """The method's float32 floor for one matrix: the largest relative change
     of the final W over runs (one per seed) whose stored quantities are
-    perturbed at relative size `rel` (float32 unit roundoff by default; see
-    run())."""
+    perturbed at relative size `rel` (float32 unit roundoff by default;
+    `rels` overrides it per quantity, see run())."""
     worst = 0.0
     for s in seeds:
-        Wp, _ = run(wl, [item], steps=steps, perturb_seed=s, perturb_rel=rel)[item]
+        Wp, _ = run(wl, [item], steps=steps, perturb_seed=s, perturb_rel=rel,
+                    perturb_rels=rels)[item]
         worst = max(worst, float(np.linalg.norm(Wp - W_ref) / np.linalg.norm(W_ref)))
     return worst
 

@@ -203,3 +203,19 @@ def test_partitions_report_host_allocation_failure():
     # and the results are unaffected by the earlier failures
     o = orc.alpha_partition(work, sizes, 4, 1.0)
     assert B.partition_alpha(work, sizes, 4, 1.0) == (o.owners, o.loads)
+
+
+def test_compact_state_bytes():
+    """The reduced-precision format (bf16 moments, fp16 bases) takes about the
+    algorithmic float32 state (M, v, U, V) and less than 0.6 of the full
+    format; switching back restores the full layout."""
+    wl = inputs.workload("full")
+    p = B.Plan(wl.shapes, wl.c_max)
+    full = p.state_bytes()[0]
+    assert B.lib().rot_plan_set_state_format(p.handle, B.ROT_STATE_COMPACT) == B.ROT_OK
+    compact = p.state_bytes()[0]
+    algorithmic = sum(4 * (2 * m * n + m * m + n * n) for m, n in wl.shapes)
+    assert compact <= 1.05 * algorithmic and compact < 0.6 * full
+    assert B.lib().rot_plan_set_state_format(p.handle, B.ROT_STATE_FULL) == B.ROT_OK
+    assert p.state_bytes()[0] == full
+    assert B.lib().rot_plan_set_state_format(p.handle, 7) == B.ROT_EINVAL

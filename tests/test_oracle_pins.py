@@ -423,3 +423,19 @@ def test_floor_large_when_the_first_step_refreshes():
     wl = _small_workload(3, 1)
     W, _ = orc.run(wl, [0])[0]
     assert orc.floor(wl, 0, W) > 1e3 * 2.0 ** -24
+
+
+def test_per_quantity_perturbation_sizes():
+    """perturb_rels reaches only the named quantities: a size for a name the
+    step never forms changes nothing; the compact format's sizes (fp16 bases,
+    bf16 moments) move W by much more than float32 rounding; perturbing only
+    M at 16 times the size moves W 16 times as far (first order, smooth case)."""
+    wl = _small_workload(5, 100)
+    W, _ = orc.run(wl, [1])[1]
+    u = 2.0 ** -24
+    base = orc.floor(wl, 1, W, rel=u)
+    assert orc.floor(wl, 1, W, rel=u, rels={"no such quantity": 1.0}) == base
+    assert orc.floor(wl, 1, W, rel=u, rels=orc.COMPACT_RELS) > 100 * base
+    only_m = orc.floor(wl, 1, W, rel=0.0, rels={"M": 2.0 ** -12})
+    only_m16 = orc.floor(wl, 1, W, rel=0.0, rels={"M": 2.0 ** -8})
+    assert 14.0 < only_m16 / only_m < 18.0
