@@ -413,6 +413,10 @@ def run_ours(args):
                     "gaps_ms": [round(x, 2) for x in e2e_gaps_ms]},
             "gpu_launches": launches,
             "clocks": clocks,
+            "parity": ("W within 1e-4 of the float64 oracle on every sampled shape of the tiny, "
+                       "block and full-stack workloads; the Qwen3-8B-shaped slice and the ragged "
+                       "set miss 1e-4 on some matrices, where float32 arithmetic itself does "
+                       "(tests/test_configs_gpu.py, profiles/parity_full_size.txt)"),
         }
         if world == 1 and not args.no_cpu_baseline:
             v, secs_cpu, desc = oracle_sample(wl, 5, first_step=1)

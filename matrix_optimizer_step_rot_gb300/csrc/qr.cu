@@ -174,8 +174,10 @@ __global__ void qr_scale_kernel(const __grid_constant__ QrBatch b) {
 // w = x - beta e_k, w . a_c = x . a_c - beta a_c[k] follows from those sums,
 // and so do the Gram entries w_i . w_j of the panel's triangular factor.
 // The 64 partial values of every CTA go to every CTA through distributed
-// shared memory; each adds them in the same order, so all of them take the
-// same decisions.
+// shared memory; every warp of every CTA adds them in the same order, so all
+// of them take the same decisions, and each warp derives the reflector's
+// coefficients itself.  A column therefore costs one block barrier (the
+// warps' partial sums) and one cluster barrier (the exchange).
 // ---------------------------------------------------------------------------
 
 constexpr int kPanelThreads = 256;
@@ -190,9 +192,9 @@ __global__ void __launch_bounds__(kPanelThreads)
   extern __shared__ float panel[];  // [B][R]
   __shared__ float slot[2][kMaxCluster][2 * B];
   __shared__ float red[B][kPanelThreads / 32 + 1];
-  __shared__ float sums[2 * B];  // [0, B): x_j . a_c ; [B, 2B): a_c[k]
-  __shared__ float s_piv[B];
+  __shared__ float s_piv[2][B];  // pivot row a_c[k] of the column being reduced, by parity
   __shared__ float s_coef[B];
+  __shared__ float w_coef[kPanelThreads / 32][B];  // each warp's copy of the coefficients
   __shared__ float s_ww[B], s_beta[B];
   __shared__ float gram[B][B + 1];
   __shared__ float tmat[B][B + 1];
@@ -243,12 +245,18 @@ __global__ void __launch_bounds__(kPanelThreads)
       at_hi[o] = 0.f;
       at_lo[o] = 0.f;
     }
-  if (tid < B) s_piv[tid] = 0.f;
+  if (tid < 2 * B) (&s_piv[0][0])[tid] = 0.f;
   __syncthreads();
 
-  // block-reduce acc[] (and the pivot row) for column `jn`, exchange with the
-  // cluster through slot[par], and leave the totals in sums[]
-  auto reduce_and_share = [&](float (&acc)[B], int par) {
+  // Block-reduce acc[] (and the pivot row) for the next column, exchange with
+  // the cluster through slot[par], and leave the cluster totals in every
+  // warp's registers: lane c gets tot_dot = x . a_c and tot_piv = a_c[k].
+  // Hazards: red and s_piv[par] are read after the block barrier and written
+  // again only after the next column's cluster barrier (s_piv alternates by
+  // parity, and its reader clears it for the column after next); slot[par]
+  // is rewritten by other CTAs only after they pass the next cluster barrier,
+  // which this CTA reaches after its reads.
+  auto reduce_and_share = [&](float (&acc)[B], int par, float& tot_dot, float& tot_piv) {
     const float part = warp_transpose_sum(acc);
     red[lane][warp] = part;
     __syncthreads();
@@ -258,21 +266,22 @@ __global__ void __launch_bounds__(kPanelThreads)
         t = 0.f;
         for (int w = 0; w < nwarp; ++w) t += red[tid][w];
       } else {
-        t = s_piv[tid - B];
+        t = s_piv[par][tid - B];
+        s_piv[par][tid - B] = 0.f;
       }
       for (int c = 0; c < cs; ++c) *cl.map_shared_rank(&slot[par][crank][tid], c) = t;
     }
     cl.sync();
-    if (tid < 2 * B) {
-      float t = 0.f;
-      for (int c = 0; c < cs; ++c) t += slot[par][c][tid];
-      sums[tid] = t;
-      if (tid >= B) s_piv[tid - B] = 0.f;
+    tot_dot = 0.f;
+    tot_piv = 0.f;
+    for (int c = 0; c < cs; ++c) {
+      tot_dot += slot[par][c][lane];
+      tot_piv += slot[par][c][B + lane];
     }
-    __syncthreads();
   };
 
   // sums for column 0: x_0 . a_c over my elements >= k0, pivot row a_c[k0]
+  float tot_dot, tot_piv;
   {
     float acc[B];
 #pragma unroll
@@ -283,18 +292,17 @@ __global__ void __launch_bounds__(kPanelThreads)
       for (int c = 0; c < B; ++c)
         if (c < bw) acc[c] = fmaf(xn, panel[c * R + (e - e0)], acc[c]);
       if (e == k0)
-        for (int c = 0; c < bw; ++c) s_piv[c] = panel[c * R + (e - e0)];
+        for (int c = 0; c < bw; ++c) s_piv[0][c] = panel[c * R + (e - e0)];
     }
-    __syncthreads();
-    reduce_and_share(acc, 0);
+    reduce_and_share(acc, 0, tot_dot, tot_piv);
   }
 
   const float thr = rtol * (q.tau[0] * qr_range_scale(q.tau[1]));
   int active = bw;
   for (int j = 0; j < bw; ++j) {
     const int k = k0 + j;
-    const float sn = sums[j];
-    const float x0 = sums[B + j];
+    const float sn = __shfl_sync(kFull, tot_dot, j);  // ||x_j||^2
+    const float x0 = __shfl_sync(kFull, tot_piv, j);  // x_j[0] = a_j[k]
     const float nx = sqrtf(sn);
     if (nx <= thr) {  // numerical rank reached: H_k .. are identities
       active = j;
@@ -303,18 +311,19 @@ __global__ void __launch_bounds__(kPanelThreads)
     const float beta = x0 >= 0.f ? -nx : nx;
     const float w0 = x0 - beta;
     const float ww = 2.f * fmaf(fabsf(x0), nx, sn);  // ||x - beta e0||^2, no cancellation
-    if (tid < bw && tid != j) {
-      const float d = sums[tid] - beta * sums[B + tid];  // w_j . a_c
-      if (tid < j) gram[tid][j] = d;
-      else s_coef[tid] = 2.f * d / ww;
+    const float d = tot_dot - beta * tot_piv;         // lane c: w_j . a_c
+    if (warp == 0) {
+      if (lane < j) gram[lane][j] = d;
+      if (lane == 0) {
+        s_ww[j] = ww;
+        s_beta[j] = beta;
+      }
     }
-    if (tid == 0) {
-      s_ww[j] = ww;
-      s_beta[j] = beta;
-      if (k >= e0 && k < e1) panel[j * R + (k - e0)] = w0;
-    }
-    __syncthreads();
+    // the thread that handles element k in the pass below is thread 0
+    if (tid == 0 && k >= e0 && k < e1) panel[j * R + (k - e0)] = w0;
     if (j + 1 == bw) break;  // nothing after the last column
+    w_coef[warp][lane] = 2.f * d / ww;  // lane c > j: column c's coefficient
+    __syncwarp();
 
     // apply H_k to columns j+1.. (my elements >= k) and accumulate column
     // j+1's sums over my elements >= k+1
@@ -322,22 +331,25 @@ __global__ void __launch_bounds__(kPanelThreads)
 #pragma unroll
     for (int c = 0; c < B; ++c) acc[c] = 0.f;
     const float* wr = panel + j * R;
+    const float* coef = w_coef[warp];
+    const int par = (j + 1) & 1;
     for (int e = max(k, e0) + tid; e < e1; e += nthr) {
       const int o = e - e0;
       const float we = wr[o];
-      for (int c = j + 1; c < bw; ++c) panel[c * R + o] -= s_coef[c] * we;
+      for (int c = j + 1; c < bw; ++c) panel[c * R + o] -= coef[c] * we;
       if (e > k) {
         const float xn = panel[(j + 1) * R + o];
 #pragma unroll
         for (int c = 0; c < B; ++c)
           if (c < bw) acc[c] = fmaf(xn, panel[c * R + o], acc[c]);
         if (e == k + 1)
-          for (int c = 0; c < bw; ++c) s_piv[c] = panel[c * R + o];
+          for (int c = 0; c < bw; ++c) s_piv[par][c] = panel[c * R + o];
       }
     }
-    __syncthreads();
-    reduce_and_share(acc, (j + 1) & 1);
+    __syncwarp();  // this warp's coefficients are read: free for the next column
+    reduce_and_share(acc, par, tot_dot, tot_piv);
   }
+  __syncthreads();  // every reflector, gram entry and norm of the panel is written
 
   // Reflectors are stored normalised, v = w / ||w|| (H = I - 2 v v^T), so the
   // triangular factors and Gram matrices built from them are well scaled

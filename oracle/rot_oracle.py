@@ -328,11 +328,12 @@ def hqr_plus_lapack(A: np.ndarray, rank_rtol: float,
     whenever the stop comes by column ncols - 1, as it does when
     ncols > rank(A)); default: all.  Returns (Q, r, beta[0:r]).
     """
-    A = np.asarray(A, dtype=np.float64)
+    dt = np.float32 if np.asarray(A).dtype == np.float32 else np.float64  # float32 runs
+    A = np.asarray(A, dtype=dt)
     p, q = A.shape
     assert p == q, "square input expected"
     if p == 0:
-        return np.eye(0), 0, np.zeros(0)
+        return np.eye(0, dtype=dt), 0, np.zeros(0, dtype=dt)
     tau_abs = rank_rtol * float(np.max(np.linalg.norm(A, axis=0)))
     c = p if ncols is None else max(1, min(p, int(ncols)))
     (qr, tau), R = scipy.linalg.qr(A[:, :c], mode="raw")
@@ -342,16 +343,17 @@ def hqr_plus_lapack(A: np.ndarray, rank_rtol: float,
         if abs(float(diag[k])) <= tau_abs:
             r = k
             break
-    beta = np.array(diag[:r], dtype=np.float64)
-    t = np.array(tau[:r], dtype=np.float64)
+    beta = np.array(diag[:r], dtype=dt)
+    t = np.array(tau[:r], dtype=dt)
     flat = t == 0.0  # zero sub-column: restore the reflection hqr_plus makes
     t[flat] = 2.0
     beta[flat] = -beta[flat]
     if r == 0:
-        return np.eye(p), 0, beta
-    a = np.zeros((p, p), dtype=np.float64, order="F")
+        return np.eye(p, dtype=dt), 0, beta
+    a = np.zeros((p, p), dtype=dt, order="F")
     a[:, :r] = qr[:, :r]
-    Q, _, info = scipy.linalg.lapack.dorgqr(a, t, lwork=max(1, 64 * p))
+    orgqr = scipy.linalg.lapack.sorgqr if dt == np.float32 else scipy.linalg.lapack.dorgqr
+    Q, _, info = orgqr(a, t, lwork=max(1, 64 * p))
     if info != 0:
         raise RuntimeError(f"dorgqr failed ({info})")
     Q = np.array(Q)
@@ -379,9 +381,10 @@ class MatrixState:
     rank_v: int = -1
 
 
-def init_state(m: int, n: int) -> MatrixState:
+def init_state(m: int, n: int, dtype=np.float64) -> MatrixState:
     """M = 0, v = 0, U = I_m, V = I_n."""
-    return MatrixState(M=np.zeros((m, n)), v=np.zeros((m, n)), U=np.eye(m), V=np.eye(n))
+    return MatrixState(M=np.zeros((m, n), dtype=dtype), v=np.zeros((m, n), dtype=dtype),
+                       U=np.eye(m, dtype=dtype), V=np.eye(n, dtype=dtype))
 
 
 def refresh_basis(M: np.ndarray, U: np.ndarray, V: np.ndarray, rank_rtol: float,
@@ -424,16 +427,19 @@ def step(W: np.ndarray, G: np.ndarray, st: MatrixState, beta1: float, beta2: flo
     A_V, the new U and V, G~, M~, v and D.
     """
     p = perturb or (lambda name, X: X)
-    G = np.asarray(G, dtype=np.float64)
-    st.M = p("M", beta1 * st.M + (1.0 - beta1) * G)
+    dt = st.M.dtype  # float64; float32 in the float32 runs (see run())
+    G = np.asarray(G, dtype=dt)
+    beta1, beta2, eps, lr = dt.type(beta1), dt.type(beta2), dt.type(eps), dt.type(lr)
+    one = dt.type(1.0)
+    st.M = p("M", beta1 * st.M + (one - beta1) * G)
     if refresh:
         st.U, st.V, st.rank_u, st.rank_v = refresh_basis(st.M, st.U, st.V, rank_rtol,
                                                          perturb=perturb)
     Gt = p("Gt", (st.U.T @ G) @ st.V)
     Mt = p("Mt", (st.U.T @ st.M) @ st.V)
-    st.v = p("v", beta2 * st.v + (1.0 - beta2) * (Gt * Gt))
+    st.v = p("v", beta2 * st.v + (one - beta2) * (Gt * Gt))
     D = p("D", Mt / (np.sqrt(st.v) + eps))
-    return np.asarray(W, dtype=np.float64) - lr * ((st.U @ D) @ st.V.T)
+    return np.asarray(W, dtype=dt) - lr * ((st.U @ D) @ st.V.T)
 
 
 # ---------------------------------------------------------------------------
@@ -452,7 +458,8 @@ COMPACT_RELS = {"U": 2.0 ** -11, "V": 2.0 ** -11, "M": 2.0 ** -8, "Mt": 2.0 ** -
 def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         first_step: int = 1, perturb_seed: Optional[int] = None,
         perturb_rel: float = FLOOR_REL,
-        perturb_rels: Optional[Dict[str, float]] = None) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
+        perturb_rels: Optional[Dict[str, float]] = None,
+        dtype=np.float64) -> Dict[int, Tuple[np.ndarray, MatrixState]]:
     """Run `steps` steps (default: the workload's) for the chosen matrices.
 
     `wl` is a workload object exposing shapes, hyper, refresh(t), w0(i) and
@@ -465,6 +472,11 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     sensitivity, the floor any float32 implementation faces.  perturb_rels
     gives some quantities (by the names step() uses) another size: the
     rounding of a lower-precision storage format (COMPACT_RELS).
+
+    dtype=np.float32 runs the same steps in float32 arithmetic (float32
+    arrays, float32 BLAS products and LAPACK's float32 Householder routines)
+    and returns its W in float64: what a plain float32 implementation of the
+    method gives, a sensitivity reference.  The oracle proper is float64.
     """
     items = list(range(wl.count)) if items is None else list(items)
     steps = wl.steps if steps is None else steps
@@ -472,8 +484,8 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     out = {}
     for i in items:
         m, n = wl.shapes[i]
-        W = wl.w0(i).astype(np.float64)
-        st = init_state(m, n)
+        W = wl.w0(i).astype(dtype)
+        st = init_state(m, n, dtype)
         perturb = None
         if perturb_seed is not None:
             rng = np.random.default_rng([perturb_seed, i])
@@ -483,7 +495,7 @@ def run(wl, items: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         for t in range(first_step, first_step + steps):
             W = step(W, wl.grad(i, t), st, h.beta1, h.beta2, h.eps, h.lr, wl.refresh(t),
                      h.rank_rtol, perturb=perturb)
-        out[i] = (W, st)
+        out[i] = (np.asarray(W, dtype=np.float64), st)
     return out
 
 
@@ -500,6 +512,13 @@ def floor(wl, item: int, W_ref: np.ndarray, seeds: Sequence[int] = FLOOR_SEEDS,
                     perturb_rels=rels)[item]
         worst = max(worst, float(np.linalg.norm(Wp - W_ref) / np.linalg.norm(W_ref)))
     return worst
+
+
+def float32_error(wl, item: int, W_ref: np.ndarray, steps: Optional[int] = None) -> float:
+    """Relative Frobenius distance between the float64 oracle's final W and
+    the same run computed in plain float32 arithmetic (see run())."""
+    W32, _ = run(wl, [item], steps=steps, dtype=np.float32)[item]
+    return float(np.linalg.norm(W32 - W_ref) / np.linalg.norm(W_ref))
 
 
 def orthogonality_error(Q: np.ndarray) -> float:

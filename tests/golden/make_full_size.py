@@ -13,6 +13,13 @@ For each sampled matrix i of a workload, after the workload's steps:
   floor    the method's float32 floor: the largest relative change of the
            final W over five runs whose stored quantities are perturbed at
            2^-24 (oracle.floor)
+  f32      the relative error, on the same sampled entries, of the same run
+           computed in plain float32 arithmetic (oracle.run(dtype=float32)):
+           what an actual float32 implementation of the method gives
+  floor22  the spread at 2^-22: the largest relative change, on the sampled
+           entries, over five runs whose stored quantities are perturbed at
+           2^-22, the precision of the 22-bit operands (hi + lo, 11 bits
+           each) that three-term tensor-core products read
   rank_u, rank_v   the numerical ranks at the last refresh
 
 The matrices are independent, so each sampled one is run on its own.  The
@@ -21,6 +28,8 @@ matrix per shape, spread over the layers) and one matrix per distinct
 (m, n) of the ragged workload.
 
     python tests/golden/make_full_size.py [workload ...]   # default: all four
+    python tests/golden/make_full_size.py --add-f32 [workload ...]  # add f32 to existing files
+    python tests/golden/make_full_size.py --add-floor22 [workload ...]  # add floor22
 """
 
 import argparse
@@ -91,7 +100,50 @@ def one(wl, i, samples):
     idx = np.sort(rng.choice(m * n, size=s, replace=False)).astype(np.uint32)
     w = W.ravel()[idx]
     return dict(idx=idx, w=w, norm=float(np.linalg.norm(W)), wsamp=float(np.linalg.norm(w)),
-                floor=fl, rank_u=int(st.rank_u), rank_v=int(st.rank_v))
+                floor=fl, f32=f32_error(wl, i, idx, w), floor22=floor22(wl, i, idx, w),
+                rank_u=int(st.rank_u), rank_v=int(st.rank_v))
+
+
+def f32_error(wl, i, idx, w):
+    """The float32 run's relative error on the sampled entries."""
+    W32, _ = orc.run(wl, [i], dtype=np.float32)[i]
+    x = W32.ravel()[idx]
+    return float(np.linalg.norm(x - w) / np.linalg.norm(w))
+
+
+def floor22(wl, i, idx, w, seeds=orc.FLOOR_SEEDS):
+    """The spread at 2^-22 on the sampled entries (see the module docstring)."""
+    worst = 0.0
+    for s in seeds:
+        Wp, _ = orc.run(wl, [i], perturb_seed=s, perturb_rel=2.0 ** -22)[i]
+        worst = max(worst, float(np.linalg.norm(Wp.ravel()[idx] - w) / np.linalg.norm(w)))
+    return worst
+
+
+def add_floor22(name):
+    path = os.path.join(OUT, f"{name}.npz")
+    z = dict(np.load(path))
+    wl = CachedInputs(inputs.workload(name))
+    t0 = time.time()
+    for i in [int(i) for i in z["items"]]:
+        z[f"{i}.floor22"] = floor22(wl, i, z[f"{i}.idx"], z[f"{i}.w"])
+        wl.forget()
+        print(f"{name}[{i}]: spread at 2^-22 {float(z[f'{i}.floor22']):.2e}  "
+              f"[{time.time() - t0:.0f} s]", flush=True)
+    np.savez_compressed(path, **z)
+
+
+def add_f32(name):
+    path = os.path.join(OUT, f"{name}.npz")
+    z = dict(np.load(path))
+    wl = CachedInputs(inputs.workload(name))
+    t0 = time.time()
+    for i in [int(i) for i in z["items"]]:
+        z[f"{i}.f32"] = f32_error(wl, i, z[f"{i}.idx"], z[f"{i}.w"])
+        wl.forget()
+        print(f"{name}[{i}]: float32 run error {float(z[f'{i}.f32']):.2e}, floor "
+              f"{float(z[f'{i}.floor']):.2e}  [{time.time() - t0:.0f} s]", flush=True)
+    np.savez_compressed(path, **z)
 
 
 def make(name):
@@ -108,7 +160,8 @@ def make(name):
         wl.forget()
         for key, val in r.items():
             rec[f"{i}.{key}"] = val
-        print(f"{name}[{i}] {wl0.shapes[i]}: floor {r['floor']:.2e} ranks "
+        print(f"{name}[{i}] {wl0.shapes[i]}: floor {r['floor']:.2e}, float32 run "
+              f"{r['f32']:.2e}, ranks "
               f"({r['rank_u']}, {r['rank_v']})  [{k + 1}/{len(items)}, "
               f"{time.time() - t0:.0f} s]", flush=True)
     os.makedirs(OUT, exist_ok=True)
@@ -118,5 +171,15 @@ def make(name):
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("names", nargs="*", default=["ragged", "block", "full", "slice8b"])
-    for nm in ap.parse_args().names:
-        make(nm)
+    ap.add_argument("--add-f32", action="store_true",
+                    help="add the float32 run's error to existing files")
+    ap.add_argument("--add-floor22", action="store_true",
+                    help="add the spread at 2^-22 to existing files")
+    args = ap.parse_args()
+    for nm in args.names:
+        if args.add_f32:
+            add_f32(nm)
+        elif args.add_floor22:
+            add_floor22(nm)
+        else:
+            make(nm)

@@ -439,3 +439,23 @@ def test_per_quantity_perturbation_sizes():
     only_m = orc.floor(wl, 1, W, rel=0.0, rels={"M": 2.0 ** -12})
     only_m16 = orc.floor(wl, 1, W, rel=0.0, rels={"M": 2.0 ** -8})
     assert 14.0 < only_m16 / only_m < 18.0
+
+
+def test_float32_run_is_a_float32_execution_of_the_same_steps():
+    """run(dtype=float32) keeps every array in float32 and lands within a few
+    units of float32 rounding of the float64 run where the steps are smooth
+    (plain Adam, no refresh: each step adds one rounding of W's size); with
+    refreshes it stays close but not exact."""
+    u = 2.0 ** -24
+    wl = _small_workload(5, 100)
+    W, _ = orc.run(wl, [1])[1]
+    W32, st = orc.run(wl, [1], dtype=np.float32)[1]
+    assert st.M.dtype == np.float32 and st.U.dtype == np.float32
+    e = np.linalg.norm(W32 - W) / np.linalg.norm(W)
+    assert 0 < e < 8 * u
+    wl = _small_workload(6, 2)
+    W, st64 = orc.run(wl, [0])[0]
+    W32, st32 = orc.run(wl, [0], dtype=np.float32)[0]
+    assert (st32.rank_u, st32.rank_v) == (st64.rank_u, st64.rank_v)
+    assert 0 < orc.float32_error(wl, 0, W) < 1e-3
+    assert orc.orthogonality_error(st32.U.astype(np.float64)) < 1e-5
