@@ -491,24 +491,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // of the result) are issued first and the four hi*hi MMAs last, so only those
 // four adds truncate at the result's magnitude.  (Accumulating two or four
 // K blocks per buffer instead measured 2.8x / 6x the error.)
-// The running sum over the K/32 blocks is compensated (Kahan, "Further
-// remarks on reducing truncation errors", CACM 1965): each addition's
-// rounding error is carried into the next, so the sum's error stays at a few
+// The sum over the K/32 blocks is taken in two levels.  Each epilogue thread
+// adds the block partials of each 16-column piece in registers (a plain
+// float32 sum of up to four terms) and every four blocks adds that group sum
+// into a running sum held in TMEM with compensation (Kahan, "Further remarks
+// on reducing truncation errors", CACM 1965): the group sum's rounding error
+// is carried into the next fold, so the running sum's error stays at a few
 // units in the last place whatever K is, instead of growing like sqrt(K/32).
-// Measured relative error of a product with K = 6144 / 12288: 1.33e-7 /
-// 1.33e-7 compensated, 2.8e-7 / 3.8e-7 plain; it took the worst
-// ||U^T U - I||_F of the 12288 x 12288 bases from 1.07e-4 to 5.7e-5.
-// The running sums live in TMEM, the compensations in registers.
-// TMEM: 3 K-block buffers x 128 columns, then the tile's 128 x 128 running
-// sums (columns 384..511).  Eight epilogue warps: warp w owns TMEM lanes
-// 32 (w % 4) .. +31 and columns 64 ((w - 2) / 4) .. +63 of each region.
+// Measured relative error of a product with K = 6144 / 12288: 1.33e-7 with
+// compensation, 2.8e-7 / 3.8e-7 with a plain float32 sum of the blocks.
+// The four pieces are folded in turn (piece q after blocks q, q + 4, ...),
+// so each block costs one TMEM load and one add per element plus one
+// piece's fold, and no block stalls the MMAs behind a long fold.
+// TMEM: 2 K-block buffers x 128 columns, then the tile's 128 x 128 running
+// sums (columns 256..383) and their compensations (384..511).  Eight
+// epilogue warps: warp w owns TMEM lanes 32 (w % 4) .. +31 and columns
+// 64 ((w - 2) / 4) .. +63 of each region.
+// Short products (SHORT: every K <= kPreciseShortK, at most 16 blocks, the
+// QR's rank-256 updates and their factors) keep the whole sum in registers,
+// a plain float32 sum of the blocks, and use the four TMEM buffers so that
+// the MMAs run three blocks ahead while the epilogue finishes a tile.
 // ---------------------------------------------------------------------------
 
 constexpr int kThreadsPrecise = 320;
-constexpr int kPreciseBufs = 3;
+constexpr int kPreciseBufs = 2;
 constexpr int kPreciseEpiWarps = 8;
-constexpr int kPreciseCols = 64;          // columns per epilogue warp
-constexpr uint32_t kPreciseSumCol = 384;  // first TMEM column of the running sums
+constexpr int kPreciseCols = 64;           // columns per epilogue warp
+constexpr int kPreciseGroup = kPreciseCols / 16;  // K blocks summed in registers between folds
+constexpr uint32_t kPreciseSumCol = 256;   // first TMEM column of the running sums
+constexpr uint32_t kPreciseCompCol = 384;  // first TMEM column of their compensations
+constexpr int kPreciseShortK = 512;        // the SHORT variant's largest K
 
 // s + x with the rounding error carried in c (Kahan): returns the new s.
 __device__ __forceinline__ float kahan_add(float s, float x, float& c) {
@@ -518,22 +530,22 @@ __device__ __forceinline__ float kahan_add(float s, float x, float& c) {
   return t;
 }
 
-template <int STAGES>
+template <int STAGES, bool SHORT>
 __global__ void __launch_bounds__(kThreadsPrecise, 1)
     gemm_tc_precise_kernel(const __grid_constant__ TcBatch b) {
   constexpr int BN = 128;
-  constexpr int kHalf = BN / 2;  // columns per epilogue warp
+  constexpr int kBufs = SHORT ? 4 : kPreciseBufs;
   using C = Cfg<BN, STAGES, true>;
   constexpr uint32_t kCols = 512;
-  static_assert((2 * STAGES + 2 * kPreciseBufs + 1) * 8 + 8 <= 256, "barrier area");
+  static_assert((2 * STAGES + 2 * kBufs + 1) * 8 + 8 <= 256, "barrier area");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + kPreciseBufs;
-  uint64_t* drain = tempty + kPreciseBufs;
+  uint64_t* tempty = tfull + kBufs;
+  uint64_t* drain = tempty + kBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -545,7 +557,7 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < kPreciseBufs; ++a) {
+    for (int a = 0; a < kBufs; ++a) {
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], kPreciseEpiWarps);
     }
@@ -612,7 +624,7 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       decode(b, tile, pi, m0, nt);
       const int kblocks = (b.p[pi].K + BK - 1) / BK;
       for (int kb = 0; kb < kblocks; ++kb, ++chunk) {
-        const uint32_t buf = chunk % kPreciseBufs, use = chunk / kPreciseBufs;
+        const uint32_t buf = chunk % kBufs, use = chunk / kBufs;
         if (!ptx::mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, limit) ||
             !ptx::mbar_wait(&full[stage], phase, abort_flag, limit)) {
           ok = false;
@@ -652,6 +664,7 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
     const int colgrp = (warp - 2) >> 2;  // columns 64 colgrp .. +63 of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t sums = tmem_base + lane_off + kPreciseSumCol + colgrp * kPreciseCols;
+    const uint32_t comps = tmem_base + lane_off + kPreciseCompCol + colgrp * kPreciseCols;
     uint32_t chunk = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
@@ -660,49 +673,105 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       const TcProblem& P = b.p[pi];
       const int n0 = nt * BN;
       const int kblocks = (P.K + BK - 1) / BK;
-      float comp[kPreciseCols];
+      // grp: per 16-column piece, the sum of the blocks since the piece's
+      // last fold.  Piece q is folded after blocks q, q + 4, q + 8, ... so
+      // that every block carries one piece's fold.
+      float grp[kPreciseCols];
 #pragma unroll
-      for (int c = 0; c < kPreciseCols; ++c) comp[c] = 0.f;
+      for (int c = 0; c < kPreciseCols; ++c) grp[c] = 0.f;
+      {  // the apply modes read C after the last block: bring it into L2 now
+        const int prow = m0 + quarter * 32 + lane, pcol = n0 + colgrp * kPreciseCols;
+        if ((P.epi == kEpiApply || P.epi == kEpiApplySplit) && prow < P.M && pcol < P.N) {
+          const int last = min(P.N - 1, pcol + kPreciseCols - 1) - pcol;
+          const int64_t o = (int64_t)prow * P.ldc + pcol;
+#pragma unroll
+          for (int c = 0; c < kPreciseCols; c += 32) {
+            ptx::prefetch_l2(P.c_hi + o + min(c, last));
+            if (P.epi == kEpiApplySplit) ptx::prefetch_l2(P.c_lo + o + min(c, last));
+          }
+          ptx::prefetch_l2(P.c_hi + o + last);
+          if (P.epi == kEpiApplySplit) ptx::prefetch_l2(P.c_lo + o + last);
+        }
+      }
       for (int kb = 0; kb < kblocks; ++kb, ++chunk) {
-        const uint32_t buf = chunk % kPreciseBufs, use = chunk / kPreciseBufs;
+        const uint32_t buf = chunk % kBufs, use = chunk / kBufs;
         if (!ptx::mbar_wait(&tfull[buf], use & 1u, abort_flag, limit)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t t = tmem_base + lane_off + buf * BN + colgrp * kPreciseCols;
-        // 16-column pieces: block partial x and running sum s in, s out
+        // the block partial, 16 columns at a time, into the group sums
 #pragma unroll
-        for (int h = 0; h < kPreciseCols / 16; ++h) {
-          uint32_t x[16], sm[16];
-          ptx::tmem_ld_32x32b_x16(t + 16 * h, x);
-          if (kb > 0) ptx::tmem_ld_32x32b_x16(sums + 16 * h, sm);
+        for (int q = 0; q < kPreciseCols / 16; ++q) {
+          uint32_t x[16];
+          ptx::tmem_ld_32x32b_x16(t + 16 * q, x);
           ptx::tmem_wait_ld();
-          if (h == kPreciseCols / 16 - 1) {  // the block buffer is read: release it
+          if (q == kPreciseCols / 16 - 1) {  // the block buffer is read: release it
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
           }
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float prev = kb > 0 ? __uint_as_float(sm[c]) : 0.f;
-            sm[c] = __float_as_uint(kahan_add(prev, __uint_as_float(x[c]), comp[16 * h + c]));
-          }
-          ptx::tmem_st_32x32b_x16(sums + 16 * h, sm);
+          for (int c = 0; c < 16; ++c) grp[16 * q + c] += __uint_as_float(x[c]);
         }
-        ptx::tmem_wait_st();  // the next block's loads of s see these stores
+        if (SHORT) continue;  // the whole sum stays in registers
+        // fold piece kb % 4 into the compensated running sum
+        const int fq = kb % kPreciseGroup;
+#pragma unroll
+        for (int q = 0; q < kPreciseCols / 16; ++q) {
+          if (q != fq) continue;
+          uint32_t sv[16], cv[16];
+          if (kb >= kPreciseGroup) {  // the piece has been folded before
+            ptx::tmem_wait_st();      // (its stores, four blocks ago, are done)
+            ptx::tmem_ld_32x32b_x16(sums + 16 * q, sv);
+            ptx::tmem_ld_32x32b_x16(comps + 16 * q, cv);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              float comp = __uint_as_float(cv[c]);
+              sv[c] = __float_as_uint(kahan_add(__uint_as_float(sv[c]), grp[16 * q + c], comp));
+              cv[c] = __float_as_uint(comp);
+            }
+          } else {  // first fold: sum = group sum, compensation 0
+            // (written 0 x group sum: a literal zero here makes the compiler
+            // hold sixteen zero registers across the whole K loop)
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              sv[c] = __float_as_uint(grp[16 * q + c]);
+              cv[c] = __float_as_uint(0.f * grp[16 * q + c]);
+            }
+          }
+          ptx::tmem_st_32x32b_x16(sums + 16 * q, sv);
+          ptx::tmem_st_32x32b_x16(comps + 16 * q, cv);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) grp[16 * q + c] = 0.f;
+        }
       }
       if (!ok) break;
+      // the blocks since each piece's last fold complete its sum, in place
+      if (!SHORT) ptx::tmem_wait_st();
+#pragma unroll
+      for (int q = 0; q < kPreciseCols / 16; ++q) {
+        if (SHORT || kblocks <= q) continue;  // never folded: grp holds the whole sum
+        uint32_t sv[16], cv[16];
+        ptx::tmem_ld_32x32b_x16(sums + 16 * q, sv);
+        ptx::tmem_ld_32x32b_x16(comps + 16 * q, cv);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float comp = __uint_as_float(cv[c]);
+          const float sum = kahan_add(__uint_as_float(sv[c]), grp[16 * q + c], comp);
+          grp[16 * q + c] = sum - comp;  // the compensated sum
+        }
+      }
       const int row = m0 + quarter * 32 + lane;
 #pragma unroll
       for (int q = 0; q < kPreciseCols / 32; ++q) {
         const int col0 = n0 + colgrp * kPreciseCols + q * 32;
         uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(sums + 32 * q, r);
-        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c)  // the compensated sums
-          r[c] = __float_as_uint(__uint_as_float(r[c]) - comp[32 * q + c]);
+        for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(grp[32 * q + c]);
         if (col0 < P.N) store_chunk(P, row, col0, r);
       }
     }
@@ -764,16 +833,30 @@ int num_sms() {
   return n;
 }
 
+using TcKernel = void (*)(TcBatch);
+
+// The kernel of a launch configuration (the precise variants only where asked
+// for, so that no unused configuration is compiled).
+template <int BN, int STAGES, bool SPLIT3, bool PRECISE, bool F16, bool SHORT>
+TcKernel pick_kernel() {
+  if constexpr (PRECISE)
+    return gemm_tc_precise_kernel<STAGES, SHORT>;
+  else
+    return gemm_tc_kernel<BN, STAGES, SPLIT3, F16>;
+}
+
 template <int BN, int STAGES, bool SPLIT3, bool PRECISE = false, bool F16 = false>
 int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
   using C = Cfg<BN, STAGES, SPLIT3>;
   static_assert(!PRECISE || (BN == 128 && SPLIT3 && !F16), "precise variant is 3xTF32, BN = 128");
-  auto kernel =
-      PRECISE ? gemm_tc_precise_kernel<STAGES> : gemm_tc_kernel<BN, STAGES, SPLIT3, F16>;
+  const TcKernel kernel = pick_kernel<BN, STAGES, SPLIT3, PRECISE, F16, false>();
+  const TcKernel kernel_short = pick_kernel<BN, STAGES, SPLIT3, PRECISE, F16, true>();
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(kernel_short, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmem) != cudaSuccess)
       return ROT_ECUDA;
     attr = true;
   }
@@ -782,7 +865,7 @@ int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
   size_t i = 0;
   while (i < probs.size()) {
     std::memset(&b, 0, sizeof(b));
-    int total = 0;
+    int total = 0, kmax = 0;
     double flops = 0.0;
     while (i < probs.size() && b.count < kMaxP) {
       const GemmProblem& G = probs[i++];
@@ -812,6 +895,7 @@ int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
       P.out_r = G.out_r;
       P.c0 = G.c0;
       total += ((G.M + BM - 1) / BM) * P.tiles_n;
+      kmax = std::max(kmax, G.K);
       flops += 2.0 * G.M * (double)G.N * G.K;
       ++b.count;
     }
@@ -823,7 +907,8 @@ int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
     {
       ProfScope prof(PRECISE ? ROT_PROF_GEMM_PRECISE : (F16 ? ROT_PROF_GEMM_F16 : ROT_PROF_GEMM),
                      flops, stream);
-      kernel<<<grid, PRECISE ? kThreadsPrecise : kThreads, C::kSmem, stream>>>(b);
+      const TcKernel k = (PRECISE && kmax <= kPreciseShortK) ? kernel_short : kernel;
+      k<<<grid, PRECISE ? kThreadsPrecise : kThreads, C::kSmem, stream>>>(b);
     }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
   }

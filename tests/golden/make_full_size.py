@@ -30,6 +30,14 @@ matrix per shape, spread over the layers) and one matrix per distinct
     python tests/golden/make_full_size.py [workload ...]   # default: all four
     python tests/golden/make_full_size.py --add-f32 [workload ...]  # add f32 to existing files
     python tests/golden/make_full_size.py --add-floor22 [workload ...]  # add floor22
+    python tests/golden/make_full_size.py slice8b --items 4 27 --seeds 3  # some matrices
+    python tests/golden/make_full_size.py slice8b --merge a.npz b.npz  # join partial files
+
+Each matrix's record is merged into the workload's file as soon as it is
+computed (so a long run can be split over processes: --items, --out).  The
+floor and the 2^-22 spread take the largest change over --seeds oracle runs
+(default five).  The Qwen3-8B-shaped slice samples one matrix per distinct
+shape (k, q, gate, down) and the second matrix of the k/v and q/o pairs.
 """
 
 import argparse
@@ -55,8 +63,8 @@ PLAN = {
     # one per shape kind, spread over the 28 layers: L0.k, L13.v, L27.q,
     # L5.o, L20.gate, L9.up, L14.down
     "full": ([1, 7 * 13 + 2, 7 * 27 + 0, 7 * 5 + 3, 7 * 20 + 4, 7 * 9 + 5, 7 * 14 + 6], 8192),
-    # L0.k, L1.v, L3.q, L2.o, L0.gate, L1.up, L3.down
-    "slice8b": ([1, 7 + 2, 21 + 0, 14 + 3, 4, 7 + 5, 21 + 6], 8192),
+    # L0.k, L1.v, L3.q, L2.o, L0.gate, L3.down (up has gate's shape and path)
+    "slice8b": ([1, 7 + 2, 21 + 0, 14 + 3, 4, 21 + 6], 8192),
     # filled in by ragged_items(): first matrix of each distinct (m, n)
     "ragged": (None, 1024),
 }
@@ -91,16 +99,16 @@ class CachedInputs:
         self._g.clear()
 
 
-def one(wl, i, samples):
+def one(wl, i, samples, seeds=orc.FLOOR_SEEDS):
     m, n = wl.shapes[i]
     W, st = orc.run(wl, [i])[i]
-    fl = orc.floor(wl, i, W)
+    fl = orc.floor(wl, i, W, seeds=seeds)
     rng = np.random.default_rng([20260, wl.seed, i])
     s = min(samples, m * n)
     idx = np.sort(rng.choice(m * n, size=s, replace=False)).astype(np.uint32)
     w = W.ravel()[idx]
     return dict(idx=idx, w=w, norm=float(np.linalg.norm(W)), wsamp=float(np.linalg.norm(w)),
-                floor=fl, f32=f32_error(wl, i, idx, w), floor22=floor22(wl, i, idx, w),
+                floor=fl, f32=f32_error(wl, i, idx, w), floor22=floor22(wl, i, idx, w, seeds),
                 rank_u=int(st.rank_u), rank_v=int(st.rank_v))
 
 
@@ -146,26 +154,35 @@ def add_f32(name):
     np.savez_compressed(path, **z)
 
 
-def make(name):
+def merge(path, wl0, i, r):
+    """Add matrix i's record to the file (created if absent)."""
+    z = dict(np.load(path)) if os.path.exists(path) else {
+        "items": np.zeros(0, dtype=np.int32), "steps": wl0.steps,
+        "refresh_every": wl0.refresh_every, "seed": wl0.seed}
+    z["items"] = np.array(sorted(set(int(k) for k in z["items"]) | {i}), dtype=np.int32)
+    for key, val in r.items():
+        z[f"{i}.{key}"] = val
+    np.savez_compressed(path + ".tmp.npz", **z)
+    os.replace(path + ".tmp.npz", path)
+
+
+def make(name, items=None, seeds=orc.FLOOR_SEEDS, out=None):
     wl0 = inputs.workload(name)
-    items, samples = PLAN[name]
+    planned, samples = PLAN[name]
     if items is None:
-        items = ragged_items(wl0)
+        items = planned if planned is not None else ragged_items(wl0)
     wl = CachedInputs(wl0)
-    rec = {"items": np.array(items, dtype=np.int32), "steps": wl0.steps,
-           "refresh_every": wl0.refresh_every, "seed": wl0.seed}
+    os.makedirs(OUT, exist_ok=True)
+    path = out or os.path.join(OUT, f"{name}.npz")
     t0 = time.time()
     for k, i in enumerate(items):
-        r = one(wl, i, samples)
+        r = one(wl, i, samples, seeds)
         wl.forget()
-        for key, val in r.items():
-            rec[f"{i}.{key}"] = val
+        merge(path, wl0, i, r)
         print(f"{name}[{i}] {wl0.shapes[i]}: floor {r['floor']:.2e}, float32 run "
-              f"{r['f32']:.2e}, ranks "
+              f"{r['f32']:.2e}, spread at 2^-22 {r['floor22']:.2e}, ranks "
               f"({r['rank_u']}, {r['rank_v']})  [{k + 1}/{len(items)}, "
               f"{time.time() - t0:.0f} s]", flush=True)
-    os.makedirs(OUT, exist_ok=True)
-    np.savez_compressed(os.path.join(OUT, f"{name}.npz"), **rec)
 
 
 if __name__ == "__main__":
@@ -175,11 +192,24 @@ if __name__ == "__main__":
                     help="add the float32 run's error to existing files")
     ap.add_argument("--add-floor22", action="store_true",
                     help="add the spread at 2^-22 to existing files")
+    ap.add_argument("--items", type=int, nargs="*", help="these matrices only")
+    ap.add_argument("--seeds", type=int, default=len(orc.FLOOR_SEEDS),
+                    help="oracle runs for the floor and the 2^-22 spread")
+    ap.add_argument("--out", help="write to this file instead of the workload's")
+    ap.add_argument("--merge", nargs="*", help="merge these files' records into the workload's")
     args = ap.parse_args()
+    seeds = tuple(range(1, args.seeds + 1))
     for nm in args.names:
-        if args.add_f32:
+        if args.merge:
+            wl0 = inputs.workload(nm)
+            for f in args.merge:
+                z = np.load(f)
+                for i in (int(k) for k in z["items"]):
+                    merge(os.path.join(OUT, f"{nm}.npz"), wl0, i,
+                          {k.split(".", 1)[1]: z[k] for k in z.files if k.startswith(f"{i}.")})
+        elif args.add_f32:
             add_f32(nm)
         elif args.add_floor22:
             add_floor22(nm)
         else:
-            make(nm)
+            make(nm, args.items, seeds, args.out)

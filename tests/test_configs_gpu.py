@@ -91,9 +91,9 @@ def reference(name):
     for i in items:
         rec[i] = {k: z[f"{i}.{k}"] for k in ("idx", "w", "norm", "wsamp", "floor", "rank_u",
                                              "rank_v")}
-        # measured where a matrix can miss the bar; absent: 0 (a miss is then "over")
+        # measured where a matrix can miss the bar; absent: None (a miss is then "over")
         for k in ("f32", "floor22"):
-            rec[i][k] = z[f"{i}.{k}"] if f"{i}.{k}" in z.files else 0.0
+            rec[i][k] = float(z[f"{i}.{k}"]) if f"{i}.{k}" in z.files else None
     return items, rec
 
 
@@ -177,16 +177,16 @@ def evaluate(name, precision):
             idx = torch.from_numpy(rec[i]["idx"].astype(np.int64)).cuda()
             x = W[i].reshape(-1)[idx].double().cpu().numpy()
             e = float(np.linalg.norm(x - rec[i]["w"]) / float(rec[i]["wsamp"]))
-            fl, f32 = float(rec[i]["floor"]), float(rec[i]["f32"])
-            f22 = float(rec[i]["floor22"])
+            fl, f32, f22 = float(rec[i]["floor"]), rec[i]["f32"], rec[i]["floor22"]
             how = f"{len(idx)} sampled entries"
-        F = max(fl, f32)
-        st = status(e, bar, F, f22)
+        F = max(fl, f32 or 0.0)
+        st = status(e, bar, F, f22 or 0.0)
         m, n = wl.shapes[i]
         label = wl.names[i] if hasattr(wl, "names") else str(i)
+        meas = lambda x: "not measured" if x is None else f"{x:.2e}"
         fl_txt = ("" if fl == float("inf") else
-                  f", float32: perturbation floor {fl:.2e}, float32 run {f32:.2e} "
-                  f"(GPU / float32 = {e / F:.2f}), spread at 2^-22 {f22:.2e}")
+                  f", float32: perturbation floor {fl:.2e}, float32 run {meas(f32)} "
+                  f"(GPU / float32 = {e / F:.2f}), spread at 2^-22 {meas(f22)}")
         log(f"{name}[{i}] {label} {m}x{n} {NAMES[precision]}: W rel err {e:.2e} ({how}); "
             f"bar {bar:.0e}{fl_txt} -> {st}")
         out.append((i, e, F, st))
