@@ -483,6 +483,114 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
+// Row-major output through shared memory.  In store_chunk lane l of a warp
+// holds row row0 + l, so each of the warp's accesses touches 32 rows (16
+// bytes of each).  Here the warp's 32 x 32 chunk goes through a padded
+// staging area (row stride 33 floats: both the write and the read are free of
+// bank conflicts) and comes back one row at a time, lane l holding column
+// col0 + l: every global access of the warp is 32 consecutive elements.  The
+// apply modes issue the loads of eight rows before their stores.  Row-major
+// modes only (the transposed ones are already row-contiguous per warp).
+// ---------------------------------------------------------------------------
+
+constexpr int kStageStride = 33;  // floats per staged row
+constexpr int kStageFloats = 32 * kStageStride;
+
+__device__ __forceinline__ bool rows_path(int epi) {
+  return epi == kEpiStoreSplit || epi == kEpiStoreF32 || epi == kEpiApply ||
+         epi == kEpiApplySplit || epi == kEpiStoreBF16;
+}
+
+__device__ __forceinline__ void store_chunk_rows(const TcProblem& P, int row0, int col0,
+                                                 const uint32_t (&r)[32], float* stage) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) stage[lane * kStageStride + c] = __uint_as_float(r[c]);
+  __syncwarp();
+  const int col = col0 + lane;
+  const bool cok = col < P.N;
+  const int nrow = min(32, P.M - row0);
+  const float alpha = P.alpha;
+  switch (P.epi) {
+    case kEpiStoreSplit:
+    case kEpiStoreF32: {
+      const bool split = P.epi == kEpiStoreSplit;
+      for (int i = 0; i < nrow; ++i) {
+        const float v = stage[i * kStageStride + lane];
+        if (!cok) continue;
+        const int64_t o = (int64_t)(row0 + i) * P.ldc + col;
+        if (split) {
+          float h, l;
+          if (P.mma_only) {
+            split_tf32_mma(v, h, l);
+          } else {
+            split_tf32(v, h, l);
+          }
+          P.c_hi[o] = h;
+          P.c_lo[o] = l;
+        } else {
+          P.c_hi[o] = v;
+        }
+      }
+      break;
+    }
+    case kEpiStoreBF16: {
+      __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(P.c_hi);
+      for (int i = 0; i < nrow; ++i)
+        if (cok)
+          c[(int64_t)(row0 + i) * P.ldc + col] = __float2bfloat16_rn(stage[i * kStageStride + lane]);
+      break;
+    }
+    case kEpiApply: {
+      for (int i0 = 0; i0 < nrow; i0 += 8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u;
+          x[u] = (cok && i < nrow) ? P.c_hi[(int64_t)(row0 + i) * P.ldc + col] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u;
+          if (cok && i < nrow)
+            P.c_hi[(int64_t)(row0 + i) * P.ldc + col] =
+                x[u] - alpha * stage[i * kStageStride + lane];
+        }
+      }
+      break;
+    }
+    case kEpiApplySplit: {
+      for (int i0 = 0; i0 < nrow; i0 += 8) {
+        float h[8], l[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u;
+          const int64_t o = (int64_t)(row0 + i) * P.ldc + col;
+          const bool ok = cok && i < nrow;
+          h[u] = ok ? P.c_hi[o] : 0.f;
+          l[u] = ok ? P.c_lo[o] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u;
+          if (cok && i < nrow) {
+            const int64_t o = (int64_t)(row0 + i) * P.ldc + col;
+            float hh, ll;
+            split_tf32((h[u] + l[u]) - alpha * stage[i * kStageStride + lane], hh, ll);
+            P.c_hi[o] = hh;
+            P.c_lo[o] = ll;
+          }
+        }
+      }
+      break;
+    }
+    default:
+      break;
+  }
+  __syncwarp();  // the staging area is read before the next chunk rewrites it
+}
+
+// ---------------------------------------------------------------------------
 // Precise 3xTF32 variant (BN = 128).  The tensor cores truncate every partial
 // sum they add into a TMEM accumulator, an error that grows with K and that
 // cancellation (a - Y T Y^T a with a small result) then magnifies.  Here each
@@ -548,6 +656,8 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
   uint64_t* drain = tempty + kBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // row-major output staging, one area per epilogue warp, after the barriers
+  float* stage_area = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t limit = b.limit_ns;
@@ -701,19 +811,20 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
         }
         ptx::tc_fence_after();
         const uint32_t t = tmem_base + lane_off + buf * BN + colgrp * kPreciseCols;
-        // the block partial, 16 columns at a time, into the group sums
-#pragma unroll
-        for (int q = 0; q < kPreciseCols / 16; ++q) {
-          uint32_t x[16];
-          ptx::tmem_ld_32x32b_x16(t + 16 * q, x);
+        // the block partial (one TMEM round trip) into the group sums
+        {
+          uint32_t xa[32], xb[32];
+          ptx::tmem_ld_32x32b_x32(t, xa);
+          ptx::tmem_ld_32x32b_x32(t + 32, xb);
           ptx::tmem_wait_ld();
-          if (q == kPreciseCols / 16 - 1) {  // the block buffer is read: release it
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
-          }
+          ptx::tc_fence_before();  // the block buffer is read: release it
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) grp[16 * q + c] += __uint_as_float(x[c]);
+          for (int c = 0; c < 32; ++c) {
+            grp[c] += __uint_as_float(xa[c]);
+            grp[32 + c] += __uint_as_float(xb[c]);
+          }
         }
         if (SHORT) continue;  // the whole sum stays in registers
         // fold piece kb % 4 into the compensated running sum
@@ -766,13 +877,20 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
         }
       }
       const int row = m0 + quarter * 32 + lane;
+      float* stage = stage_area + (warp - 2) * kStageFloats;
 #pragma unroll
       for (int q = 0; q < kPreciseCols / 32; ++q) {
         const int col0 = n0 + colgrp * kPreciseCols + q * 32;
         uint32_t r[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(grp[32 * q + c]);
-        if (col0 < P.N) store_chunk(P, row, col0, r);
+        if (col0 < P.N) {
+          if (rows_path(P.epi)) {
+            store_chunk_rows(P, m0 + quarter * 32, col0, r, stage);
+          } else {
+            store_chunk(P, row, col0, r);
+          }
+        }
       }
     }
   }
@@ -848,15 +966,19 @@ TcKernel pick_kernel() {
 template <int BN, int STAGES, bool SPLIT3, bool PRECISE = false, bool F16 = false>
 int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
   using C = Cfg<BN, STAGES, SPLIT3>;
+  // the precise kernel also stages its row-major output (one area per epilogue warp)
+  constexpr int kSmem =
+      C::kSmem + (PRECISE ? kPreciseEpiWarps * kStageFloats * (int)sizeof(float) : 0);
+  static_assert(kSmem <= 232448, "dynamic shared memory above 227 KB");
   static_assert(!PRECISE || (BN == 128 && SPLIT3 && !F16), "precise variant is 3xTF32, BN = 128");
   const TcKernel kernel = pick_kernel<BN, STAGES, SPLIT3, PRECISE, F16, false>();
   const TcKernel kernel_short = pick_kernel<BN, STAGES, SPLIT3, PRECISE, F16, true>();
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kernel_short, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmem) != cudaSuccess)
+                             kSmem) != cudaSuccess)
       return ROT_ECUDA;
     attr = true;
   }
@@ -908,7 +1030,7 @@ int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
       ProfScope prof(PRECISE ? ROT_PROF_GEMM_PRECISE : (F16 ? ROT_PROF_GEMM_F16 : ROT_PROF_GEMM),
                      flops, stream);
       const TcKernel k = (PRECISE && kmax <= kPreciseShortK) ? kernel_short : kernel;
-      k<<<grid, PRECISE ? kThreadsPrecise : kThreads, C::kSmem, stream>>>(b);
+      k<<<grid, PRECISE ? kThreadsPrecise : kThreads, kSmem, stream>>>(b);
     }
     if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
   }

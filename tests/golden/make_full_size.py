@@ -99,7 +99,7 @@ class CachedInputs:
         self._g.clear()
 
 
-def one(wl, i, samples, seeds=orc.FLOOR_SEEDS):
+def one(wl, i, samples, seeds=orc.FLOOR_SEEDS, with_floor22=True):
     m, n = wl.shapes[i]
     W, st = orc.run(wl, [i])[i]
     fl = orc.floor(wl, i, W, seeds=seeds)
@@ -107,9 +107,12 @@ def one(wl, i, samples, seeds=orc.FLOOR_SEEDS):
     s = min(samples, m * n)
     idx = np.sort(rng.choice(m * n, size=s, replace=False)).astype(np.uint32)
     w = W.ravel()[idx]
-    return dict(idx=idx, w=w, norm=float(np.linalg.norm(W)), wsamp=float(np.linalg.norm(w)),
-                floor=fl, f32=f32_error(wl, i, idx, w), floor22=floor22(wl, i, idx, w, seeds),
-                rank_u=int(st.rank_u), rank_v=int(st.rank_v))
+    r = dict(idx=idx, w=w, norm=float(np.linalg.norm(W)), wsamp=float(np.linalg.norm(w)),
+             floor=fl, f32=f32_error(wl, i, idx, w),
+             rank_u=int(st.rank_u), rank_v=int(st.rank_v))
+    if with_floor22:
+        r["floor22"] = floor22(wl, i, idx, w, seeds)
+    return r
 
 
 def f32_error(wl, i, idx, w):
@@ -166,7 +169,7 @@ def merge(path, wl0, i, r):
     os.replace(path + ".tmp.npz", path)
 
 
-def make(name, items=None, seeds=orc.FLOOR_SEEDS, out=None):
+def make(name, items=None, seeds=orc.FLOOR_SEEDS, out=None, with_floor22=True):
     wl0 = inputs.workload(name)
     planned, samples = PLAN[name]
     if items is None:
@@ -176,11 +179,11 @@ def make(name, items=None, seeds=orc.FLOOR_SEEDS, out=None):
     path = out or os.path.join(OUT, f"{name}.npz")
     t0 = time.time()
     for k, i in enumerate(items):
-        r = one(wl, i, samples, seeds)
+        r = one(wl, i, samples, seeds, with_floor22)
         wl.forget()
         merge(path, wl0, i, r)
         print(f"{name}[{i}] {wl0.shapes[i]}: floor {r['floor']:.2e}, float32 run "
-              f"{r['f32']:.2e}, spread at 2^-22 {r['floor22']:.2e}, ranks "
+              f"{r['f32']:.2e}, spread at 2^-22 {r.get('floor22', float('nan')):.2e}, ranks "
               f"({r['rank_u']}, {r['rank_v']})  [{k + 1}/{len(items)}, "
               f"{time.time() - t0:.0f} s]", flush=True)
 
@@ -197,6 +200,8 @@ if __name__ == "__main__":
                     help="oracle runs for the floor and the 2^-22 spread")
     ap.add_argument("--out", help="write to this file instead of the workload's")
     ap.add_argument("--merge", nargs="*", help="merge these files' records into the workload's")
+    ap.add_argument("--no-floor22", action="store_true",
+                    help="skip the spread at 2^-22 (the test then bounds by 4 x float32's)")
     args = ap.parse_args()
     seeds = tuple(range(1, args.seeds + 1))
     for nm in args.names:
@@ -212,4 +217,4 @@ if __name__ == "__main__":
         elif args.add_floor22:
             add_floor22(nm)
         else:
-            make(nm, args.items, seeds, args.out)
+            make(nm, args.items, seeds, args.out, not args.no_floor22)
