@@ -489,7 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // staging area (row stride 33 floats: both the write and the read are free of
 // bank conflicts) and comes back one row at a time, lane l holding column
 // col0 + l: every global access of the warp is 32 consecutive elements.  The
-// apply modes issue the loads of eight rows before their stores.  Row-major
+// apply modes issue the loads of eight rows (sixteen for the split) before
+// their stores.  Row-major
 // modes only (the transposed ones are already row-contiguous per warp).
 // ---------------------------------------------------------------------------
 
@@ -560,10 +561,10 @@ __device__ __forceinline__ void store_chunk_rows(const TcProblem& P, int row0, i
       break;
     }
     case kEpiApplySplit: {
-      for (int i0 = 0; i0 < nrow; i0 += 8) {
-        float h[8], l[8];
+      for (int i0 = 0; i0 < nrow; i0 += 16) {
+        float h[16], l[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const int i = i0 + u;
           const int64_t o = (int64_t)(row0 + i) * P.ldc + col;
           const bool ok = cok && i < nrow;
@@ -571,7 +572,7 @@ __device__ __forceinline__ void store_chunk_rows(const TcProblem& P, int row0, i
           l[u] = ok ? P.c_lo[o] : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const int i = i0 + u;
           if (cok && i < nrow) {
             const int64_t o = (int64_t)(row0 + i) * P.ldc + col;
