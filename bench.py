@@ -37,6 +37,10 @@ TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 : BF16 tensor rates
 # micro-groups hold the same shapes, so traffic scales with the flops);
 # commands and figures in profiles/gemm_f16_block.md, gemm_tc_kernel_block.md
 TRAFFIC_PER_FLOP = {"3xf16": 3.2e-3, "3xtf32": 6.85e-3}
+# The same for the precise kernel (refresh products and the QR's products, in
+# the mix one refresh of a block launches): 37.6 GB over 2.418e12 flops in 55
+# launches (profiles/gemm_precise_block.md)
+TRAFFIC_PER_FLOP_PRECISE = 1.556e-2
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -355,6 +359,8 @@ def run_ours(args):
             traffic = None
             if cls in ("gemm_f16", "gemm") and args.precision in TRAFFIC_PER_FLOP and g["launches"]:
                 traffic = TRAFFIC_PER_FLOP[args.precision] * g["work"] / g["launches"]
+            elif cls == "gemm_precise" and g["launches"]:
+                traffic = TRAFFIC_PER_FLOP_PRECISE * g["work"] / g["launches"]
             return {
                 "bound": "tensor", "kernel": desc, "class": cls,
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

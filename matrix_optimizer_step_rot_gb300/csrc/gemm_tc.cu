@@ -80,12 +80,25 @@ struct Cfg {
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of 2");
 };
 
-__device__ __forceinline__ void decode(const TcBatch& b, int tile, int& pi, int& m0, int& n0) {
+// Tile order within a problem: groups of kGroupM row blocks, column-major
+// inside a group.  The persistent CTAs work on consecutive tiles at the same
+// time, so a wave touches ~kGroupM row blocks of A and ~(CTAs / kGroupM)
+// column blocks of B, which L2 keeps, instead of a few rows of A against every
+// column block of B (re-read from DRAM by every wave).  The order does not
+// change any result: tiles are independent.
+constexpr int kGroupM = 8;
+
+__device__ __forceinline__ void decode(const TcBatch& b, int tile, int& pi, int& m0, int& nt) {
   pi = 0;
   while (pi + 1 < b.count && tile >= b.p[pi + 1].tile_start) ++pi;
-  const int local = tile - b.p[pi].tile_start;
-  m0 = (local / b.p[pi].tiles_n) * BM;
-  n0 = (local % b.p[pi].tiles_n);
+  const TcProblem& P = b.p[pi];
+  const int local = tile - P.tile_start;
+  const int tn = P.tiles_n, tm = (P.M + BM - 1) / BM;
+  const int per_group = kGroupM * tn;
+  const int g = local / per_group, r = local - g * per_group;
+  const int h = min(kGroupM, tm - g * kGroupM);  // the last group may be shorter
+  m0 = (g * kGroupM + r % h) * BM;
+  nt = r / h;
 }
 
 // Waits without regard to the abort flag (used only to drain at exit).  The
