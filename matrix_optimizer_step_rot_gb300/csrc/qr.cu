@@ -551,16 +551,64 @@ __global__ void __launch_bounds__(256) qr_apply_update_kernel(const __grid_const
 
 // ---------------------------------------------------------------------------
 // block factor T (nb x nb, upper triangular, nb <= NB = 256) from the Gram
-// S = Y^T Y of the block's reflectors.  Each 128-wide half h follows the
-// column recurrence T_ii = 2 / S_ii, T[0:i, i] = -T_ii T[0:i, 0:i] S[0:i, i];
-// the two halves then join as T = [[T0, -T0 S01 T1], [0, T1]] (the product of
-// two compact-WY blocks).  Reflectors past the numerical rank get zero rows and
-// columns.  T is assembled in float32 scratch and written as T and T^T splits
-// (ld NB).  One CTA per matrix, 256 threads, three 128 x 129 shared tiles.
+// S = Y^T Y of the block's reflectors.  The compact-WY product of two
+// consecutive runs of reflectors joins their factors as
+// T = [[T0, -T0 S01 T1], [0, T1]]; applied recursively down to runs of 32,
+// where the column recurrence T_ii = 2 / S_ii, T[0:i, i] = -T_ii T[0:i, 0:i]
+// S[0:i, i] takes over (one warp per run of 32, warp barriers only).  The
+// joins at widths 32, 64 and 128 are small register-blocked products.
+// Reflectors past the numerical rank get zero rows and columns.  T is
+// assembled in float32 scratch and written as T and T^T splits (ld NB).  One
+// CTA per matrix, 256 threads, three 128 x 129 shared tiles.
 // ---------------------------------------------------------------------------
 
 constexpr int TH = NB / 2;  // 128
 constexpr int kTThreads = 256;
+constexpr int kLeaf = 32;   // run of reflectors the column recurrence handles
+
+// C (n x n, ld TH + 1) = A B for n x n shared tiles, all 256 threads: thread t
+// computes row t / (256 / n), n^2 / 256 consecutive columns.
+template <int n>
+__device__ __forceinline__ void tile_mul(const float* A, const float* Bt, float* C) {
+  constexpr int LD = TH + 1;
+  constexpr int tpr = kTThreads / n, cpt = n * n / kTThreads;
+  const int r = threadIdx.x / tpr, c0 = (threadIdx.x % tpr) * cpt;
+  float acc[cpt];
+#pragma unroll
+  for (int c = 0; c < cpt; ++c) acc[c] = 0.f;
+  for (int k = 0; k < n; ++k) {
+    const float av = A[r * LD + k];
+#pragma unroll
+    for (int c = 0; c < cpt; ++c) acc[c] = fmaf(av, Bt[k * LD + c0 + c], acc[c]);
+  }
+#pragma unroll
+  for (int c = 0; c < cpt; ++c) C[r * LD + c0 + c] = acc[c];
+}
+
+// T[o:o+n, o+n:o+2n] = -T0 (S01 T1) with T0, T1 the diagonal blocks at o and
+// o + n (already in T), S01 = S[o:o+n, o+n:o+2n].
+template <int n>
+__device__ void join_block(const QrProblem& q, float* T, int o, int nb, float* tA, float* tB,
+                           float* tC) {
+  constexpr int LD = TH + 1;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < n * n; i += kTThreads) {
+    const int r = i / n, c = i % n;
+    tA[r * LD + c] = o + n + c < nb ? q.s[(int64_t)(o + r) * NB + o + n + c] : 0.f;  // S01
+    tB[r * LD + c] = T[(int64_t)(o + n + r) * NB + o + n + c];                      // T1
+  }
+  __syncthreads();
+  tile_mul<n>(tA, tB, tC);  // X = S01 T1
+  __syncthreads();
+  for (int i = tid; i < n * n; i += kTThreads)
+    tA[(i / n) * LD + i % n] = T[(int64_t)(o + i / n) * NB + o + i % n];  // T0
+  __syncthreads();
+  tile_mul<n>(tA, tC, tB);  // T0 X
+  __syncthreads();
+  for (int i = tid; i < n * n; i += kTThreads)
+    T[(int64_t)(o + i / n) * NB + o + n + i % n] = -tB[(i / n) * LD + i % n];
+  __syncthreads();
+}
 
 __global__ void __launch_bounds__(kTThreads) qr_tblock_kernel(const __grid_constant__ QrBatch b,
                                                               int kb0) {
@@ -577,65 +625,43 @@ __global__ void __launch_bounds__(kTThreads) qr_tblock_kernel(const __grid_const
   const int tid = threadIdx.x, nt = blockDim.x;
   float* T = q.tmp;  // NB x NB float32
   for (int i = tid; i < NB * NB; i += nt) T[i] = 0.f;
+  __syncthreads();
 
-  // diagonal halves by the column recurrence (T half in tA, S half in tB)
-  for (int h = 0; h < 2; ++h) {
-    const int o = h * TH;
-    const int a = max(0, min(TH, act - o));
-    __syncthreads();
-    for (int i = tid; i < TH * LD; i += nt) tA[i] = 0.f;
-    for (int i = tid; i < TH * TH; i += nt) {  // entries past nb were never written
-      const int r = o + i / TH, c = o + i % TH;
-      tB[(i / TH) * LD + i % TH] = (r < nb && c < nb) ? q.s[(int64_t)r * NB + c] : 0.f;
+  // runs of 32 by the column recurrence: warp w takes reflectors 32w .. 32w+31
+  // (its S block and T block in 32 x 33 shared tiles carved from tA .. tC)
+  {
+    const int w = tid >> 5, lane = tid & 31, o = w * kLeaf;
+    constexpr int LL = kLeaf + 1;
+    float* ls = sm + w * 2 * kLeaf * LL;  // 8 warps x 2 x 32 x 33 floats < 3 tiles
+    float* lt = ls + kLeaf * LL;
+    for (int i = lane; i < kLeaf * kLeaf; i += 32) {
+      const int r = o + i / kLeaf, c = o + i % kLeaf;
+      ls[(i / kLeaf) * LL + i % kLeaf] = (r < nb && c < nb) ? q.s[(int64_t)r * NB + c] : 0.f;
+      lt[(i / kLeaf) * LL + i % kLeaf] = 0.f;
     }
-    __syncthreads();
+    __syncwarp();
+    const int a = max(0, min(kLeaf, act - o));
     for (int i = 0; i < a; ++i) {
-      const float tii = 2.f / tB[i * LD + i];
+      const float tii = 2.f / ls[i * LL + i];
       float t = 0.f;
-      if (tid < i)
-        for (int l = tid; l < i; ++l) t = fmaf(tA[tid * LD + l], tB[l * LD + i], t);
-      __syncthreads();
-      if (tid < i) tA[tid * LD + i] = -tii * t;
-      if (tid == i) tA[i * LD + i] = tii;
-      __syncthreads();
+      if (lane < i)
+        for (int l = lane; l < i; ++l) t = fmaf(lt[lane * LL + l], ls[l * LL + i], t);
+      __syncwarp();
+      if (lane < i) lt[lane * LL + i] = -tii * t;
+      if (lane == i) lt[i * LL + i] = tii;
+      __syncwarp();
     }
-    for (int i = tid; i < TH * TH; i += nt)
-      T[(int64_t)(o + i / TH) * NB + o + i % TH] = tA[(i / TH) * LD + i % TH];
+    for (int i = lane; i < kLeaf * kLeaf; i += 32)
+      T[(int64_t)(o + i / kLeaf) * NB + o + i % kLeaf] = lt[(i / kLeaf) * LL + i % kLeaf];
   }
   __syncthreads();
 
-  // off-diagonal block: T01 = -T0 (S01 T1)
-  if (act > TH) {
-    for (int i = tid; i < TH * TH; i += nt) {
-      const int r = i / TH, c = i % TH;
-      tA[r * LD + c] = TH + c < nb ? q.s[(int64_t)r * NB + TH + c] : 0.f;  // S01
-      tB[r * LD + c] = T[(int64_t)(TH + r) * NB + TH + c];  // T1
-    }
-    __syncthreads();
-    const int r = tid >> 1, c0 = (tid & 1) * (TH / 2);
-    float acc[TH / 2];
-#pragma unroll
-    for (int c = 0; c < TH / 2; ++c) acc[c] = 0.f;
-    for (int k = 0; k < TH; ++k) {
-      const float av = tA[r * LD + k];
-#pragma unroll
-      for (int c = 0; c < TH / 2; ++c) acc[c] = fmaf(av, tB[k * LD + c0 + c], acc[c]);
-    }
-#pragma unroll
-    for (int c = 0; c < TH / 2; ++c) tC[r * LD + c0 + c] = acc[c];  // X = S01 T1
-    __syncthreads();
-    for (int i = tid; i < TH * TH; i += nt) tA[(i / TH) * LD + i % TH] = T[(int64_t)(i / TH) * NB + i % TH];
-    __syncthreads();
-#pragma unroll
-    for (int c = 0; c < TH / 2; ++c) acc[c] = 0.f;
-    for (int k = 0; k < TH; ++k) {
-      const float av = tA[r * LD + k];
-#pragma unroll
-      for (int c = 0; c < TH / 2; ++c) acc[c] = fmaf(av, tC[k * LD + c0 + c], acc[c]);
-    }
-#pragma unroll
-    for (int c = 0; c < TH / 2; ++c) T[(int64_t)r * NB + TH + c0 + c] = -acc[c];
-  }
+  // joins: 32 -> 64 -> 128 -> 256 (only where the second run has active reflectors)
+  for (int o = 0; o < NB; o += 64)
+    if (act > o + 32) join_block<32>(q, T, o, nb, tA, tB, tC);
+  for (int o = 0; o < NB; o += 128)
+    if (act > o + 64) join_block<64>(q, T, o, nb, tA, tB, tC);
+  if (act > TH) join_block<TH>(q, T, 0, nb, tA, tB, tC);
   __syncthreads();
 
   float* th = q.tb.hi + (int64_t)blk * NB * NB;
@@ -643,14 +669,29 @@ __global__ void __launch_bounds__(kTThreads) qr_tblock_kernel(const __grid_const
   float* uh = q.tbt.hi + (int64_t)blk * NB * NB;
   float* ul = q.tbt.lo + (int64_t)blk * NB * NB;
   for (int i = tid; i < NB * NB; i += nt) {
-    const int r = i / NB, c = i % NB;
     float h, l;
     split_tf32_mma(T[i], h, l);
     th[i] = h;
     tl[i] = l;
-    split_tf32_mma(T[(int64_t)c * NB + r], h, l);
-    uh[i] = h;
-    ul[i] = l;
+  }
+  // T^T through 32 x 33 shared tiles (one per warp), so that both the reads
+  // of T and the writes of T^T are row-contiguous
+  {
+    const int w = tid >> 5, lane = tid & 31;
+    float* tile = sm + w * 32 * 33;
+    for (int tt = w; tt < (NB / 32) * (NB / 32); tt += nt >> 5) {
+      const int r0 = (tt / (NB / 32)) * 32, c0 = (tt % (NB / 32)) * 32;
+      for (int i = 0; i < 32; ++i) tile[i * 33 + lane] = T[(int64_t)(r0 + i) * NB + c0 + lane];
+      __syncwarp();
+      for (int i = 0; i < 32; ++i) {  // row c0 + i of T^T = column c0 + i of T
+        float h, l;
+        split_tf32_mma(tile[lane * 33 + i], h, l);
+        const int64_t o = (int64_t)(c0 + i) * NB + r0 + lane;
+        uh[o] = h;
+        ul[o] = l;
+      }
+      __syncwarp();
+    }
   }
 }
 
