@@ -798,13 +798,15 @@ int configure_panel(size_t smem) {
 // Cluster size for the panel kernel: at least enough CTAs that a slice of
 // the panel fits in shared memory (<= 1536 elements x 32 rows = 192 KB); then
 // the largest size (up to 16, each CTA keeping >= 640 elements) at which
-// every cluster of the batch can be resident at once.
+// every cluster of the batch can be resident at once (two CTAs to an SM
+// where their slices fit: a column's pass over a CTA's slice is bound by
+// shared-memory traffic, so smaller slices shorten every column).
 int pick_cluster(int count, int pmax, int sms) {
   const int lo = std::max(1, (pmax + 1535) / 1536);
   int best = std::min(lo, kMaxCluster);
   for (int cs = best; cs <= kMaxCluster; ++cs) {
     if (cs > lo && pmax / cs < 640) break;  // small slices: cluster barriers dominate
-    if (cs * count > sms) break;
+    if (cs * count > 2 * sms) break;
     const size_t smem = sizeof(float) * (size_t)B * panel_slice(pmax, cs);
     if (configure_panel(smem) != ROT_OK) break;
     cudaLaunchConfig_t cfg = {};
