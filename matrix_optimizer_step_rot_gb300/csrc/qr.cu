@@ -442,29 +442,42 @@ __global__ void __launch_bounds__(256) qr_apply_partial_kernel(const __grid_cons
   __shared__ float ys[B][33];
   const int tid = threadIdx.x, r = tid >> 3, i4 = (tid & 7) * 4;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c0 = e_begin; c0 < e_end; c0 += 32) {
-    __syncthreads();
-    for (int t = tid; t < kRows * 32; t += 256) {
-      const int rr = t >> 5, ee = t & 31, e = c0 + ee;
+  // each thread's four elements of a 32 x 32 sub-chunk, loaded one sub-chunk
+  // ahead (the loads are in flight while the previous one is multiplied)
+  float xv[4], yv[4];
+  auto load = [&](int c0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = tid + 256 * u, rr = t >> 5, ee = t & 31, e = c0 + ee;
       const int row = r0 + rr;
-      float xv = 0.f, yv = 0.f;
+      xv[u] = 0.f;
+      yv[u] = 0.f;
       if (row < row_end && e < e_end) {
         const int64_t o = (int64_t)row * ld + e;
-        xv = xh[o] + xl[o];
+        xv[u] = xh[o] + xl[o];
       }
       if (rr < active && e < e_end && e >= k0 + rr) {
         const int64_t o = (int64_t)(k0 + rr) * ld + e;
-        yv = xh[o] + xl[o];
+        yv[u] = xh[o] + xl[o];
       }
-      xs[rr][ee] = xv;
-      ys[rr][ee] = yv;
+    }
+  };
+  load(e_begin);
+  for (int c0 = e_begin; c0 < e_end; c0 += 32) {
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = tid + 256 * u;
+      xs[t >> 5][t & 31] = xv[u];
+      ys[t >> 5][t & 31] = yv[u];
     }
     __syncthreads();
+    if (c0 + 32 < e_end) load(c0 + 32);
 #pragma unroll 8
     for (int ee = 0; ee < 32; ++ee) {
-      const float xv = xs[r][ee];
+      const float xe = xs[r][ee];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[c] = fmaf(xv, ys[i4 + c][ee], acc[c]);
+      for (int c = 0; c < 4; ++c) acc[c] = fmaf(xe, ys[i4 + c][ee], acc[c]);
     }
   }
   float* part = q.part + ((int64_t)blockIdx.x * kRowTiles + blockIdx.y) * (kRows * B);
@@ -505,32 +518,51 @@ __global__ void __launch_bounds__(256) qr_apply_update_kernel(const __grid_const
     zt[r][i] = t;
   }
   const int e4 = (tid & 7) * 4;
-  for (int c0 = e_begin; c0 < e_end; c0 += 32) {
-    __syncthreads();
-    for (int t = tid; t < B * 32; t += 256) {
-      const int yi = t >> 5, ee = t & 31, e = c0 + ee;
-      float yv = 0.f;
+  const int row = r0 + r;
+  // the next sub-chunk's reflector elements (four per thread) and this
+  // thread's four elements of its row, loaded one sub-chunk ahead; all of a
+  // sub-chunk's loads go out before its stores (a store could alias a later
+  // load as far as the compiler knows)
+  float yv[4], hv[4], lv[4];
+  auto load = [&](int c0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = tid + 256 * u, yi = t >> 5, ee = t & 31, e = c0 + ee;
+      yv[u] = 0.f;
       if (yi < active && e < e_end && e >= k0 + yi) {
         const int64_t o = (int64_t)(k0 + yi) * ld + e;
-        yv = xh[o] + xl[o];
+        yv[u] = xh[o] + xl[o];
       }
-      ys[yi][ee] = yv;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int e = c0 + e4 + c;
+      hv[c] = 0.f;
+      lv[c] = 0.f;
+      if (row < row_end && e < e_end) {
+        const int64_t o = (int64_t)row * ld + e;
+        hv[c] = xh[o];
+        lv[c] = xl[o];
+      }
+    }
+  };
+  load(e_begin);
+  for (int c0 = e_begin; c0 < e_end; c0 += 32) {
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = tid + 256 * u;
+      ys[t >> 5][t & 31] = yv[u];
     }
     __syncthreads();
-    const int row = r0 + r;
-    if (row < row_end) {
-      // the four elements' loads go out before any store (a store could
-      // alias a later load as far as the compiler knows)
-      float hv[4], lv[4];
+    float hc[4], lc[4];  // this sub-chunk's row elements
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int e = c0 + e4 + c;
-        if (e < e_end) {
-          const int64_t o = (int64_t)row * ld + e;
-          hv[c] = xh[o];
-          lv[c] = xl[o];
-        }
-      }
+    for (int c = 0; c < 4; ++c) {
+      hc[c] = hv[c];
+      lc[c] = lv[c];
+    }
+    if (c0 + 32 < e_end) load(c0 + 32);
+    if (row < row_end) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int e = c0 + e4 + c;
@@ -540,7 +572,7 @@ __global__ void __launch_bounds__(256) qr_apply_update_kernel(const __grid_const
           for (int i = 0; i < B; ++i) t = fmaf(zt[r][i], ys[i][e4 + c], t);
           const int64_t o = (int64_t)row * ld + e;
           float h, l;
-          split_tf32((hv[c] + lv[c]) - t, h, l);
+          split_tf32((hc[c] + lc[c]) - t, h, l);
           xh[o] = h;
           xl[o] = l;
         }
