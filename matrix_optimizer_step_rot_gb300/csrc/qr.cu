@@ -38,6 +38,7 @@
 #include "profile.h"
 #include "rot_internal.h"
 #include "split.cuh"
+#include "tc_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -51,8 +52,28 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct QrBatch {
   int count;
+  int* status;                  // ROT_ETIMEOUT when a bounded wait runs out
+  unsigned long long limit_ns;  // the bound
   QrProblem p[kMaxQ];
 };
+
+// Remote store into a peer CTA's shared memory (the address of `local` in the
+// CTA of cluster rank `rank`) that completes as 4 transaction bytes on the
+// barrier at `bar`'s offset in that CTA.
+__device__ __forceinline__ void push_b32(const void* local, float v, const uint64_t* bar,
+                                         uint32_t rank) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(ra)
+               : "r"(ptx::smem_u32(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(rb)
+               : "r"(ptx::smem_u32(bar)), "r"(rank));
+  asm volatile("st.async.weak.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::
+                   "r"(ra),
+               "r"(__float_as_uint(v)), "r"(rb)
+               : "memory");
+}
 
 __host__ __device__ inline int npanels(int rmax) { return (rmax + B - 1) / B; }
 __host__ __device__ inline int nblocks(int rmax) { return (rmax + NB - 1) / NB; }
@@ -198,6 +219,7 @@ __global__ void __launch_bounds__(kPanelThreads)
   __shared__ float s_ww[B], s_beta[B];
   __shared__ float gram[B][B + 1];
   __shared__ float tmat[B][B + 1];
+  __shared__ uint64_t xbar[2];  // the exchange of each parity completes here
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarp = nthr >> 5;
@@ -246,7 +268,12 @@ __global__ void __launch_bounds__(kPanelThreads)
       at_lo[o] = 0.f;
     }
   if (tid < 2 * B) (&s_piv[0][0])[tid] = 0.f;
-  __syncthreads();
+  if (tid == 0) {
+    ptx::mbar_init(&xbar[0], 1);
+    ptx::mbar_init(&xbar[1], 1);
+    ptx::fence_barrier_init();
+  }
+  cl.sync();  // every CTA's barriers exist before any CTA pushes to them
 
   // Block-reduce acc[] (and the pivot row) for the next column, exchange with
   // the cluster through slot[par], and leave the cluster totals in every
@@ -256,10 +283,19 @@ __global__ void __launch_bounds__(kPanelThreads)
   // parity, and its reader clears it for the column after next); slot[par]
   // is rewritten by other CTAs only after they pass the next cluster barrier,
   // which this CTA reaches after its reads.
+  // The exchange completes on this CTA's barrier xbar[par] (armed for the
+  // cs x 64 values of the column; a peer's values may land before the
+  // arming, which the barrier's transaction count allows) instead of a
+  // cluster barrier.  A slot and barrier of parity par are written again only
+  // two columns later, by a peer that has by then received this CTA's values
+  // of the column in between, which this CTA sends only after reading them.
+  uint32_t xphase = 0;  // bit p: parity of xbar[p]'s current phase
+  bool xfailed = false;  // a wait ran out: stop waiting (the status says so)
   auto reduce_and_share = [&](float (&acc)[B], int par, float& tot_dot, float& tot_piv) {
     const float part = warp_transpose_sum(acc);
     red[lane][warp] = part;
     __syncthreads();
+    if (tid == 0) ptx::mbar_arrive_expect_tx(&xbar[par], (uint32_t)(cs * 2 * B * 4));
     if (tid < 2 * B) {
       float t;
       if (tid < B) {
@@ -269,9 +305,21 @@ __global__ void __launch_bounds__(kPanelThreads)
         t = s_piv[par][tid - B];
         s_piv[par][tid - B] = 0.f;
       }
-      for (int c = 0; c < cs; ++c) *cl.map_shared_rank(&slot[par][crank][tid], c) = t;
+      for (int c = 0; c < cs; ++c) push_b32(&slot[par][crank][tid], t, &xbar[par], (uint32_t)c);
     }
-    cl.sync();
+    const uint32_t ph = (xphase >> par) & 1u;
+    xphase ^= 1u << par;
+    if (!xfailed && !ptx::mbar_try_wait(&xbar[par], ph)) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(&xbar[par], ph)) break;
+        if ((it & 63u) == 0u && (ptx::globaltimer_ns() - t0 > b.limit_ns || it > (1u << 30))) {
+          xfailed = true;
+          if (b.status) atomicExch(b.status, ROT_ETIMEOUT);
+          break;
+        }
+      }
+    }
     tot_dot = 0.f;
     tot_piv = 0.f;
     for (int c = 0; c < cs; ++c) {
@@ -944,6 +992,8 @@ int qr_batched(const hvec<QrProblem>& probs, float rank_rtol, int* status,
     QrBatch b;
     std::memset(&b, 0, sizeof(b));
     b.count = (int)std::min<size_t>(kMaxQ, probs.size() - base);
+    b.status = status;
+    b.limit_ns = g_wait_limit_ns;
     int rmax = 0, pmax = 0;
     for (int i = 0; i < b.count; ++i) {
       b.p[i] = probs[base + i];
