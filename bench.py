@@ -423,8 +423,8 @@ def run_ours(args):
                        "oracle on every sampled shape of the tiny, block and full-stack "
                        "workloads; the Qwen3-8B-shaped slice and the ragged set miss 1e-4 on "
                        "some matrices, where float32 arithmetic itself does: all 8B-slice "
-                       "matrices within what 22-bit product operands allow, 3 (3xTF32) / 2 "
-                       "(3xF16) of 154 ragged matrices beyond it by at most 1.47x "
+                       "matrices within what 22-bit product operands allow, 2 (3xTF32) / 1 "
+                       "(3xF16) of 154 ragged matrices beyond it by at most 1.46x "
                        "(tests/test_configs_gpu.py, profiles/parity_full_size.txt)"),
         }
         if world == 1 and not args.no_cpu_baseline:
