@@ -199,10 +199,10 @@ def run_ours(args):
 
     t = 0
 
-    def step(G):
+    def step(G, Wl=None):
         nonlocal t
         t += 1
-        opt.step(W, G, wl.refresh(t))
+        opt.step(W if Wl is None else Wl, G, wl.refresh(t))
 
     for _ in range(args.warmup):
         step(Gsets[t % 2])
@@ -256,10 +256,12 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers.  Each step's
     # gradients come from pinned host memory and its updated W goes back to
     # pinned host memory.  The next step's gradients are copied in on a side
-    # stream while the current step computes (two device buffers); W's copy out
-    # runs on another side stream, and the next step waits for it because it
-    # updates W in place.
+    # stream while the current step computes (two device buffers).  W is kept
+    # twice on the device: step i starts from a device copy of step i-1's W
+    # and updates that copy, while step i-1's W goes to the host on another
+    # side stream (a buffer is overwritten only once its copy out is done).
     e_steps = 0 if args.no_e2e else max(1, min(args.steps, 5))
+    w_dev = [W, [w.clone() for w in W]] if e_steps else []
     g_host = [g.cpu().pin_memory() for g in Gsets[0]] if e_steps else []
     w_host = [w.cpu().pin_memory() for w in W] if e_steps else []
     g_dev = [[torch.empty_like(g) for g in Gsets[0]] for _ in range(2)] if e_steps else []
@@ -292,16 +294,20 @@ def run_ours(args):
     ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(max(e_steps, 1))]
     ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(max(e_steps, 1))]
     for i in range(e_steps):
+        cur, prev = w_dev[i % 2], w_dev[(i + 1) % 2]
         stream.wait_event(ev_in[i % 2])
         if i > 0:
-            stream.wait_event(ev_out[i - 1])
+            if i > 1:
+                stream.wait_event(ev_out[i - 2])  # cur's previous contents are on the host
+            for c, p in zip(cur, prev):  # step i starts from step i-1's W
+                c.copy_(p, non_blocking=True)
         ev_start[i].record(stream)
-        step(g_dev[i % 2])
+        step(g_dev[i % 2], cur)
         ev_end[i].record(stream)
         ev_done[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[i])
-            for wh, wd in zip(w_host, W):
+            for wh, wd in zip(w_host, cur):
                 wh.copy_(wd, non_blocking=True)
         ev_out[i].record(s_out)
         if i + 1 < e_steps:
@@ -317,10 +323,11 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e2e_ms = x0.elapsed_time(x1) if e_steps else 0.0
     # device time of the steps themselves inside the end-to-end run; the rest
-    # is copies on the critical path (the first H2D and each step's D2H)
+    # is copies on the critical path (the first H2D, the device copies of W
+    # between steps and the last step's D2H)
     e2e_compute_ms = sum(ev_start[i].elapsed_time(ev_end[i]) for i in range(e_steps))
     # what lies between: before the first step (its gradients' H2D), between
-    # steps (the previous W's D2H), after the last (its D2H)
+    # steps (the device copy of W), after the last (its D2H)
     e2e_gaps_ms = ([x0.elapsed_time(ev_start[0])]
                    + [ev_end[i].elapsed_time(ev_start[i + 1]) for i in range(e_steps - 1)]
                    + [ev_end[e_steps - 1].elapsed_time(x1)]) if e_steps else []
