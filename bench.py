@@ -260,7 +260,7 @@ def run_ours(args):
     # twice on the device: step i starts from a device copy of step i-1's W
     # and updates that copy, while step i-1's W goes to the host on another
     # side stream (a buffer is overwritten only once its copy out is done).
-    e_steps = 0 if args.no_e2e else max(1, min(args.steps, 5))
+    e_steps = 0 if args.no_e2e else max(1, args.steps)  # as many steps as the timed region
     w_dev = [W, [w.clone() for w in W]] if e_steps else []
     g_host = [g.cpu().pin_memory() for g in Gsets[0]] if e_steps else []
     w_host = [w.cpu().pin_memory() for w in W] if e_steps else []
