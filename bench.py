@@ -260,23 +260,42 @@ def run_ours(args):
     # twice on the device: step i starts from a device copy of step i-1's W
     # and updates that copy, while step i-1's W goes to the host on another
     # side stream (a buffer is overwritten only once its copy out is done).
+    # Every buffer is one flat allocation with the matrices as views into it,
+    # so that a step's copies are three calls (gradients in, W's device copy,
+    # W out), not three per matrix.
     e_steps = 0 if args.no_e2e else max(1, args.steps)  # as many steps as the timed region
-    w_dev = [W, [w.clone() for w in W]] if e_steps else []
-    g_host = [g.cpu().pin_memory() for g in Gsets[0]] if e_steps else []
-    w_host = [w.cpu().pin_memory() for w in W] if e_steps else []
-    g_dev = [[torch.empty_like(g) for g in Gsets[0]] for _ in range(2)] if e_steps else []
-    h2d = sum(g.numel() * 4 for g in g_host)
-    d2h = sum(w.numel() * 4 for w in w_host)
+    offsets, total = [], 0
+    for m, n in wl.shapes:  # each matrix on a 256-byte boundary
+        offsets.append(total)
+        total += (m * n + 63) // 64 * 64
+
+    def views(flat):
+        return [flat[o:o + m * n].view(m, n) for o, (m, n) in zip(offsets, wl.shapes)]
+
+    def flat_of(mats, pinned=False, device=None):
+        f = torch.zeros(total, dtype=torch.float32, device=device)
+        for v, x in zip(views(f), mats):
+            v.copy_(x)
+        return f.pin_memory() if pinned else f
+
+    g_host_flat = flat_of([g.cpu() for g in Gsets[0]], pinned=True) if e_steps else None
+    w_host_flat = torch.empty(total, dtype=torch.float32).pin_memory() if e_steps else None
+    g_dev_flat = [torch.empty(total, dtype=torch.float32, device=dev) for _ in range(2)] if e_steps else []
+    w_dev_flat = [flat_of(W, device=dev),
+                  torch.empty(total, dtype=torch.float32, device=dev)] if e_steps else []
+    g_dev = [views(f) for f in g_dev_flat]
+    w_dev = [views(f) for f in w_dev_flat]
+    # bytes per step: the matrices themselves (the padding travels too, < 256 B each)
+    h2d = sum(m * n for m, n in wl.shapes) * 4 if e_steps else 0
+    d2h = h2d
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
     if e_steps:
         # untimed: one round trip through every pinned buffer, so that the
         # timed copies do not pay for the first device access to fresh pages
-        for buf in g_dev:
-            for gd, gh in zip(buf, g_host):
-                gd.copy_(gh, non_blocking=True)
-        for wh, wd in zip(w_host, W):
-            wh.copy_(wd, non_blocking=True)
+        for f in g_dev_flat:
+            f.copy_(g_host_flat, non_blocking=True)
+        w_host_flat.copy_(w_dev_flat[0], non_blocking=True)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -288,34 +307,30 @@ def run_ours(args):
     x0.record(s_in)
     if e_steps:
         with torch.cuda.stream(s_in):
-            for gd, gh in zip(g_dev[0], g_host):
-                gd.copy_(gh, non_blocking=True)
+            g_dev_flat[0].copy_(g_host_flat, non_blocking=True)
         ev_in[0].record(s_in)
     ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(max(e_steps, 1))]
     ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(max(e_steps, 1))]
     for i in range(e_steps):
-        cur, prev = w_dev[i % 2], w_dev[(i + 1) % 2]
+        cur, prev = i % 2, (i + 1) % 2
         stream.wait_event(ev_in[i % 2])
         if i > 0:
             if i > 1:
                 stream.wait_event(ev_out[i - 2])  # cur's previous contents are on the host
-            for c, p in zip(cur, prev):  # step i starts from step i-1's W
-                c.copy_(p, non_blocking=True)
+            w_dev_flat[cur].copy_(w_dev_flat[prev], non_blocking=True)  # from step i-1's W
         ev_start[i].record(stream)
-        step(g_dev[i % 2], cur)
+        step(g_dev[i % 2], w_dev[cur])
         ev_end[i].record(stream)
         ev_done[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[i])
-            for wh, wd in zip(w_host, cur):
-                wh.copy_(wd, non_blocking=True)
+            w_host_flat.copy_(w_dev_flat[cur], non_blocking=True)
         ev_out[i].record(s_out)
         if i + 1 < e_steps:
             with torch.cuda.stream(s_in):
                 if i > 0:
                     s_in.wait_event(ev_done[i - 1])  # buffer (i+1)%2 last read by step i-1
-                for gd, gh in zip(g_dev[(i + 1) % 2], g_host):
-                    gd.copy_(gh, non_blocking=True)
+                g_dev_flat[(i + 1) % 2].copy_(g_host_flat, non_blocking=True)
             ev_in[(i + 1) % 2].record(s_in)
     if e_steps:
         stream.wait_event(ev_out[e_steps - 1])

@@ -257,7 +257,11 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
             for (int u = 0; u < 4; ++u) {
               const float v =
                   (hp[u] + lp[u]) - P.alpha * __uint_as_float(r[16 * half + 4 * i + u]);
-              split_tf32(v, hp[u], lp[u]);
+              if (P.mma_only) {
+                split_tf32_mma(v, hp[u], lp[u]);
+              } else {
+                split_tf32(v, hp[u], lp[u]);
+              }
             }
             reinterpret_cast<float4*>(hi)[4 * half + i] = h4[i];
             reinterpret_cast<float4*>(lo)[4 * half + i] = l4[i];
@@ -269,7 +273,11 @@ __device__ __forceinline__ void store_chunk(const TcProblem& P, int row, int col
           if (t < ncol) {
             const float v = (hi[t] + lo[t]) - P.alpha * __uint_as_float(r[t]);
             float h, l;
-            split_tf32(v, h, l);
+            if (P.mma_only) {
+              split_tf32_mma(v, h, l);
+            } else {
+              split_tf32(v, h, l);
+            }
             hi[t] = h;
             lo[t] = l;
           }
@@ -590,7 +598,12 @@ __device__ __forceinline__ void store_chunk_rows(const TcProblem& P, int row0, i
           if (cok && i < nrow) {
             const int64_t o = (int64_t)(row0 + i) * P.ldc + col;
             float hh, ll;
-            split_tf32((h[u] + l[u]) - alpha * stage[i * kStageStride + lane], hh, ll);
+            const float v = (h[u] + l[u]) - alpha * stage[i * kStageStride + lane];
+            if (P.mma_only) {
+              split_tf32_mma(v, hh, ll);
+            } else {
+              split_tf32(v, hh, ll);
+            }
             P.c_hi[o] = hh;
             P.c_lo[o] = ll;
           }

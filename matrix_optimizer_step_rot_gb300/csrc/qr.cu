@@ -56,6 +56,7 @@ struct QrBatch {
   unsigned long long limit_ns;  // the bound
   QrProblem p[kMaxQ];
 };
+static_assert(sizeof(QrBatch) <= 32764, "kernel parameter block above the 32764-byte limit");
 
 // Remote store into a peer CTA's shared memory (the address of `local` in the
 // CTA of cluster rank `rank`) that completes as 4 transaction bytes on the
@@ -224,7 +225,6 @@ __global__ void __launch_bounds__(kPanelThreads)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarp = nthr >> 5;
   const int p = q.p, ld = q.ld;
-  const int kb0 = (k0 / NB) * NB;  // start of this panel's block
   const int panel_id = k0 / B;
   const bool in_range = k0 < q.rmax;
   const int bw = in_range ? min(B, q.rmax - k0) : 0;
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kPanelThreads)
     // stopped in an earlier panel: these rows are identities; clear them so
     // that the block GEMMs read zeros there
     for (int j = 0; j < bw; ++j)
-      for (int e = kb0 + crank * nthr + tid; e < p; e += cs * nthr) {
+      for (int e = crank * nthr + tid; e < p; e += cs * nthr) {
         const int64_t o = (int64_t)(k0 + j) * ld + e;
         at_hi[o] = 0.f;
         at_lo[o] = 0.f;
@@ -251,7 +251,9 @@ __global__ void __launch_bounds__(kPanelThreads)
   }
 
   // load my slice of the panel; clear the R entries in front of it
-  // (elements kb0 .. k0-1 of the panel's rows)
+  // (elements 0 .. k0-1 of the panel's rows, so that a row of `at` is its
+  // reflector from element 0: Q formation reads pairs of blocks from the
+  // first block's start)
   for (int i = tid; i < bw * R; i += nthr) {
     const int j = i / R, e = e0 + i % R;
     float x = 0.f;
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kPanelThreads)
     panel[i] = x;
   }
   for (int j = 0; j < bw; ++j)
-    for (int e = kb0 + crank * nthr + tid; e < k0; e += cs * nthr) {
+    for (int e = crank * nthr + tid; e < k0; e += cs * nthr) {
       const int64_t o = (int64_t)(k0 + j) * ld + e;
       at_hi[o] = 0.f;
       at_lo[o] = 0.f;
@@ -793,6 +795,34 @@ __global__ void qr_eye_kernel(const __grid_constant__ QrBatch b) {
   }
 }
 
+// The factor of a pair of consecutive blocks b, b+1 (compact WY):
+// T = [[T_b, -T_b S01 T_{b+1}], [0, T_{b+1}]], 2 NB x 2 NB (ld 2 NB).  This
+// kernel places T_b and T_{b+1} and zeroes the rest; the upper-right block is
+// then added by a product.  Problems whose pair has one block are skipped.
+__global__ void qr_pair_assemble_kernel(const __grid_constant__ QrBatch b, int kb0) {
+  const QrProblem& q = b.p[blockIdx.y];
+  if (kb0 + NB >= q.rmax) return;
+  const int64_t blk = kb0 / NB;
+  const float* t0h = q.tb.hi + blk * NB * NB;
+  const float* t0l = q.tb.lo + blk * NB * NB;
+  const float* t1h = q.tb.hi + (blk + 1) * NB * NB;
+  const float* t1l = q.tb.lo + (blk + 1) * NB * NB;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < 4 * NB * NB;
+       e += gridDim.x * blockDim.x) {
+    const int r = e / (2 * NB), c = e % (2 * NB);
+    float h = 0.f, l = 0.f;
+    if (r < NB && c < NB) {
+      h = t0h[r * NB + c];
+      l = t0l[r * NB + c];
+    } else if (r >= NB && c >= NB) {
+      h = t1h[(r - NB) * NB + c - NB];
+      l = t1l[(r - NB) * NB + c - NB];
+    }
+    q.tpair.hi[e] = h;
+    q.tpair.lo[e] = l;
+  }
+}
+
 __global__ void qr_finalize_kernel(const __grid_constant__ QrBatch b) {
   __shared__ float tile[32][33];
   const QrProblem& q = b.p[blockIdx.y];
@@ -938,12 +968,14 @@ uint64_t qr_aux_bytes(int p, int rmax) {
   return align256(np * B * B * 4)                   // panel T factors
          + align256((uint64_t)rmax * 4 + 4)         // beta
          + align256((np + 2) * 4) + 256             // ctrl, tau
-         + 2 * align256((uint64_t)p * NB * 4)       // yt split
-         + 2 * align256((uint64_t)NB * ld * 4)      // w1t split
-         + 2 * align256((uint64_t)p * NB * 4)       // z split
+         + 2 * align256((uint64_t)p * 2 * NB * 4)   // yt split (up to a pair of blocks)
+         + 2 * align256((uint64_t)2 * NB * ld * 4)  // w1t split
+         + 2 * align256((uint64_t)p * 2 * NB * 4)   // z split
          + align256((uint64_t)NB * NB * 4)          // Gram S
          + align256((uint64_t)NB * NB * 4)          // T assembly scratch
          + 4 * align256(nbk * NB * NB * 4)          // T and T^T splits per block
+         + 2 * align256((uint64_t)4 * NB * NB * 4)  // a pair's T split
+         + 4 * align256((uint64_t)NB * NB * 4)      // S01 and X^T splits
          + align256(((uint64_t)p / kChunk + 1) * kRowTiles * kRows * B * 4);  // partials
 }
 
@@ -960,18 +992,24 @@ void qr_bind_aux(QrProblem& q, char* aux, int p, int rmax) {
   q.beta = reinterpret_cast<float*>(take((uint64_t)rmax * 4 + 4));
   q.ctrl = reinterpret_cast<int*>(take((np + 2) * 4));
   q.tau = reinterpret_cast<float*>(take(256));
-  q.yt.hi = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
-  q.yt.lo = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
-  q.w1t.hi = reinterpret_cast<float*>(take((uint64_t)NB * ld * 4));
-  q.w1t.lo = reinterpret_cast<float*>(take((uint64_t)NB * ld * 4));
-  q.z.hi = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
-  q.z.lo = reinterpret_cast<float*>(take((uint64_t)p * NB * 4));
+  q.yt.hi = reinterpret_cast<float*>(take((uint64_t)p * 2 * NB * 4));
+  q.yt.lo = reinterpret_cast<float*>(take((uint64_t)p * 2 * NB * 4));
+  q.w1t.hi = reinterpret_cast<float*>(take((uint64_t)2 * NB * ld * 4));
+  q.w1t.lo = reinterpret_cast<float*>(take((uint64_t)2 * NB * ld * 4));
+  q.z.hi = reinterpret_cast<float*>(take((uint64_t)p * 2 * NB * 4));
+  q.z.lo = reinterpret_cast<float*>(take((uint64_t)p * 2 * NB * 4));
   q.s = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
   q.tmp = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
   q.tb.hi = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
   q.tb.lo = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
   q.tbt.hi = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
   q.tbt.lo = reinterpret_cast<float*>(take(nbk * NB * NB * 4));
+  q.tpair.hi = reinterpret_cast<float*>(take((uint64_t)4 * NB * NB * 4));
+  q.tpair.lo = reinterpret_cast<float*>(take((uint64_t)4 * NB * NB * 4));
+  q.s01.hi = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
+  q.s01.lo = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
+  q.xt.hi = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
+  q.xt.lo = reinterpret_cast<float*>(take((uint64_t)NB * NB * 4));
   q.part = reinterpret_cast<float*>(take(((uint64_t)p / kChunk + 1) * kRowTiles * kRows * B * 4));
 }
 
@@ -1090,23 +1128,60 @@ int qr_batched(const hvec<QrProblem>& probs, float rank_rtol, int* status,
       qr_eye_kernel<<<dim3((unsigned)std::min<int64_t>(4096, (most + 1023) / 1024), n), 256, 0,
                       stream>>>(b);
     }
-    for (int kb0 = ((rmax - 1) / NB) * NB; kb0 >= 0; kb0 -= NB) {
+    // Pairs of blocks (b, b+1) are applied together as one rank-(up to 512)
+    // update, with the pair's factor joined from the two blocks' factors: half
+    // the passes over Q, and twice the K of each update.  A last block without
+    // a partner is applied alone.
+    const int npairs = (nblocks(rmax) + 1) / 2;
+    for (int pp = npairs - 1; pp >= 0; --pp) {
+      const int kb0 = pp * 2 * NB;
+      hvec<GemmProblem> gs, gx, gt;
+      for (int i = 0; i < b.count; ++i) {
+        const QrProblem& q = b.p[i];
+        const int e1 = kb0 + NB;  // the second block's first reflector
+        if (e1 >= q.rmax) continue;
+        const int nb1 = std::min(NB, q.rmax - e1);
+        const int64_t blk = kb0 / NB;
+        // S01 = Y_b^T Y_{b+1} (NB x nb1), over elements >= e1 (Y_{b+1} is 0 before)
+        gs.push_back(gp(NB, nb1, q.p - e1, q.at.hi + (int64_t)kb0 * q.ld + e1,
+                        q.at.lo + (int64_t)kb0 * q.ld + e1, q.ld,
+                        q.at.hi + (int64_t)e1 * q.ld + e1, q.at.lo + (int64_t)e1 * q.ld + e1,
+                        q.ld, q.s01.hi, q.s01.lo, NB, kEpiStoreSplit, 0.f, 1));
+        // X^T = T_{b+1}^T S01^T (nb1 x NB)
+        gx.push_back(gp(nb1, NB, nb1, q.tbt.hi + (blk + 1) * NB * NB,
+                        q.tbt.lo + (blk + 1) * NB * NB, NB, q.s01.hi, q.s01.lo, NB, q.xt.hi,
+                        q.xt.lo, NB, kEpiStoreSplit, 0.f, 1));
+        // upper-right block of the pair's factor: 0 - T_b X
+        gt.push_back(gp(NB, nb1, NB, q.tb.hi + blk * NB * NB, q.tb.lo + blk * NB * NB, NB,
+                        q.xt.hi, q.xt.lo, NB, q.tpair.hi + NB, q.tpair.lo + NB, 2 * NB,
+                        kEpiApplySplit, 1.f, 1));
+      }
+      if (!gs.empty()) {
+        if (gemm_grouped(gs, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+        if (gemm_grouped(gx, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+        {
+          ProfScope prof(ROT_PROF_QR_OTHER, 0.0, stream);
+          qr_pair_assemble_kernel<<<dim3(64, n), 256, 0, stream>>>(b, kb0);
+        }
+        if (gemm_grouped(gt, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
+      }
       hvec<TransposeSeg> tr;
       hvec<GemmProblem> q1, q2, q3;
       for (int i = 0; i < b.count; ++i) {
         const QrProblem& q = b.p[i];
         if (kb0 >= q.rmax) continue;
-        const int nb = std::min(NB, q.rmax - kb0), L = q.p - kb0;
-        const int blk = kb0 / NB;
+        const int nb = std::min(2 * NB, q.rmax - kb0), L = q.p - kb0;
+        const bool pair = nb > NB;
         const int64_t oy = (int64_t)kb0 * q.ld + kb0;
-        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, NB, nb, L, 1, 1, 1});
-        q1.push_back(gp(nb, L, nb, q.tb.hi + (int64_t)blk * NB * NB,
-                        q.tb.lo + (int64_t)blk * NB * NB, NB, q.yt.hi, q.yt.lo, NB, q.w1t.hi,
-                        q.w1t.lo, q.ld, kEpiStoreSplit, 0.f, 1));
+        const float* th = pair ? q.tpair.hi : q.tb.hi + (int64_t)(kb0 / NB) * NB * NB;
+        const float* tl = pair ? q.tpair.lo : q.tb.lo + (int64_t)(kb0 / NB) * NB * NB;
+        tr.push_back({q.at.hi + oy, q.at.lo + oy, q.ld, q.yt.hi, q.yt.lo, 2 * NB, nb, L, 1, 1, 1});
+        q1.push_back(gp(nb, L, nb, th, tl, pair ? 2 * NB : NB, q.yt.hi, q.yt.lo, 2 * NB,
+                        q.w1t.hi, q.w1t.lo, q.ld, kEpiStoreSplit, 0.f, 1));
         q2.push_back(gp(L, nb, L, q.qt.hi + oy, q.qt.lo + oy, q.ld, q.w1t.hi, q.w1t.lo, q.ld,
-                        q.z.hi, q.z.lo, NB, kEpiStoreSplit, 0.f, 1));
-        q3.push_back(gp(L, L, nb, q.z.hi, q.z.lo, NB, q.yt.hi, q.yt.lo, NB, q.qt.hi + oy,
-                        q.qt.lo + oy, q.ld, kEpiApplySplit, 1.f));
+                        q.z.hi, q.z.lo, 2 * NB, kEpiStoreSplit, 0.f, 1));
+        q3.push_back(gp(L, L, nb, q.z.hi, q.z.lo, 2 * NB, q.yt.hi, q.yt.lo, 2 * NB,
+                        q.qt.hi + oy, q.qt.lo + oy, q.ld, kEpiApplySplit, 1.f));
       }
       if (tr.empty()) continue;
       if (launch_transpose(tr, stream) != ROT_OK) return ROT_ECUDA;

@@ -77,6 +77,7 @@ enum GemmEpi : int {
   kEpiStoreF32T = 3,    // C^T <- acc, float32 into c.hi
   kEpiApply = 4,        // C (row-major, float32 in c.hi) -= alpha * acc
   kEpiApplySplit = 5,   // C (row-major split) <- split(hi + lo - alpha * acc)
+                        // (with mma_only: the TF32-rounded split of arrays only MMAs read)
   kEpiStoreF16SplitT = 6,  // C^T (row-major N x M fp16 arrays) <- scaled fp16 split (3xF16)
   kEpiStoreBF16 = 7,    // C (row-major) <- acc rounded to bf16, into c.hi (compact state)
 };
@@ -305,6 +306,12 @@ struct QrProblem {
   float* tmp;   // kQrBlock x kQrBlock: T of the current block, float32
   Split tb;     // per block: T (kQrBlock x kQrBlock)
   Split tbt;    // per block: T^T
+  // Q formation in pairs of blocks (rank-512 updates): the pair's factor
+  // T (2 kQrBlock x 2 kQrBlock) and its parts S01 = Y_b^T Y_{b+1} and
+  // X^T = (S01 T_{b+1})^T (kQrBlock x kQrBlock each)
+  Split tpair;
+  Split s01;
+  Split xt;
   float* tf;    // per panel: 32 x 32 triangular factor
   float* part;  // within-block update: per element chunk and row tile, Y^T a partials
   float* beta;  // rmax: R diagonal before the sign fix

@@ -103,6 +103,16 @@ def test_gemm_precise_error_does_not_grow_with_k(K):
     assert err <= 2e-7, err
 
 
+@pytest.mark.parametrize("epi", [0, 1, 2, 4, 5])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 300), (256, 384, 512), (130, 260, 513)])
+def test_gemm_precise_around_the_short_k_limit(M, N, K, epi):
+    """K up to 512 runs the short-K variant (the whole sum in registers, four
+    TMEM buffers), K = 513 the long one: both in every output mode."""
+    out, ref = run(M, N, K, epi, PRECISE, seed=K + epi)
+    err = float((out - ref).norm() / ref.norm())
+    assert err <= (1e-5 if epi in (4, 5) else TOL[PRECISE]), err
+
+
 @pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, PRECISE])
 @pytest.mark.parametrize("epi", [0, 1, 3, 4, 5])
 @pytest.mark.parametrize("M,N,K", [(300, 520, 100), (64, 64, 64), (1, 40, 7)])
