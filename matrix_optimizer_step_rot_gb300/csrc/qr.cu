@@ -24,10 +24,11 @@
 //     the panel's 32 x 32 triangular factor;
 //   * each 256-column block's reflectors form H_k..H_{k+255} = I - Y T Y^T;
 //     the columns after the block (up to rmax) receive a <- (I - Y T^T Y^T) a,
-//     and Q is accumulated backwards block by block, q <- (I - Y T Y^T) q, both
-//     as three tensor-core GEMMs (T^T Y^T or T Y^T, then X (Y T), X -= Z Y^T),
-//     on the precise kernel (K-blocks summed in float32 registers): Q's
-//     orthogonality error adds up over all p^2 entries.
+//     and Q is accumulated backwards a pair of blocks at a time (the pair's
+//     factor joined from the two blocks'), q <- (I - Y T Y^T) q, both as
+//     three tensor-core GEMMs (T^T Y^T or T Y^T, then X (Y T), X -= Z Y^T),
+//     on the precise kernel (K-blocks summed in float32): Q's orthogonality
+//     error adds up over all p^2 entries.
 // A range guard (qr_colnorm_kernel, qr_scale_kernel) rescales inputs whose
 // squared column norms would leave float32's range.
 #include <cooperative_groups.h>
@@ -1186,8 +1187,8 @@ int qr_batched(const hvec<QrProblem>& probs, float rank_rtol, int* status,
       if (tr.empty()) continue;
       if (launch_transpose(tr, stream) != ROT_OK) return ROT_ECUDA;
       // precise: Q's orthogonality error adds up over all p^2 entries (the
-      // rank-256 update too: accumulated in TMEM, in 3xTF32 or 3xF16, it moved
-      // the bases' orthogonality and the W parity measurably)
+      // rank-256/512 updates too: accumulated in TMEM, in 3xTF32 or 3xF16, they
+      // moved the bases' orthogonality and the W parity measurably)
       if (gemm_grouped(q1, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
       if (gemm_grouped(q2, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
       if (gemm_grouped(q3, kPrecPrecise, status, stream) != ROT_OK) return ROT_ECUDA;
