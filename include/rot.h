@@ -59,6 +59,9 @@ extern "C" {
                                 rot_status while rot_set_nonfinite_check is on) */
 #define ROT_ENOTSUP (-6)     /* GPU is not sm_103 or the feature is not built */
 #define ROT_ETOOLARGE (-7)   /* plan needs more scratch than rot_step_noalloc holds */
+#define ROT_ECORRUPT (-8)    /* bounds-checked builds (compiled with ROT_CHECK) only: a
+                                guard region around a workspace slice was overwritten
+                                during a step (reported by rot_status) */
 
 #define ROT_PREC_TF32 1      /* one TF32 tensor-core product per GEMM */
 #define ROT_PREC_3XTF32 3    /* hi*hi + hi*lo + lo*hi TF32 split, ~fp32 accuracy */

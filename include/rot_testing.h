@@ -49,6 +49,26 @@ int rot_test_fail_host_alloc(int64_t after);
 /* Workspace bytes rot_test_gemm needs for these sizes. */
 uint64_t rot_test_gemm_work_bytes(int32_t M, int32_t N, int32_t K);
 
+/* Bounds-checked builds (the library compiled with ROT_CHECK; the survey's
+ * canary words).  The plan then leaves a 256-byte guard region after every
+ * slice of the workspace; rot_step fills each micro-group's guards with a
+ * fixed pattern before the group's work and checks them after it, setting the
+ * status word to ROT_ECORRUPT (rot_status) if any was overwritten.
+ *
+ * rot_test_guard_offsets: byte offsets (into the workspace) of micro-group
+ * `group`'s guards, up to `capacity` of them into `offsets` (host array),
+ * their number into *count.  Host-side.  Errors: ROT_EINVAL (null plan or
+ * count, group out of range), ROT_ENOTSUP (a build without ROT_CHECK).
+ *
+ * rot_test_check_guards: runs only the check of micro-group `group`'s guards
+ * on `stream` (device pointers `state`, `work` as for rot_step), so that a
+ * test can overwrite a guard and see it reported.  Errors: ROT_EINVAL,
+ * ROT_ENOTSUP, ROT_ECUDA. */
+int rot_test_guard_offsets(const rot_plan* plan, int32_t group, uint64_t* offsets,
+                           int32_t capacity, int32_t* count);
+int rot_test_check_guards(const rot_plan* plan, int32_t group, void* state, void* work,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,9 @@ import re
 from typing import List, Optional, Sequence, Tuple
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "librot.so")
+# the library to load: librot.so, or the file ROT_LIB names (the bounds-checked
+# build, librot_check.so, in its tests)
+LIB_PATH = os.environ.get("ROT_LIB") or os.path.join(PKG, "librot.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 HEADERS = [os.path.join(INCLUDE, "rot.h"), os.path.join(INCLUDE, "rot_testing.h")]
 
@@ -26,6 +28,7 @@ ROT_ETIMEOUT = -4
 ROT_ENONFINITE = -5
 ROT_ENOTSUP = -6
 ROT_ETOOLARGE = -7
+ROT_ECORRUPT = -8
 ROT_NOALLOC_MAX_BYTES = 64 << 20
 ROT_PREC_TF32 = 1
 ROT_PREC_3XTF32 = 3
@@ -81,6 +84,9 @@ _SIGS = {
     "rot_test_gemm": (_i32, [_i32, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _i32,
                              _vp, _u64, _vp, _vp]),
     "rot_test_gemm_work_bytes": (_u64, [_i32, _i32, _i32]),
+    "rot_test_guard_offsets": (_i32, [_vp, _i32, ctypes.POINTER(_u64), _i32,
+                                      ctypes.POINTER(_i32)]),
+    "rot_test_check_guards": (_i32, [_vp, _i32, _vp, _vp, _vp]),
     "rot_test_wait_timeout": (_i32, [_u64, _vp, _vp]),
     "rot_test_fail_host_alloc": (_i32, [ctypes.c_int64]),
     "rot_item_work": (_i32, [ctypes.POINTER(rot_shape), _i32, ctypes.POINTER(_u64)]),
@@ -94,19 +100,26 @@ _SIGS = {
 }
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """A build of the library at `path` with every entry point's signature set
+    (the default build is lib()'s; this also opens the bounds-checked one)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "matrix_optimizer_step_rot_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib() -> ctypes.CDLL:
-    """Load librot.so (raises if it has not been built)."""
+    """Load librot.so, or the library ROT_LIB names (raises if it has not been
+    built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                               "matrix_optimizer_step_rot_gb300.build.build()")
-        L = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGS.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = L
+        _lib = load_library(LIB_PATH)
     return _lib
 
 

@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librot.so")
+# the bounds-checked variant (ROT_CHECK: guard regions around every workspace
+# slice, checked after each micro-group; include/rot_testing.h)
+BUILD_CHECK = os.path.join(PKG, "_build_check")
+LIB_CHECK = os.path.join(PKG, "librot_check.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
@@ -42,15 +46,17 @@ def _headers():
     return hs + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
 
 
-def build(verbose: bool = False, extra_flags=None) -> str:
-    """Build librot.so if needed; returns its path.  Raises on compiler errors."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags=None, check: bool = False) -> str:
+    """Build librot.so (check: the bounds-checked librot_check.so) if needed;
+    returns its path.  Raises on compiler errors."""
+    build_dir, lib = (BUILD_CHECK, LIB_CHECK) if check else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + (["-DROT_CHECK"] if check else []) + list(extra_flags or [])
     newest_header = max(os.path.getmtime(h) for h in _headers())
     jobs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         stale = (not os.path.exists(obj) or os.path.getmtime(obj) < os.path.getmtime(src)
                  or os.path.getmtime(obj) < newest_header)
         cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
@@ -71,13 +77,13 @@ def build(verbose: bool = False, extra_flags=None) -> str:
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     objs = [o for _, _, o in jobs]
-    if stale_cmds or not os.path.exists(LIB):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
+    if stale_cmds or not os.path.exists(lib):
+        cmd = [nvcc, *ARCH, "-shared", "-o", lib + ".tmp", *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -662,6 +662,44 @@ int launch_transpose(const hvec<TransposeSeg>& segs, cudaStream_t stream) {
   return ROT_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Guard regions of bounds-checked builds: one CTA of 64 threads per region,
+// one 32-bit word per thread.
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxGuards = 1024;
+
+struct GuardBatch {
+  int count;
+  uint64_t off[kMaxGuards];
+};
+
+__global__ void guard_kernel(const __grid_constant__ GuardBatch b, uint32_t* work, int* status,
+                             int check) {
+  if (blockIdx.x >= b.count) return;
+  uint32_t* g = work + b.off[blockIdx.x] / 4;
+  for (int i = threadIdx.x; i < (int)(kGuardBytes / 4); i += blockDim.x) {
+    if (!check) {
+      g[i] = kGuardWord;
+    } else if (g[i] != kGuardWord && status) {
+      atomicCAS(status, ROT_OK, ROT_ECORRUPT);
+    }
+  }
+}
+
+int launch_guards(const hvec<uint64_t>& offsets, void* work, int* status, bool check,
+                  cudaStream_t stream) {
+  thread_local static GuardBatch b;  // ~8 KB parameter block: keep off the stack
+  for (size_t base = 0; base < offsets.size(); base += kMaxGuards) {
+    b.count = (int)std::min<size_t>(kMaxGuards, offsets.size() - base);
+    for (int i = 0; i < b.count; ++i) b.off[i] = offsets[base + i];
+    guard_kernel<<<b.count, 64, 0, stream>>>(b, static_cast<uint32_t*>(work), status,
+                                            check ? 1 : 0);
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+  }
+  return ROT_OK;
+}
+
 int launch_fill(const hvec<FillSeg>& segs, cudaStream_t stream) {
   return launch_segs(segs, 8.0, fill_kernel, stream);
 }

@@ -102,9 +102,14 @@ namespace {
 
 struct Cursor {
   uint64_t at = 0;
+  hvec<uint64_t>* guards = nullptr;  // bounds-checked builds: a guard after every slice
   uint64_t take(uint64_t bytes) {
     const uint64_t o = at;
     at = align256(at + bytes);
+    if (guards) {
+      guards->push_back(at);
+      at += kGuardBytes;
+    }
     return o;
   }
   uint64_t floats(int64_t rows, int64_t ld) { return take(4ull * (uint64_t)rows * (uint64_t)ld); }
@@ -168,9 +173,11 @@ void build_layout(rot_plan* p) {
   // momentum kernel stays live across the refresh, so the regions do not
   // overlap.
   p->work.resize(p->groups.size());
+  p->guards.assign(p->groups.size(), hvec<uint64_t>());
   uint64_t most = 256;
   for (size_t g = 0; g < p->groups.size(); ++g) {
     Cursor w;
+    if (kChecked) w.guards = &p->guards[g];
     hvec<WorkLayout>& WL = p->work[g];
     WL.resize(p->groups[g].size());
     for (size_t k = 0; k < p->groups[g].size(); ++k) {

@@ -88,6 +88,9 @@ struct rot_plan {
   uint64_t ranks_off = 0;  // int32 pairs (rank_u, rank_v) per item
   rot::hvec<rot::ItemLayout> items;
   rot::hvec<rot::hvec<rot::WorkLayout>> work;  // [group][position in group]
+  // bounds-checked builds (ROT_CHECK): offsets of the 256-byte guard regions
+  // after every workspace slice, per micro-group (empty otherwise)
+  rot::hvec<rot::hvec<uint64_t>> guards;
 };
 
 namespace rot {

@@ -167,6 +167,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   const int compact = p->state_format == ROT_STATE_COMPACT;
   const int mt_epi = compact ? kEpiStoreBF16 : kEpiStoreF32;  // M~ as the state keeps it
   Range group_range("rot: micro-group");
+  if (kChecked) ROT_TRY(launch_guards(p->guards[g], work, status, false, s));
 
   // (1) momentum, and the TF32 split of G (3xF16: its scaled fp16 split)
   if (f16) {
@@ -413,6 +414,8 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     ROT_TRY(gemm_grouped(a, precision, status, s));
     ROT_TRY(gemm_grouped(b, precision, status, s));
   }
+  // bounds-checked builds: every guard of the group still holds its pattern
+  if (kChecked) ROT_TRY(launch_guards(p->guards[g], work, status, true, s));
   return ROT_OK;
 }
 
@@ -555,6 +558,7 @@ const char* rot_strerror(int code) {
     case ROT_ENONFINITE: return "non-finite value";
     case ROT_ENOTSUP: return "device is not sm_103 or feature not built";
     case ROT_ETOOLARGE: return "workspace need exceeds the static no-allocation scratch";
+    case ROT_ECORRUPT: return "a workspace guard was overwritten (bounds-checked build)";
     default: return "unknown error";
   }
 }

@@ -57,6 +57,21 @@ constexpr int kLdAlign = 32;
 inline int64_t pad_ld(int64_t x) { return (x + kLdAlign - 1) / kLdAlign * kLdAlign; }
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
+// Bounds-checked builds (compiled with ROT_CHECK): a guard region of
+// kGuardBytes follows every workspace slice (plan.cpp), filled with
+// kGuardWord before a micro-group's work and checked after it.
+#ifdef ROT_CHECK
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+constexpr uint64_t kGuardBytes = 256;
+constexpr uint32_t kGuardWord = 0xA5C3E1F7u;
+// fill (check = false) or check (true) the guards at `offsets` in `work`;
+// a changed word sets *status to ROT_ECORRUPT (if it held ROT_OK)
+int launch_guards(const hvec<uint64_t>& offsets, void* work, int* status, bool check,
+                  cudaStream_t stream);
+
 // A float32 matrix stored as an exact split x = hi + lo, hi = x rounded to
 // TF32 (10 explicit mantissa bits), lo = x - hi.  Tensor-core operands are
 // always held in this form; the float32 value is hi + lo.

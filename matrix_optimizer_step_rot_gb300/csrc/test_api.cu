@@ -1,4 +1,5 @@
 // Test entry points (include/rot_testing.h) and the wait-limit setter.
+#include "plan.h"
 #include "rot_internal.h"
 #include "rot_testing.h"
 
@@ -139,6 +140,29 @@ int rot_test_wait_timeout(uint64_t limit_ns, int32_t* status, void* stream) {
   if (!status || limit_ns > 10000000000ull) return ROT_EINVAL;
   return launch_wait_timeout(limit_ns, reinterpret_cast<int*>(status),
                              static_cast<cudaStream_t>(stream));
+}
+
+int rot_test_guard_offsets(const rot_plan* plan, int32_t group, uint64_t* offsets,
+                           int32_t capacity, int32_t* count) {
+  if (!plan || !count || group < 0 || (size_t)group >= plan->groups.size()) return ROT_EINVAL;
+  if (!rot::kChecked) return ROT_ENOTSUP;
+  const rot::hvec<uint64_t>& g = plan->guards[group];
+  *count = (int32_t)g.size();
+  for (int32_t i = 0; offsets && i < capacity && (size_t)i < g.size(); ++i) offsets[i] = g[i];
+  return ROT_OK;
+}
+
+int rot_test_check_guards(const rot_plan* plan, int32_t group, void* state, void* work,
+                          void* stream) {
+  if (!plan || !state || !work || group < 0 || (size_t)group >= plan->groups.size())
+    return ROT_EINVAL;
+  if (!rot::kChecked) return ROT_ENOTSUP;
+  try {
+    return rot::launch_guards(plan->guards[group], work, static_cast<int*>(state), true,
+                              static_cast<cudaStream_t>(stream));
+  } catch (const std::bad_alloc&) {
+    return ROT_ENOMEM;
+  }
 }
 
 uint64_t rot_set_wait_timeout_ns(uint64_t ns) {
