@@ -87,6 +87,24 @@ def test_plain_adam_steps_match_closed_form(precision):
 
 
 @pytest.mark.parametrize("precision", FULL)
+def test_item_larger_than_c_max_runs_in_its_own_group(precision):
+    """A matrix above the byte cap (130 x 90: 46800 bytes, C_max 40000) forms a
+    group of one (the planner's oversize rule) and steps like the others."""
+    shapes = ((130, 90), (60, 40), (40, 60))
+    wl = inputs.Workload("oversize", shapes, ("big", "a", "b"), 0.02, 1e-3, "normal", 6, 3,
+                         40000, 13)
+    W, opt = run_gpu(wl, precision)
+    groups = opt.plan.groups()
+    assert [0] in groups, groups
+    ref = orc.run(wl)
+    for i in range(wl.count):
+        Wo, st = ref[i]
+        e = rel(W[i].cpu().numpy().astype(np.float64), Wo)
+        assert e <= TOL_W[precision], (i, shapes[i], e)
+        assert opt.ranks(i) == (st.rank_u, st.rank_v), (i, shapes[i])
+
+
+@pytest.mark.parametrize("precision", FULL)
 def test_ragged_small_parity(precision):
     """Shapes that are not multiples of the tile sizes, several groups."""
     shapes = ((100, 36), (36, 100), (97, 97), (1, 40), (40, 1), (130, 70), (33, 65))
