@@ -37,10 +37,16 @@ TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 : BF16 tensor rates
 # micro-groups hold the same shapes, so traffic scales with the flops);
 # commands and figures in profiles/gemm_f16_block.md, gemm_tc_kernel_block.md
 TRAFFIC_PER_FLOP = {"3xf16": 3.2e-3, "3xtf32": 6.85e-3}
-# The same for the precise kernel (refresh products and the QR's products, in
-# the mix one refresh of a block launches): 37.6 GB over 2.418e12 flops in 55
-# launches (profiles/gemm_precise_block.md)
-TRAFFIC_PER_FLOP_PRECISE = 1.556e-2
+# The same for the precise kernel, by mode and class, in the mix one refresh
+# of a block launches (profiles/gemm_precise_block.md).  TF32-class modes: the
+# refresh products and the QR's products on the TF32 form, 37.6 GB over
+# 2.418e12 flops in 55 launches.  3xF16: the refresh products on the fp16
+# form (gemm_precise_f16), 4.34 GB over 1.319e12 flops in 2 launches, and the
+# QR's products on the TF32 form, 22.36 GB over 1.201e12 flops in 53 launches.
+TRAFFIC_PER_FLOP_PRECISE = {("3xtf32", "gemm_precise"): 1.556e-2,
+                            ("tf32", "gemm_precise"): 1.556e-2,
+                            ("3xf16", "gemm_precise"): 1.861e-2,
+                            ("3xf16", "gemm_precise_f16"): 3.29e-3}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -240,7 +246,8 @@ def run_ours(args):
 
     prof = {}
     import ctypes
-    names = ["gemm", "elementwise", "qr_panel", "qr_apply", "qr_other", "gemm_precise", "gemm_f16"]
+    names = ["gemm", "elementwise", "qr_panel", "qr_apply", "qr_other", "gemm_precise", "gemm_f16",
+             "gemm_precise_f16"]
     for c, nm in enumerate(names):
         n_, tot, mx, work = ctypes.c_uint64(), ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
         B.lib().rot_profile_read(c, ctypes.byref(n_), ctypes.byref(tot), ctypes.byref(mx),
@@ -369,6 +376,9 @@ def run_ours(args):
                              "K blocks of 32 summed with compensation)", tf32_sust, tf32_burst, 3),
             "gemm_f16": ("gemm_tc_kernel<F16> (tcgen05 kind::f16, 3 MMAs per K step)",
                          tf32_sust / TF32_OVER_BF16, tf32_burst / TF32_OVER_BF16, 3),
+            "gemm_precise_f16": ("gemm_tc_precise_kernel<F16> (tcgen05 kind::f16, 3 MMAs per K "
+                                 "step, K blocks of 32 summed with compensation)",
+                                 tf32_sust / TF32_OVER_BF16, tf32_burst / TF32_OVER_BF16, 3),
             "gemm": ("gemm_tc_kernel (tcgen05 kind::tf32, "
                      + ("1 MMA per K step)" if args.precision == "tf32" else "3 MMAs per K step)"),
                      tf32_sust, tf32_burst, 1 if args.precision == "tf32" else 3),
@@ -381,8 +391,8 @@ def run_ours(args):
             traffic = None
             if cls in ("gemm_f16", "gemm") and args.precision in TRAFFIC_PER_FLOP and g["launches"]:
                 traffic = TRAFFIC_PER_FLOP[args.precision] * g["work"] / g["launches"]
-            elif cls == "gemm_precise" and g["launches"]:
-                traffic = TRAFFIC_PER_FLOP_PRECISE * g["work"] / g["launches"]
+            elif (args.precision, cls) in TRAFFIC_PER_FLOP_PRECISE and g["launches"]:
+                traffic = TRAFFIC_PER_FLOP_PRECISE[(args.precision, cls)] * g["work"] / g["launches"]
             return {
                 "bound": "tensor", "kernel": desc, "class": cls,
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -390,7 +400,8 @@ def run_ours(args):
                 "traffic": traffic,
                 "traffic_unit": "bytes per launch (ncu, scaled from one block by flops)",
                 "peak_source": f"{peak_kind} bf16 sustained"
-                               + (" (fp16 and bf16 share the rate)" if cls == "gemm_f16" else
+                               + (" (fp16 and bf16 share the rate)"
+                                  if cls in ("gemm_f16", "gemm_precise_f16") else
                                   f" x {TF32_OVER_BF16:.4f} (nominal TF32:BF16 dense ratio)"),
                 "peak_burst": burst, "mma_issue_factor": issue,
                 "launches": g["launches"], "ms": g["ms"],

@@ -69,8 +69,9 @@ extern "C" {
                                      registers: float32-level accuracy at any K */
 #define ROT_PREC_3XF16 5     /* the three split products on power-of-two-scaled fp16
                                 splits (11 + 11 significant bits, as 3XTF32) at twice
-                                the TF32 tensor-core rate; the basis refresh's long
-                                products stay 3XTF32_PRECISE */
+                                the TF32 tensor-core rate; the basis refresh's products
+                                run on the precise kernel's fp16 form, the QR's on
+                                3XTF32_PRECISE */
 
 #define ROT_MAX_DIM 65536
 
@@ -214,7 +215,10 @@ int rot_state_init(const rot_plan* plan, void* state, void* stream);
  * initialised state blob; work: the workspace blob.  refresh != 0 runs the
  * basis refresh (2) before the rotated update.  precision of the rotation
  * products: ROT_PREC_TF32, ROT_PREC_3XTF32, ROT_PREC_3XTF32_PRECISE or
- * ROT_PREC_3XF16 (the basis refresh always uses ROT_PREC_3XTF32_PRECISE).
+ * ROT_PREC_3XF16 (the basis refresh always runs with float32-level accuracy:
+ * its products on the precise kernel, K blocks summed with compensation, in
+ * the TF32 split or, with ROT_PREC_3XF16, the scaled fp16 split; the QR in
+ * ROT_PREC_3XTF32_PRECISE).
  * The mode may change from step to step.  rank_rtol in
  * [1e-6, 1): the QR's numerical-rank threshold relative to the largest
  * column norm.  Non-finite inputs propagate (IEEE).
@@ -296,7 +300,9 @@ uint64_t rot_set_wait_timeout_ns(uint64_t ns);
 #define ROT_PROF_QR_OTHER 4    /* QR set-up, column norms, identity, sign fix; work = 0 */
 #define ROT_PROF_GEMM_PRECISE 5 /* precise 3xTF32 GEMM (refresh products, QR blocks) */
 #define ROT_PROF_GEMM_F16 6    /* 3xF16 tensor-core GEMM; work = 2 M N K flops */
-#define ROT_PROF_CLASSES 7
+#define ROT_PROF_GEMM_PRECISE_F16 7 /* the precise GEMM on scaled fp16 splits (the
+                                       refresh products in ROT_PREC_3XF16 mode) */
+#define ROT_PROF_CLASSES 8
 
 /* Turn event recording on (on != 0) or off.  Returns ROT_OK. */
 int rot_profile_enable(int32_t on);

@@ -19,13 +19,17 @@ extern "C" {
  * K)).  epi selects the output: 0 C = split(A B^T) into C (hi) and C + M*ldc
  * (lo); 1 the same for C^T (N x M, ldc >= M); 2 C = A B^T (float32); 3 C^T
  * = (A B^T)^T; 4 C -= alpha A B^T; 5 C (split) -= alpha A B^T.  precision:
- * ROT_PREC_TF32, ROT_PREC_3XTF32, ROT_PREC_3XTF32_PRECISE or ROT_PREC_3XF16
- * (rot.h).  With ROT_PREC_3XF16, A gets per-row power-of-two scales and B one
- * scale below its largest row norm (undone by the epilogue); epi 1 then
- * writes C^T as a fp16 split (hi: N x ldc halves at C, lo right after), and
- * epi 0 and 5 are rejected.  status: device int that receives ROT_ETIMEOUT
+ * ROT_PREC_TF32, ROT_PREC_3XTF32, ROT_PREC_3XTF32_PRECISE, ROT_PREC_3XF16
+ * (rot.h) or ROT_TEST_PREC_3XF16_PRECISE (the precise kernel on the scaled
+ * fp16 splits, which the basis refresh runs in ROT_PREC_3XF16 mode).  With
+ * either fp16 code, A gets per-row power-of-two scales and B one scale below
+ * its largest row norm (undone by the epilogue); epi 1 then writes C^T as a
+ * fp16 split (hi: N x ldc halves at C, lo right after), and epi 0 and 5 are
+ * rejected.  status: device int that receives ROT_ETIMEOUT
  * if a device-side wait gives up (may be NULL).
  * Errors: ROT_EINVAL (sizes < 1, null pointers, work too small), ROT_ECUDA. */
+#define ROT_TEST_PREC_3XF16_PRECISE 16
+
 int rot_test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
                   int32_t ldb, float* C, int32_t ldc, int32_t epi, float alpha,
                   int32_t precision, void* work, uint64_t work_bytes, int32_t* status,

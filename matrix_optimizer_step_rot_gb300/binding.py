@@ -34,6 +34,7 @@ ROT_PREC_TF32 = 1
 ROT_PREC_3XTF32 = 3
 ROT_PREC_3XTF32_PRECISE = 4
 ROT_PREC_3XF16 = 5
+ROT_TEST_PREC_3XF16_PRECISE = 16  # rot_test_gemm only: the precise kernel on fp16 splits
 ROT_WHICH_M, ROT_WHICH_V2, ROT_WHICH_U, ROT_WHICH_V = 0, 1, 2, 3
 ROT_STATE_FULL, ROT_STATE_COMPACT = 0, 1
 

@@ -244,12 +244,17 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
       }
       unsigned short* m16h = s.m16_hi + (int64_t)r * s.ldm;
       unsigned short* m16l = s.m16_lo + (int64_t)r * s.ldm;
-      float* mth = s.m_hi + (int64_t)r * s.ldm;
-      float* mtl = s.m_lo + (int64_t)r * s.ldm;
-      for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
-        const float m = ld_state(mr, c, bf);
-        split_f16(m * mscale, m16h[c], m16l[c]);
-        split_tf32(m, mth[c], mtl[c]);
+      if (s.m_hi) {
+        float* mth = s.m_hi + (int64_t)r * s.ldm;
+        float* mtl = s.m_lo + (int64_t)r * s.ldm;
+        for (int c = threadIdx.x; c < s.cols; c += blockDim.x) {
+          const float m = ld_state(mr, c, bf);
+          split_f16(m * mscale, m16h[c], m16l[c]);
+          split_tf32(m, mth[c], mtl[c]);
+        }
+      } else {
+        for (int c = threadIdx.x; c < s.cols; c += blockDim.x)
+          split_f16(ld_state(mr, c, bf) * mscale, m16h[c], m16l[c]);
       }
     }
     for (int q = threadIdx.x; q < nv; q += blockDim.x) {
@@ -413,6 +418,34 @@ __global__ void to_tf32_kernel(const __grid_constant__ SegBatch<ToTf32Seg> b) {
   }
 }
 
+// M^T as a fp16 split under one power-of-two scale (TransposeF16Seg), 32 x 32
+// tiles through shared memory: rows of M are read and rows of M^T written
+// 32 consecutive elements at a time.
+__global__ void transpose16_kernel(const __grid_constant__ SegBatch<TransposeF16Seg> b) {
+  __shared__ float tile[32][33];
+  const TransposeF16Seg& s = b.seg[blockIdx.y];
+  const bool bf = s.m_bf16 != 0;
+  const float scale = pow2_below(*s.rmax, kF16ScaleExp);
+  const int tiles_r = (s.rows + 31) / 32, tiles_c = (s.cols + 31) / 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+    for (int i = ty; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + tx;
+      tile[i][tx] = (r < s.rows && c < s.cols) ? ld_state(s.m, (int64_t)r * s.ld_src + c, bf) : 0.f;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int c = c0 + i, r = r0 + tx;  // output row c, column r
+      if (r < s.rows && c < s.cols) {
+        const int64_t o = (int64_t)c * s.ld_dst + r;
+        split_f16(tile[tx][i] * scale, s.d_hi[o], s.d_lo[o]);
+      }
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void combine16_kernel(const unsigned short* hi, const unsigned short* lo, int ld_src,
                                  float* dst, int ld_dst, int rows, int cols) {
   const int64_t total = (int64_t)rows * cols;
@@ -572,8 +605,12 @@ int launch_momentum16(const hvec<Momentum16Seg>& segs, float beta1, int* flag,
                       cudaStream_t stream) {
   // read G (4) and M (4); write M (4) and G's fp16 split (4) (refresh steps:
   // and M's fp16 split, 4, and TF32 split, 8)
+  // read G, M (8); write M, G's fp16 split (8); refresh: M's fp16 split (4)
+  // and, where asked for, its TF32 split (8)
   const bool split_m = !segs.empty() && segs[0].m16_hi;
-  return launch_rows(segs, split_m ? 28.0 : 16.0, momentum16_kernel, stream, beta1, flag);
+  const bool tf32_m = split_m && segs[0].m_hi;
+  return launch_rows(segs, tf32_m ? 28.0 : (split_m ? 20.0 : 16.0), momentum16_kernel, stream,
+                     beta1, flag);
 }
 
 namespace {
@@ -637,6 +674,29 @@ int launch_split16(const hvec<Split16Seg>& segs, cudaStream_t stream) {
 
 int launch_to_f16(const hvec<ToF16Seg>& segs, cudaStream_t stream) {
   return launch_segs(segs, 12.0, to_f16_kernel, stream);
+}
+
+int launch_transpose16(const hvec<TransposeF16Seg>& segs, cudaStream_t stream) {
+  for (size_t base = 0; base < segs.size(); base += kMaxSegs) {
+    SegBatch<TransposeF16Seg> b;
+    std::memset(&b, 0, sizeof(b));
+    b.count = (int)std::min<size_t>(kMaxSegs, segs.size() - base);
+    int64_t most = 0;
+    double bytes = 0.0;
+    for (int i = 0; i < b.count; ++i) {
+      b.seg[i] = segs[base + i];
+      most = std::max<int64_t>(most, (int64_t)((b.seg[i].rows + 31) / 32) *
+                                         ((b.seg[i].cols + 31) / 32));
+      // read M (4, or 2 as bf16); write the fp16 split (4)
+      bytes += (double)b.seg[i].rows * b.seg[i].cols * (b.seg[i].m_bf16 ? 6 : 8);
+    }
+    if (most == 0) continue;
+    dim3 grid((unsigned)std::min<int64_t>(most, 2048), b.count);
+    ProfScope prof(ROT_PROF_ELEMENTWISE, bytes, stream);
+    transpose16_kernel<<<grid, 256, 0, stream>>>(b);
+    if (cudaGetLastError() != cudaSuccess) return ROT_ECUDA;
+  }
+  return ROT_OK;
 }
 
 int launch_transpose(const hvec<TransposeSeg>& segs, cudaStream_t stream) {

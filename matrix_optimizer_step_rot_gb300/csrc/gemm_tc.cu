@@ -60,6 +60,10 @@ struct TcProblem {
   const float* in_r;
   const float* out_r;
   float c0;
+  // the precise 3xF16 kernel's scales (GemmProblem): per column of C and
+  // uniform for A, B and the fp16 split output
+  const float* col_inv;
+  Bound ina, inb, outb;
 };
 
 struct TcBatch {
@@ -69,6 +73,14 @@ struct TcBatch {
   int* status;
   unsigned long long limit_ns;
 };
+static_assert(sizeof(TcBatch) <= 32764, "kernel parameter block above 32764 bytes");
+
+// The bound of a Bound (see rot_internal.h); evaluated the same way wherever
+// a scale is applied or undone.
+__device__ __forceinline__ float bound_value(const Bound& b) {
+  const float r = *b.r;
+  return (b.sq ? r * r : r) * b.mul;
+}
 
 template <int BN, int STAGES, bool SPLIT3>
 struct Cfg {
@@ -646,6 +658,14 @@ __device__ __forceinline__ void store_chunk_rows(const TcProblem& P, int row0, i
 // QR's rank-256 and rank-512 updates and their factors) keep the whole sum in registers,
 // a plain float32 sum of the blocks, and use the four TMEM buffers so that
 // the MMAs run three blocks ahead while the epilogue finishes a tile.
+// F16: the same kernel on power-of-two scaled fp16 splits (kind::f16, 11 + 11
+// significant bits like the TF32 split).  A 128-byte TMA stage then holds 64
+// elements of K for the twelve MMA slots of a TF32 stage, twice the work.  It
+// is accumulated as two TMEM blocks of 32 (six MMAs each; one block of 64
+// measured about 1.2x the error on Gram products), and the pieces are folded
+// once per stage, so the sums in registers still cover up to 256 elements of
+// K between folds.  The epilogue undoes the operands' scales on the
+// compensated sum and may write a scaled fp16 split (kEpiStoreF16SplitT).
 // ---------------------------------------------------------------------------
 
 constexpr int kThreadsPrecise = 320;
@@ -665,10 +685,15 @@ __device__ __forceinline__ float kahan_add(float s, float x, float& c) {
   return t;
 }
 
-template <int STAGES, bool SHORT>
+template <int STAGES, bool SHORT, bool F16>
 __global__ void __launch_bounds__(kThreadsPrecise, 1)
     gemm_tc_precise_kernel(const __grid_constant__ TcBatch b) {
   constexpr int BN = 128;
+  constexpr int BKE = F16 ? 2 * BK : BK;  // elements per 128-byte K stage
+  // TMEM K blocks per stage: 32 elements each in both forms (two per fp16
+  // stage), kMmaPerBlock 32-byte MMA steps per block and term
+  constexpr int kSub = F16 ? 2 : 1;
+  constexpr int kMmaPerBlock = BK / 8 / kSub;
   constexpr int kBufs = SHORT ? 4 : kPreciseBufs;
   using C = Cfg<BN, STAGES, true>;
   constexpr uint32_t kCols = 512;
@@ -726,7 +751,7 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       decode(b, tile, pi, m0, nt);
       const TcProblem& P = b.p[pi];
       const int n0 = nt * BN;
-      const int kblocks = (P.K + BK - 1) / BK;
+      const int kblocks = (P.K + BKE - 1) / BKE;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit)) {
           ok = false;
@@ -736,7 +761,7 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
         ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
         armed_mask |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        const int x = kb * BK;
+        const int x = kb * BKE;
         ptx::tma_load_2d(st, &P.a_hi, &full[stage], x, m0);
         ptx::tma_load_2d(st + C::kABytes, &P.a_lo, &full[stage], x, m0);
         ptx::tma_load_2d(st + 2 * C::kABytes, &P.b_hi, &full[stage], x, n0);
@@ -751,7 +776,14 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       if (armed_mask & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u, limit);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issue
-    constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
+    constexpr uint32_t idesc = F16 ? ptx::idesc_f16(BM, BN) : ptx::idesc_tf32(BM, BN);
+    auto mma = [&](uint32_t d, uint64_t a, uint64_t bb, uint32_t accum) {
+      if (F16) {
+        ptx::umma_f16(d, a, bb, idesc, accum);
+      } else {
+        ptx::umma_tf32(d, a, bb, idesc, accum);
+      }
+    };
     int stage = 0;
     uint32_t phase = 0;
     uint32_t chunk = 0;  // K blocks issued so far by this CTA
@@ -759,34 +791,43 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
     for (int tile = blockIdx.x; ok && tile < b.total_tiles; tile += gridDim.x) {
       int pi, m0, nt;
       decode(b, tile, pi, m0, nt);
-      const int kblocks = (b.p[pi].K + BK - 1) / BK;
-      for (int kb = 0; kb < kblocks; ++kb, ++chunk) {
-        const uint32_t buf = chunk % kBufs, use = chunk / kBufs;
-        if (!ptx::mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, limit) ||
-            !ptx::mbar_wait(&full[stage], phase, abort_flag, limit)) {
+      const int kstages = (b.p[pi].K + BKE - 1) / BKE;
+      for (int ks = 0; ok && ks < kstages; ++ks) {
+        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, limit)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d = tmem_base + buf * BN;
         const uint32_t s = ptx::smem_u32(smem + stage * C::kStageBytes);
         const uint64_t ah = ptx::sw128_kmajor_desc(s);
         const uint64_t al = ptx::sw128_kmajor_desc(s + C::kABytes);
         const uint64_t bh = ptx::sw128_kmajor_desc(s + 2 * C::kABytes);
         const uint64_t bl = ptx::sw128_kmajor_desc(s + 2 * C::kABytes + C::kBBytes);
 #pragma unroll
-        for (int kk = 0; kk < BK / 8; ++kk) {  // cross terms first ...
-          const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);
-          ptx::umma_tf32(d, ah + off, bl + off, idesc, kk > 0 ? 1u : 0u);
-          ptx::umma_tf32(d, al + off, bh + off, idesc, 1u);
-        }
+        for (int sb = 0; sb < kSub; ++sb, ++chunk) {  // the stage's K blocks
+          const uint32_t buf = chunk % kBufs, use = chunk / kBufs;
+          if (!ptx::mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, limit)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem_base + buf * BN;
+          // 32 bytes per MMA (8 tf32 or 16 fp16 elements of K)
 #pragma unroll
-        for (int kk = 0; kk < BK / 8; ++kk) {  // ... then hi*hi
-          const uint64_t off = static_cast<uint64_t>(kk * 32 >> 4);
-          ptx::umma_tf32(d, ah + off, bh + off, idesc, 1u);
+          for (int kk = 0; kk < kMmaPerBlock; ++kk) {  // cross terms first ...
+            const uint64_t off = static_cast<uint64_t>((sb * kMmaPerBlock + kk) * 32 >> 4);
+            mma(d, ah + off, bl + off, kk > 0 ? 1u : 0u);
+            mma(d, al + off, bh + off, 1u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kMmaPerBlock; ++kk) {  // ... then hi*hi
+            const uint64_t off = static_cast<uint64_t>((sb * kMmaPerBlock + kk) * 32 >> 4);
+            mma(d, ah + off, bh + off, 1u);
+          }
+          ptx::umma_commit(&tfull[buf]);
         }
-        ptx::umma_commit(&empty[stage]);
-        ptx::umma_commit(&tfull[buf]);
+        if (!ok) break;
+        ptx::umma_commit(&empty[stage]);  // frees the stage once its MMAs finish
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -809,7 +850,7 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       decode(b, tile, pi, m0, nt);
       const TcProblem& P = b.p[pi];
       const int n0 = nt * BN;
-      const int kblocks = (P.K + BK - 1) / BK;
+      const int kblocks = kSub * ((P.K + BKE - 1) / BKE);
       // grp: per 16-column piece, the sum of the blocks since the piece's
       // last fold.  Piece q is folded after blocks q, q + 4, q + 8, ... so
       // that every block carries one piece's fold.
@@ -854,14 +895,17 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
           }
         }
         if (SHORT) continue;  // the whole sum stays in registers
-        // fold piece kb % 4 into the compensated running sum
-        const int fq = kb % kPreciseGroup;
+        // after every kSub-th block, fold piece (kb / kSub) % 4 into the
+        // compensated running sum (fp16 stages: one fold per stage)
+        if (kb % kSub != kSub - 1) continue;
+        const int fi = kb / kSub;
+        const int fq = fi % kPreciseGroup;
 #pragma unroll
         for (int q = 0; q < kPreciseCols / 16; ++q) {
           if (q != fq) continue;
           uint32_t sv[16], cv[16];
-          if (kb >= kPreciseGroup) {  // the piece has been folded before
-            ptx::tmem_wait_st();      // (its stores, four blocks ago, are done)
+          if (fi >= kPreciseGroup) {  // the piece has been folded before
+            ptx::tmem_wait_st();      // (its stores, four folds ago, are done)
             ptx::tmem_ld_32x32b_x16(sums + 16 * q, sv);
             ptx::tmem_ld_32x32b_x16(comps + 16 * q, cv);
             ptx::tmem_wait_ld();
@@ -891,7 +935,9 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       if (!SHORT) ptx::tmem_wait_st();
 #pragma unroll
       for (int q = 0; q < kPreciseCols / 16; ++q) {
-        if (SHORT || kblocks <= q) continue;  // never folded: grp holds the whole sum
+        // never folded (its first fold comes after block kSub (q + 1) - 1):
+        // grp holds the whole sum
+        if (SHORT || kblocks <= kSub * (q + 1) - 1) continue;
         uint32_t sv[16], cv[16];
         ptx::tmem_ld_32x32b_x16(sums + 16 * q, sv);
         ptx::tmem_ld_32x32b_x16(comps + 16 * q, cv);
@@ -904,6 +950,27 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
         }
       }
       const int row = m0 + quarter * 32 + lane;
+      float fout = 1.f;
+      if (F16) {  // undo the operands' power-of-two scales (exact)
+        float f = P.c0;
+        if (P.row_inv && row < P.M) f *= P.row_inv[row];
+        if (P.ina.r) f *= pow2_below_inv(bound_value(P.ina), kF16ScaleExp);
+        if (P.inb.r) f *= pow2_below_inv(bound_value(P.inb), kF16ScaleExp);
+        if (P.outb.r) fout = pow2_below(bound_value(P.outb), kF16ScaleExp);
+        // B's row scales: lane l loads those of columns l and 32 + l, and
+        // the warp passes them round (64 loads per thread spilled registers)
+        const int cbase = n0 + colgrp * kPreciseCols;
+        float ci0 = 1.f, ci1 = 1.f;
+        if (P.col_inv) {
+          ci0 = P.col_inv[min(cbase + lane, P.N - 1)];
+          ci1 = P.col_inv[min(cbase + 32 + lane, P.N - 1)];
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          grp[c] *= f * __shfl_sync(0xffffffffu, ci0, c);
+          grp[32 + c] *= f * __shfl_sync(0xffffffffu, ci1, c);
+        }
+      }
       float* stage = stage_area + (warp - 2) * kStageFloats;
 #pragma unroll
       for (int q = 0; q < kPreciseCols / 32; ++q) {
@@ -912,7 +979,13 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(grp[32 * q + c]);
         if (col0 < P.N) {
-          if (rows_path(P.epi)) {
+          if (F16) {  // (the refresh's outputs are transposed: no staging)
+            if (P.epi == kEpiStoreF16SplitT) {
+              store_chunk_f16t(P, row, col0, r, fout);
+            } else {
+              store_chunk(P, row, col0, r);
+            }
+          } else if (rows_path(P.epi)) {
             store_chunk_rows(P, m0 + quarter * 32, col0, r, stage);
           } else {
             store_chunk(P, row, col0, r);
@@ -985,7 +1058,7 @@ using TcKernel = void (*)(TcBatch);
 template <int BN, int STAGES, bool SPLIT3, bool PRECISE, bool F16, bool SHORT>
 TcKernel pick_kernel() {
   if constexpr (PRECISE)
-    return gemm_tc_precise_kernel<STAGES, SHORT>;
+    return gemm_tc_precise_kernel<STAGES, SHORT, F16>;
   else
     return gemm_tc_kernel<BN, STAGES, SPLIT3, F16>;
 }
@@ -997,7 +1070,7 @@ int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
   constexpr int kSmem =
       C::kSmem + (PRECISE ? kPreciseEpiWarps * kStageFloats * (int)sizeof(float) : 0);
   static_assert(kSmem <= 232448, "dynamic shared memory above 227 KB");
-  static_assert(!PRECISE || (BN == 128 && SPLIT3 && !F16), "precise variant is 3xTF32, BN = 128");
+  static_assert(!PRECISE || (BN == 128 && SPLIT3), "precise variants are split, BN = 128");
   const TcKernel kernel = pick_kernel<BN, STAGES, SPLIT3, PRECISE, F16, false>();
   const TcKernel kernel_short = pick_kernel<BN, STAGES, SPLIT3, PRECISE, F16, true>();
   static bool attr = false;
@@ -1043,6 +1116,10 @@ int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
       P.in_r = G.in_r;
       P.out_r = G.out_r;
       P.c0 = G.c0;
+      P.col_inv = G.col_inv;
+      P.ina = G.ina;
+      P.inb = G.inb;
+      P.outb = G.outb;
       total += ((G.M + BM - 1) / BM) * P.tiles_n;
       kmax = std::max(kmax, G.K);
       flops += 2.0 * G.M * (double)G.N * G.K;
@@ -1054,7 +1131,8 @@ int launch(const hvec<GemmProblem>& probs, int* status, cudaStream_t stream) {
     b.limit_ns = g_wait_limit_ns;
     const int grid = std::min(total, num_sms());
     {
-      ProfScope prof(PRECISE ? ROT_PROF_GEMM_PRECISE : (F16 ? ROT_PROF_GEMM_F16 : ROT_PROF_GEMM),
+      ProfScope prof(PRECISE ? (F16 ? ROT_PROF_GEMM_PRECISE_F16 : ROT_PROF_GEMM_PRECISE)
+                             : (F16 ? ROT_PROF_GEMM_F16 : ROT_PROF_GEMM),
                      flops, stream);
       const TcKernel k = (PRECISE && kmax <= kPreciseShortK) ? kernel_short : kernel;
       k<<<grid, PRECISE ? kThreadsPrecise : kThreads, kSmem, stream>>>(b);
@@ -1091,6 +1169,7 @@ int launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream) {
 int gemm_tc(const hvec<GemmProblem>& probs, int precision, int* status,
             cudaStream_t stream) {
   if (precision == kPrecPrecise) return launch<128, 3, true, true>(probs, status, stream);
+  if (precision == kPrecPrecise16) return launch<128, 3, true, true, true>(probs, status, stream);
   if (precision == ROT_PREC_3XF16) {
     bool narrow16 = true;
     for (const GemmProblem& P : probs) narrow16 = narrow16 && P.N <= 128;

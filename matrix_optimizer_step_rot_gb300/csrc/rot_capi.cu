@@ -13,6 +13,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -94,6 +95,22 @@ GemmProblem gp16(int M, int N, int K, const unsigned short* ah, const unsigned s
   P.row_inv = row_inv;
   P.in_r = in_r;
   P.out_r = out_r;
+  return P;
+}
+
+// A precise 3xF16 problem (kPrecPrecise16): fp16 operands scaled by rows
+// (row_inv for A's rows, col_inv for B's) or uniformly (ina, inb), c0 for the
+// bases' fixed 2^14; outb scales a fp16 split output.
+GemmProblem gpp16(int M, int N, int K, const unsigned short* ah, const unsigned short* al,
+                  int lda, const unsigned short* bh, const unsigned short* bl, int ldb, void* ch,
+                  void* cl, int ldc, int epi, float c0, const float* row_inv,
+                  const float* col_inv, Bound ina, Bound inb, Bound outb) {
+  GemmProblem P = gp16(M, N, K, ah, al, lda, bh, bl, ldb, ch, cl, ldc, epi, c0, row_inv, nullptr,
+                       nullptr);
+  P.col_inv = col_inv;
+  P.ina = ina;
+  P.inb = inb;
+  P.outb = outb;
   return P;
 }
 
@@ -183,7 +200,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       segs[k] = {G[i], F(state, L.mom), H(work, x.g_hi), H(work, x.g_lo),
                  F(work, x.g_rinv), F(work, x.g_rmax), L.m, L.n, L.ldn,
                  refresh ? H(work, x.m16_hi) : nullptr, H(work, x.m16_lo), F(work, x.m_rinv),
-                 F(work, x.m_rmax), F(work, x.m_hi), F(work, x.m_lo), compact};
+                 F(work, x.m_rmax), nullptr, nullptr, compact};
     }
     ROT_TRY(launch_momentum16(segs, beta1, nonfinite, s));
   } else {
@@ -199,65 +216,131 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
     ROT_TRY(launch_momentum(segs, beta1, nonfinite, s));
   }
 
-  // (2) basis refresh
+  // (2) basis refresh.  3xF16: the products on the precise kernel's fp16 form.
+  // M's operands: its row-scaled split (rows i scaled by s_i, m_rinv) and M^T
+  // under one scale below the row-norm bound r = *m_rmax (|M_ij| <= r).  The
+  // intermediates Z and the Gram matrices are stored as fp16 splits under one
+  // scale below a bound on their entries: |(M V)_ij| <= ||M_i|| <= r,
+  // |(M^T U)_ij| <= ||M_:j|| <= sqrt(m) r, |(M M^T)_ij| <= r^2,
+  // |(M^T M)_ij| <= m r^2 (U, V orthonormal).  A_U^T and A_V^T come out as the
+  // QR's TF32 splits, as in the other modes.
   if (refresh) {
     Range range("rot: basis refresh");
-    hvec<TransposeSeg> tr(n_items);
-    hvec<ToTf32Seg> old_bases;
-    for (size_t k = 0; k < n_items; ++k) {
-      const ItemLayout& L = p->items[items[k]];
-      const WorkLayout& x = WL[k];
-      tr[k] = {F(work, x.m_hi), F(work, x.m_lo), L.ldn, F(work, x.mT_hi), F(work, x.mT_lo),
-               L.ldm, L.m, L.n, 1, 1, 1};
-      // the products' TF32 operands U^T and V^T (the bases before the refresh)
-      old_bases.push_back({H(state, L.ut16_hi), H(state, L.ut16_lo), L.ldm, F(work, x.ut_hi),
-                           F(work, x.ut_lo), L.ldm, L.m, L.m});
-      old_bases.push_back({H(state, L.vt16_hi), H(state, L.vt16_lo), L.ldn, F(work, x.vt_hi),
-                           F(work, x.vt_lo), L.ldn, L.n, L.n});
-    }
-    ROT_TRY(launch_transpose(tr, s));
-    ROT_TRY(launch_to_tf32(old_bases, s));
+    if (f16) {
+      hvec<TransposeF16Seg> tr(n_items);
+      for (size_t k = 0; k < n_items; ++k) {
+        const ItemLayout& L = p->items[items[k]];
+        const WorkLayout& x = WL[k];
+        tr[k] = {F(state, L.mom), L.ldn, H(work, x.mT_hi), H(work, x.mT_lo), L.ldm, L.m, L.n,
+                 F(work, x.m_rmax), compact};
+      }
+      ROT_TRY(launch_transpose16(tr, s));
+      hvec<GemmProblem> first, second;
+      for (size_t k = 0; k < n_items; ++k) {
+        const ItemLayout& L = p->items[items[k]];
+        const WorkLayout& x = WL[k];
+        const int m = L.m, n = L.n;
+        const float* rinv = F(work, x.m_rinv);
+        const float* rmax = F(work, x.m_rmax);
+        const unsigned short *Mh = H(work, x.m16_hi), *Ml = H(work, x.m16_lo);  // m x ldn
+        const unsigned short *MTh = H(work, x.mT_hi), *MTl = H(work, x.mT_lo);  // n x ldm
+        const unsigned short *Uth = H(state, L.ut16_hi), *Utl = H(state, L.ut16_lo);
+        const unsigned short *Vth = H(state, L.vt16_hi), *Vtl = H(state, L.vt16_lo);
+        unsigned short *Zuh = H(work, x.zu_hi), *Zul = H(work, x.zu_lo);
+        unsigned short *Zvh = H(work, x.zv_hi), *Zvl = H(work, x.zv_lo);
+        float *Auh = F(work, x.aut_hi), *Aul = F(work, x.aut_lo);
+        float *Avh = F(work, x.avt_hi), *Avl = F(work, x.avt_lo);
+        const Bound none, bm{rmax, 1.f, 0};
+        if (n < m) {
+          // Z_U = M^T U, stored transposed (m x n);  A_U = M Z_U
+          const Bound bz{rmax, std::sqrt((float)m), 0};
+          first.push_back(gpp16(n, m, m, MTh, MTl, L.ldm, Uth, Utl, L.ldm, Zuh, Zul, x.zu_ld,
+                                kEpiStoreF16SplitT, kF16Inv, nullptr, nullptr, bm, none, bz));
+          second.push_back(gpp16(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, Auh, Aul, L.ldm,
+                                 kEpiStoreSplitT, 1.f, rinv, nullptr, none, bz, none));
+        } else {
+          // Gram M M^T (m x m, stored transposed);  A_U = Gram U
+          const Bound bg{rmax, 1.f, 1};
+          first.push_back(gpp16(m, m, n, Mh, Ml, L.ldn, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld,
+                                kEpiStoreF16SplitT, 1.f, rinv, rinv, none, none, bg));
+          second.push_back(gpp16(m, m, m, Zuh, Zul, x.zu_ld, Uth, Utl, L.ldm, Auh, Aul, L.ldm,
+                                 kEpiStoreSplitT, kF16Inv, nullptr, nullptr, bg, none, none));
+        }
+        if (m < n) {
+          // Z_V = M V, stored transposed (n x m);  A_V = M^T Z_V
+          first.push_back(gpp16(m, n, n, Mh, Ml, L.ldn, Vth, Vtl, L.ldn, Zvh, Zvl, x.zv_ld,
+                                kEpiStoreF16SplitT, kF16Inv, rinv, nullptr, none, none, bm));
+          second.push_back(gpp16(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, Avh, Avl, L.ldn,
+                                 kEpiStoreSplitT, 1.f, nullptr, nullptr, bm, bm, none));
+        } else {
+          // Gram M^T M (n x n, stored transposed);  A_V = Gram V
+          const Bound bg{rmax, (float)m, 1};
+          first.push_back(gpp16(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
+                                kEpiStoreF16SplitT, 1.f, nullptr, nullptr, bm, bm, bg));
+          second.push_back(gpp16(n, n, n, Zvh, Zvl, x.zv_ld, Vth, Vtl, L.ldn, Avh, Avl, L.ldn,
+                                 kEpiStoreSplitT, kF16Inv, nullptr, nullptr, bg, none, none));
+        }
+      }
+      ROT_TRY(gemm_grouped(first, kPrecPrecise16, status, s));
+      ROT_TRY(gemm_grouped(second, kPrecPrecise16, status, s));
+    } else {
+      hvec<TransposeSeg> tr(n_items);
+      hvec<ToTf32Seg> old_bases;
+      for (size_t k = 0; k < n_items; ++k) {
+        const ItemLayout& L = p->items[items[k]];
+        const WorkLayout& x = WL[k];
+        tr[k] = {F(work, x.m_hi), F(work, x.m_lo), L.ldn, F(work, x.mT_hi), F(work, x.mT_lo),
+                 L.ldm, L.m, L.n, 1, 1, 1};
+        // the products' TF32 operands U^T and V^T (the bases before the refresh)
+        old_bases.push_back({H(state, L.ut16_hi), H(state, L.ut16_lo), L.ldm, F(work, x.ut_hi),
+                             F(work, x.ut_lo), L.ldm, L.m, L.m});
+        old_bases.push_back({H(state, L.vt16_hi), H(state, L.vt16_lo), L.ldn, F(work, x.vt_hi),
+                             F(work, x.vt_lo), L.ldn, L.n, L.n});
+      }
+      ROT_TRY(launch_transpose(tr, s));
+      ROT_TRY(launch_to_tf32(old_bases, s));
 
-    hvec<GemmProblem> first, second;
-    for (size_t k = 0; k < n_items; ++k) {
-      const ItemLayout& L = p->items[items[k]];
-      const WorkLayout& x = WL[k];
-      const int m = L.m, n = L.n;
-      const float *Mh = F(work, x.m_hi), *Ml = F(work, x.m_lo);
-      const float *MTh = F(work, x.mT_hi), *MTl = F(work, x.mT_lo);
-      float *Zuh = F(work, x.zu_hi), *Zul = F(work, x.zu_lo);
-      float *Zvh = F(work, x.zv_hi), *Zvl = F(work, x.zv_lo);
-      float *Auh = F(work, x.aut_hi), *Aul = F(work, x.aut_lo);
-      float *Avh = F(work, x.avt_hi), *Avl = F(work, x.avt_lo);
-      if (n < m) {
-        // Z_U = M^T U (n x m), stored transposed (m x n);  A_U = M Z_U
-        first.push_back(gp(n, m, m, MTh, MTl, L.ldm, F(work, x.ut_hi), F(work, x.ut_lo), L.ldm,
-                           Zuh, Zul, x.zu_ld, kEpiStoreSplitT, 0.f, 1));
-        second.push_back(gp(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, Auh, Aul, L.ldm,
-                            kEpiStoreSplitT));
-      } else {
-        // Gram M M^T (m x m);  A_U = Gram U
-        first.push_back(gp(m, m, n, Mh, Ml, L.ldn, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld,
-                           kEpiStoreSplit, 0.f, 1));
-        second.push_back(gp(m, m, m, Zuh, Zul, x.zu_ld, F(work, x.ut_hi), F(work, x.ut_lo),
-                            L.ldm, Auh, Aul, L.ldm, kEpiStoreSplitT));
+      hvec<GemmProblem> first, second;
+      for (size_t k = 0; k < n_items; ++k) {
+        const ItemLayout& L = p->items[items[k]];
+        const WorkLayout& x = WL[k];
+        const int m = L.m, n = L.n;
+        const float *Mh = F(work, x.m_hi), *Ml = F(work, x.m_lo);
+        const float *MTh = F(work, x.mT_hi), *MTl = F(work, x.mT_lo);
+        float *Zuh = F(work, x.zu_hi), *Zul = F(work, x.zu_lo);
+        float *Zvh = F(work, x.zv_hi), *Zvl = F(work, x.zv_lo);
+        float *Auh = F(work, x.aut_hi), *Aul = F(work, x.aut_lo);
+        float *Avh = F(work, x.avt_hi), *Avl = F(work, x.avt_lo);
+        if (n < m) {
+          // Z_U = M^T U (n x m), stored transposed (m x n);  A_U = M Z_U
+          first.push_back(gp(n, m, m, MTh, MTl, L.ldm, F(work, x.ut_hi), F(work, x.ut_lo), L.ldm,
+                             Zuh, Zul, x.zu_ld, kEpiStoreSplitT, 0.f, 1));
+          second.push_back(gp(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, Auh, Aul, L.ldm,
+                              kEpiStoreSplitT));
+        } else {
+          // Gram M M^T (m x m);  A_U = Gram U
+          first.push_back(gp(m, m, n, Mh, Ml, L.ldn, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld,
+                             kEpiStoreSplit, 0.f, 1));
+          second.push_back(gp(m, m, m, Zuh, Zul, x.zu_ld, F(work, x.ut_hi), F(work, x.ut_lo),
+                              L.ldm, Auh, Aul, L.ldm, kEpiStoreSplitT));
+        }
+        if (m < n) {
+          // Z_V = M V (m x n), stored transposed (n x m);  A_V = M^T Z_V
+          first.push_back(gp(m, n, n, Mh, Ml, L.ldn, F(work, x.vt_hi), F(work, x.vt_lo), L.ldn,
+                             Zvh, Zvl, x.zv_ld, kEpiStoreSplitT, 0.f, 1));
+          second.push_back(gp(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, Avh, Avl, L.ldn,
+                              kEpiStoreSplitT));
+        } else {
+          // Gram M^T M (n x n);  A_V = Gram V
+          first.push_back(gp(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
+                             kEpiStoreSplit, 0.f, 1));
+          second.push_back(gp(n, n, n, Zvh, Zvl, x.zv_ld, F(work, x.vt_hi), F(work, x.vt_lo),
+                              L.ldn, Avh, Avl, L.ldn, kEpiStoreSplitT));
+        }
       }
-      if (m < n) {
-        // Z_V = M V (m x n), stored transposed (n x m);  A_V = M^T Z_V
-        first.push_back(gp(m, n, n, Mh, Ml, L.ldn, F(work, x.vt_hi), F(work, x.vt_lo), L.ldn,
-                           Zvh, Zvl, x.zv_ld, kEpiStoreSplitT, 0.f, 1));
-        second.push_back(gp(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, Avh, Avl, L.ldn,
-                            kEpiStoreSplitT));
-      } else {
-        // Gram M^T M (n x n);  A_V = Gram V
-        first.push_back(gp(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
-                           kEpiStoreSplit, 0.f, 1));
-        second.push_back(gp(n, n, n, Zvh, Zvl, x.zv_ld, F(work, x.vt_hi), F(work, x.vt_lo),
-                            L.ldn, Avh, Avl, L.ldn, kEpiStoreSplitT));
-      }
+      ROT_TRY(gemm_grouped(first, kPrecPrecise, status, s));
+      ROT_TRY(gemm_grouped(second, kPrecPrecise, status, s));
     }
-    ROT_TRY(gemm_grouped(first, kPrecPrecise, status, s));
-    ROT_TRY(gemm_grouped(second, kPrecPrecise, status, s));
 
     hvec<QrProblem> qp;
     int32_t* ranks = reinterpret_cast<int32_t*>(static_cast<char*>(state) + p->ranks_off);

@@ -97,6 +97,17 @@ enum GemmEpi : int {
   kEpiStoreBF16 = 7,    // C (row-major) <- acc rounded to bf16, into c.hi (compact state)
 };
 
+// A power-of-two operand or output scale of the precise 3xF16 products,
+// taken from a bound on the magnitudes it scales: bound = (*r)^(sq ? 2 : 1) *
+// mul, scale = pow2_below(bound) (split.cuh).  The producer of a scaled
+// array and its consumer evaluate the same expression, so the two scales
+// cancel exactly.  r == nullptr: no scale.
+struct Bound {
+  const float* r = nullptr;
+  float mul = 1.f;
+  int sq = 0;
+};
+
 struct GemmProblem {
   int M, N, K;
   const float* a_hi;
@@ -120,12 +131,23 @@ struct GemmProblem {
   const float* in_r = nullptr;
   const float* out_r = nullptr;
   float c0 = 1.f;
+  // kPrecPrecise16 problems: the accumulator is scaled by c0 * row_inv[row] *
+  // col_inv[col] / scale(ina) / scale(inb) (A's rows, B's rows and uniform
+  // operand scales), and a fp16 split output by scale(outb).  in_r / out_r
+  // are not read.
+  const float* col_inv = nullptr;
+  Bound ina, inb, outb;
 };
 
 // 3xTF32 with each K block of 32 accumulated afresh in TMEM (cross terms
 // first, hi*hi last) and summed in float32 registers (ROT_PREC_3XTF32_PRECISE);
 // used for products whose results cancel.
 constexpr int kPrecPrecise = ROT_PREC_3XTF32_PRECISE;
+
+// The same K-blocked, compensated kernel on scaled fp16 splits (kind::f16,
+// K blocks of 64, twice the TF32 rate; problems marked f16): the basis
+// refresh's products in ROT_PREC_3XF16 mode.  Not a rot_step mode.
+constexpr int kPrecPrecise16 = 16;
 
 // Upper bound on every device-side wait, in nanoseconds.
 extern uint64_t g_wait_limit_ns;
@@ -185,8 +207,8 @@ struct Momentum16Seg {
   float* g_rinv;
   float* g_rmax;
   int rows, cols, ldm;
-  // refresh steps: M's row-scaled fp16 split and its exact TF32 split too
-  // (m16_hi == nullptr: neither)
+  // refresh steps: M's row-scaled fp16 split (m16_hi == nullptr: none), and
+  // its exact TF32 split where m_hi is set
   unsigned short* m16_hi;
   unsigned short* m16_lo;
   float* m_rinv;
@@ -258,6 +280,23 @@ struct TransposeSeg {
   int dst_mma_only = 0;  // the split output feeds only tensor cores
 };
 int launch_transpose(const hvec<TransposeSeg>& segs, cudaStream_t stream);
+
+// M^T as a fp16 split with one power-of-two scale for the whole matrix:
+// d = split(M^T * pow2_below(*rmax)), *rmax a bound on every |M_ij| (the
+// largest row norm that the momentum kernel leaves).  m: the state's momentum
+// (rows x cols, float32 or bf16 when m_bf16, ld_src elements); d_hi / d_lo:
+// fp16 arrays, cols x rows, ld_dst elements.
+struct TransposeF16Seg {
+  const float* m;
+  int ld_src;
+  unsigned short* d_hi;
+  unsigned short* d_lo;
+  int ld_dst;
+  int rows, cols;
+  const float* rmax;
+  int m_bf16;
+};
+int launch_transpose16(const hvec<TransposeF16Seg>& segs, cudaStream_t stream);
 
 // TF32 split (hi, lo: float32 arrays, lo rounded to TF32 as well) of a basis
 // held as a 2^14-scaled fp16 split; dst is src (transpose == 0) or src^T.

@@ -27,15 +27,18 @@ uint64_t rot_test_gemm_work_bytes(int32_t M, int32_t N, int32_t K) {
 
 namespace {
 
+static_assert(ROT_TEST_PREC_3XF16_PRECISE == kPrecPrecise16, "test code of the precise 3xF16 kernel");
+
 int test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, const float* B,
               int32_t ldb, float* C, int32_t ldc, int32_t epi, float alpha, int32_t precision,
               void* work, uint64_t work_bytes, int32_t* status, void* stream) {
   if (M < 1 || N < 1 || K < 1 || !A || !B || !C || !work) return ROT_EINVAL;
   if (lda < K || ldb < K || epi < kEpiStoreSplit || epi > kEpiApplySplit) return ROT_EINVAL;
+  const bool f16 = precision == ROT_PREC_3XF16 || precision == ROT_TEST_PREC_3XF16_PRECISE;
   if (precision != ROT_PREC_TF32 && precision != ROT_PREC_3XTF32 &&
-      precision != ROT_PREC_3XTF32_PRECISE && precision != ROT_PREC_3XF16)
+      precision != ROT_PREC_3XTF32_PRECISE && !f16)
     return ROT_EINVAL;
-  if (precision == ROT_PREC_3XF16 && (epi == kEpiStoreSplit || epi == kEpiApplySplit))
+  if (f16 && (epi == kEpiStoreSplit || epi == kEpiApplySplit))
     return ROT_EINVAL;  // no fp16 form of the untransposed split outputs
   const bool transposed = epi == kEpiStoreSplitT || epi == kEpiStoreF32T;
   if (ldc < (transposed ? M : N)) return ROT_EINVAL;
@@ -44,7 +47,7 @@ int test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int ldk = (int)pad_ld(K);
   char* w = static_cast<char*>(work);
-  if (precision == ROT_PREC_3XF16) {
+  if (f16) {
     // A: per-row scales; B: one scale below its largest row norm (the
     // epilogue undoes both).  Scaled fp16 splits, then the row scales of A and
     // B's norm bound in a small tail.
@@ -84,8 +87,12 @@ int test_gemm(int32_t M, int32_t N, int32_t K, const float* A, int32_t lda, cons
     P.alpha = alpha;
     P.f16 = 1;
     P.row_inv = rinv;
-    P.in_r = bnorm;
-    return gemm_grouped({P}, precision, reinterpret_cast<int*>(status), s);
+    if (precision == ROT_PREC_3XF16) {
+      P.in_r = bnorm;
+      return gemm_grouped({P}, precision, reinterpret_cast<int*>(status), s);
+    }
+    P.inb.r = bnorm;  // the same scale as B's split, as a Bound
+    return gemm_grouped({P}, kPrecPrecise16, reinterpret_cast<int*>(status), s);
   }
   float* a_hi = reinterpret_cast<float*>(w);
   float* a_lo = reinterpret_cast<float*>(w + split_bytes(M, ldk));

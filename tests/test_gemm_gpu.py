@@ -13,7 +13,9 @@ SHAPES = [(128, 256, 32), (64, 64, 64), (300, 520, 100), (1, 40, 7), (33, 1, 65)
           (1000, 1000, 1000), (2048, 256, 4096), (130, 300, 2000)]
 PRECISE = B.ROT_PREC_3XTF32_PRECISE
 F16 = B.ROT_PREC_3XF16
-TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3, PRECISE: 1.5e-6, F16: 3e-6}
+PRECISE16 = B.ROT_TEST_PREC_3XF16_PRECISE  # the precise kernel on fp16 splits
+TOL = {B.ROT_PREC_3XTF32: 3e-6, B.ROT_PREC_TF32: 2e-3, PRECISE: 1.5e-6, F16: 3e-6,
+       PRECISE16: 1.5e-6}
 
 
 def tol(precision, K):
@@ -60,7 +62,7 @@ def run(M, N, K, epi, precision, alpha=0.5, seed=0, row_spread=False):
                     torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    if epi == 1 and precision == F16:
+    if epi == 1 and precision in (F16, PRECISE16):
         halves = C.view(torch.float16)
         out = (halves[:rows * ldc].double() + halves[rows * ldc:2 * rows * ldc].double())
         out = out.view(rows, ldc)
@@ -82,7 +84,7 @@ def run(M, N, K, epi, precision, alpha=0.5, seed=0, row_spread=False):
     return out, ref
 
 
-@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32, PRECISE, F16])
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, B.ROT_PREC_TF32, PRECISE, F16, PRECISE16])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_store_f32(M, N, K, precision):
     out, ref = run(M, N, K, 2, precision)
@@ -91,13 +93,14 @@ def test_gemm_store_f32(M, N, K, precision):
     assert err <= tol(precision, K), err
 
 
+@pytest.mark.parametrize("precision", [PRECISE, PRECISE16])
 @pytest.mark.parametrize("K", [6144, 12288])
-def test_gemm_precise_error_does_not_grow_with_k(K):
-    """The precise product sums its K/32 block partials with compensation:
-    its error stays near the split's own (1.3e-7 measured) at long K, where a
-    plain float32 running sum of the blocks gives 2.8e-7 (K = 6144) and
-    3.8e-7 (K = 12288)."""
-    out, ref = run(256, 256, K, 2, PRECISE, seed=K)
+def test_gemm_precise_error_does_not_grow_with_k(K, precision):
+    """The precise product sums its K-block partials (32 TF32 or 64 fp16
+    elements) with compensation: its error stays near the split's own (1.3e-7
+    measured) at long K, where a plain float32 running sum of the blocks gives
+    2.8e-7 (K = 6144) and 3.8e-7 (K = 12288)."""
+    out, ref = run(256, 256, K, 2, precision, seed=K)
     err = float((out - ref).norm() / ref.norm())
     print(f"precise 256x256x{K}: rel err {err:.3e}")
     assert err <= 2e-7, err
@@ -111,6 +114,19 @@ def test_gemm_precise_around_the_short_k_limit(M, N, K, epi):
     out, ref = run(M, N, K, epi, PRECISE, seed=K + epi)
     err = float((out - ref).norm() / ref.norm())
     assert err <= (1e-5 if epi in (4, 5) else TOL[PRECISE]), err
+
+
+@pytest.mark.parametrize("epi", [1, 2, 3, 4])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 300), (256, 384, 512), (130, 260, 513),
+                                   (200, 72, 1000)])
+def test_gemm_precise16_output_modes(M, N, K, epi):
+    """The precise kernel on fp16 splits: the short-K variant (K <= 512, up to
+    eight blocks of 64) and the long one; the transposed fp16-split store
+    (unscaled here), the float32 stores and the apply mode."""
+    out, ref = run(M, N, K, epi, PRECISE16, seed=K + epi)
+    err = float((out - ref).norm() / ref.norm())
+    bound = {1: 2e-6, 2: TOL[PRECISE16], 3: TOL[PRECISE16], 4: 1e-5}[epi]
+    assert err <= bound, err
 
 
 @pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, PRECISE])
@@ -134,7 +150,7 @@ def test_gemm_f16_output_modes(M, N, K, epi):
     assert err <= bound, err
 
 
-@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, F16])
+@pytest.mark.parametrize("precision", [B.ROT_PREC_3XTF32, F16, PRECISE16])
 def test_gemm_rows_of_very_different_magnitude(precision):
     """Rows of A spanning 18 decades and of B 6: per-row scaling keeps every
     row's product at float32-level relative accuracy in 3xF16, as 3xTF32
@@ -151,7 +167,9 @@ def test_gemm_f16_rejects_untransposed_split_modes():
     C = torch.zeros(2 * M * N, device="cuda")
     wb = B.rot_test_gemm_work_bytes(M, N, K)
     work = torch.empty(wb, dtype=torch.uint8, device="cuda")
-    for epi in (0, 5):
-        with pytest.raises(B.RotError):
-            B.rot_test_gemm(M, N, K, A.data_ptr(), K, A.data_ptr(), K, C.data_ptr(), N, epi, 1.0,
-                            F16, work.data_ptr(), wb, 0, torch.cuda.current_stream().cuda_stream)
+    for precision in (F16, PRECISE16):
+        for epi in (0, 5):
+            with pytest.raises(B.RotError):
+                B.rot_test_gemm(M, N, K, A.data_ptr(), K, A.data_ptr(), K, C.data_ptr(), N, epi,
+                                1.0, precision, work.data_ptr(), wb, 0,
+                                torch.cuda.current_stream().cuda_stream)

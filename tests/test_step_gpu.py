@@ -138,26 +138,51 @@ def test_medium_multi_block_parity(precision):
         assert orth(U) <= TOL_ORTH and orth(V) <= TOL_ORTH, (i, orth(U), orth(V))
 
 
+def scaled_workload(scale):
+    hyper = inputs.Hyper(eps=float(np.float32(1e-8 * scale)))
+    return inputs.Workload("scaled", ((96, 64), (64, 160)), ("a", "b"), 0.02, 1e-3 * scale,
+                           "normal", 4, 2, 1 << 30, 31, hyper)
+
+
+def arithmetic_allowance(wl, i):
+    """What 22-bit product operands allow for matrix i of wl, relative to its
+    update (the full-size parity tests' criterion, tests/test_configs_gpu.py):
+    A = max(4 F, the spread at 2^-22), F the larger of the float32 run's error
+    and the perturbation floor at 2^-24 (five oracle runs each)."""
+    w0 = wl.w0(i).astype(np.float64)
+    d0 = orc.run(wl, items=[i])[i][0] - w0
+    f32 = rel(orc.run(wl, items=[i], dtype=np.float32)[i][0] - w0, d0)
+    floor = max(rel(orc.run(wl, items=[i], perturb_seed=s)[i][0] - w0, d0) for s in range(5))
+    spread = max(rel(orc.run(wl, items=[i], perturb_seed=s, perturb_rel=2.0 ** -22)[i][0] - w0,
+                     d0) for s in range(5))
+    return max(4.0 * max(f32, floor), spread)
+
+
 @pytest.mark.parametrize("precision", FULL)
 def test_gradients_of_any_scale(precision):
     """Gradients of order 1e-15 and 1e9 -- far outside fp16's range (its
     smallest subnormal is 6e-8, its largest value 65504), and squared (M M^T U,
     then the QR's column norms) far outside float32's -- with eps scaled alike
     so that Adam's step is the same, match the oracle as at the usual scale:
-    3xF16 scales its operands, and the QR its input, by powers of two.  A zero
-    gradient leaves W unchanged."""
-    shapes = ((96, 64), (64, 160))
+    3xF16 scales its operands, and the QR its input, by powers of two.  Each
+    matrix is held to the bar or, where the method's own sensitivity exceeds
+    it, to what 22-bit product operands allow at the usual scale (the 64 x 160
+    matrix: float32 run 6.7e-5, spread at 2^-22 2.7e-4).  The sensitivity is
+    the same at every scale; the float32 run is taken at the usual scale,
+    where plain float32 does not underflow.  A zero gradient leaves W
+    unchanged."""
+    usual = scaled_workload(1.0)
+    allowed = [max(TOL_W[precision], arithmetic_allowance(usual, i)) for i in range(usual.count)]
     for scale in (1e-12, 1e12):
-        hyper = inputs.Hyper(eps=float(np.float32(1e-8 * scale)))
-        wl = inputs.Workload("scaled", shapes, ("a", "b"), 0.02, 1e-3 * scale, "normal", 4, 2,
-                             1 << 30, 31, hyper)
+        wl = scaled_workload(scale)
         Wg, _ = run_gpu(wl, precision)
         ref = orc.run(wl)
         for i in range(wl.count):
             w0 = wl.w0(i).astype(np.float64)
             e = rel(Wg[i].cpu().numpy().astype(np.float64) - w0, ref[i][0] - w0)
-            assert e <= TOL_W[precision], (scale, i, e)
-    wl = inputs.Workload("zero", shapes, ("a", "b"), 0.02, 0.0, "normal", 3, 2, 1 << 30, 32)
+            print(f"scale {scale:g} matrix {i}: update rel err {e:.3e} (allowed {allowed[i]:.3e})")
+            assert e <= allowed[i], (scale, i, e, allowed[i])
+    wl = inputs.Workload("zero", usual.shapes, ("a", "b"), 0.02, 0.0, "normal", 3, 2, 1 << 30, 32)
     Wg, opt = run_gpu(wl, precision)
     for i in range(wl.count):
         np.testing.assert_array_equal(Wg[i].cpu().numpy(), wl.w0(i))
