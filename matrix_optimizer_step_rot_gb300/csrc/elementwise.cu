@@ -241,6 +241,7 @@ __global__ void momentum16_kernel(const __grid_constant__ SegBatch<Momentum16Seg
       if (threadIdx.x == 0) {
         s.m_rinv[r] = pow2_below_inv(mmx, kF16ScaleExp);
         atomic_max_nonneg(s.m_rmax, row_norm_bound(msum, mmx, s.cols));
+        if (s.m_amax) atomic_max_nonneg(s.m_amax, mmx);
       }
       unsigned short* m16h = s.m16_hi + (int64_t)r * s.ldm;
       unsigned short* m16l = s.m16_lo + (int64_t)r * s.ldm;

@@ -198,11 +198,12 @@ void build_layout(rot_plan* p) {
       x.m16_lo = w.halves(L.m, L.ldn);
     }
     {
-      const uint64_t norms = w.floats(1, 3 * (int64_t)WL.size());
+      const uint64_t norms = w.floats(1, 4 * (int64_t)WL.size());
       for (size_t k = 0; k < WL.size(); ++k) {
-        WL[k].g_rmax = norms + 12 * k;
-        WL[k].d_rmax = norms + 12 * k + 4;
-        WL[k].m_rmax = norms + 12 * k + 8;
+        WL[k].g_rmax = norms + 16 * k;
+        WL[k].d_rmax = norms + 16 * k + 4;
+        WL[k].m_rmax = norms + 16 * k + 8;
+        WL[k].m_amax = norms + 16 * k + 12;
       }
     }
     for (size_t k = 0; k < p->groups[g].size(); ++k) {

@@ -43,11 +43,12 @@ struct WorkLayout {
   // inverse of its power-of-two scale (m floats each), and the largest row
   // 2-norm of G and of D (one float each, set by atomic max; the group's
   // row-norm slots are contiguous from WorkLayout of its first item's g_rmax,
-  // three floats per item, so one memset clears them).
+  // four floats per item, so one memset clears them).
   uint64_t g_rinv, d_rinv, g_rmax, d_rmax;
   // refresh steps in 3xF16: M's row-scaled fp16 split (m x ldn), its rows'
-  // inverse scales and row-norm bound (third float of the item's slots)
-  uint64_t m16_hi, m16_lo, m_rinv, m_rmax;
+  // inverse scales, row-norm bound and largest |M_ij| (third and fourth
+  // floats of the item's slots)
+  uint64_t m16_hi, m16_lo, m_rinv, m_rmax, m_amax;
   // TF32 splits of the bases (made from the fp16 state copies): U^T and
   // V^T for the refresh products; all four for the TF32-class rotation
   // modes.  M's TF32 split on refresh steps.

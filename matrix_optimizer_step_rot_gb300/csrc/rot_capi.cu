@@ -189,7 +189,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
   // (1) momentum, and the TF32 split of G (3xF16: its scaled fp16 split)
   if (f16) {
     Range range("rot: momentum");
-    if (cudaMemsetAsync(F(work, WL[0].g_rmax), 0, 12 * n_items, s) != cudaSuccess)
+    if (cudaMemsetAsync(F(work, WL[0].g_rmax), 0, 16 * n_items, s) != cudaSuccess)
       return ROT_ECUDA;
     hvec<Momentum16Seg> segs(n_items);
     for (size_t k = 0; k < n_items; ++k) {
@@ -200,7 +200,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
       segs[k] = {G[i], F(state, L.mom), H(work, x.g_hi), H(work, x.g_lo),
                  F(work, x.g_rinv), F(work, x.g_rmax), L.m, L.n, L.ldn,
                  refresh ? H(work, x.m16_hi) : nullptr, H(work, x.m16_lo), F(work, x.m_rinv),
-                 F(work, x.m_rmax), nullptr, nullptr, compact};
+                 F(work, x.m_rmax), nullptr, nullptr, compact, F(work, x.m_amax)};
     }
     ROT_TRY(launch_momentum16(segs, beta1, nonfinite, s));
   } else {
@@ -218,12 +218,12 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
 
   // (2) basis refresh.  3xF16: the products on the precise kernel's fp16 form.
   // M's operands: its row-scaled split (rows i scaled by s_i, m_rinv) and M^T
-  // under one scale below the row-norm bound r = *m_rmax (|M_ij| <= r).  The
-  // intermediates Z and the Gram matrices are stored as fp16 splits under one
-  // scale below a bound on their entries: |(M V)_ij| <= ||M_i|| <= r,
-  // |(M^T U)_ij| <= ||M_:j|| <= sqrt(m) r, |(M M^T)_ij| <= r^2,
-  // |(M^T M)_ij| <= m r^2 (U, V orthonormal).  A_U^T and A_V^T come out as the
-  // QR's TF32 splits, as in the other modes.
+  // under one scale below a = *m_amax, the largest |M_ij|.  The intermediates
+  // Z and the Gram matrices are stored as fp16 splits under one scale below a
+  // bound on their entries, with r = *m_rmax the largest row norm:
+  // |(M V)_ij| <= ||M_i|| <= r, |(M^T U)_ij| <= ||M_:j|| <= sqrt(m) a,
+  // |(M M^T)_ij| <= r^2, |(M^T M)_ij| <= m a^2 (U, V orthonormal).  A_U^T and
+  // A_V^T come out as the QR's TF32 splits, as in the other modes.
   if (refresh) {
     Range range("rot: basis refresh");
     if (f16) {
@@ -232,7 +232,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         const ItemLayout& L = p->items[items[k]];
         const WorkLayout& x = WL[k];
         tr[k] = {F(state, L.mom), L.ldn, H(work, x.mT_hi), H(work, x.mT_lo), L.ldm, L.m, L.n,
-                 F(work, x.m_rmax), compact};
+                 F(work, x.m_amax), compact};
       }
       ROT_TRY(launch_transpose16(tr, s));
       hvec<GemmProblem> first, second;
@@ -242,6 +242,7 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         const int m = L.m, n = L.n;
         const float* rinv = F(work, x.m_rinv);
         const float* rmax = F(work, x.m_rmax);
+        const float* amax = F(work, x.m_amax);
         const unsigned short *Mh = H(work, x.m16_hi), *Ml = H(work, x.m16_lo);  // m x ldn
         const unsigned short *MTh = H(work, x.mT_hi), *MTl = H(work, x.mT_lo);  // n x ldm
         const unsigned short *Uth = H(state, L.ut16_hi), *Utl = H(state, L.ut16_lo);
@@ -250,12 +251,12 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         unsigned short *Zvh = H(work, x.zv_hi), *Zvl = H(work, x.zv_lo);
         float *Auh = F(work, x.aut_hi), *Aul = F(work, x.aut_lo);
         float *Avh = F(work, x.avt_hi), *Avl = F(work, x.avt_lo);
-        const Bound none, bm{rmax, 1.f, 0};
+        const Bound none, bmt{amax, 1.f, 0}, bzv{rmax, 1.f, 0};
         if (n < m) {
           // Z_U = M^T U, stored transposed (m x n);  A_U = M Z_U
-          const Bound bz{rmax, std::sqrt((float)m), 0};
+          const Bound bz{amax, std::sqrt((float)m), 0};
           first.push_back(gpp16(n, m, m, MTh, MTl, L.ldm, Uth, Utl, L.ldm, Zuh, Zul, x.zu_ld,
-                                kEpiStoreF16SplitT, kF16Inv, nullptr, nullptr, bm, none, bz));
+                                kEpiStoreF16SplitT, kF16Inv, nullptr, nullptr, bmt, none, bz));
           second.push_back(gpp16(m, m, n, Mh, Ml, L.ldn, Zuh, Zul, x.zu_ld, Auh, Aul, L.ldm,
                                  kEpiStoreSplitT, 1.f, rinv, nullptr, none, bz, none));
         } else {
@@ -269,14 +270,14 @@ int run_group(const rot_plan* p, size_t g, float* const* W, const float* const* 
         if (m < n) {
           // Z_V = M V, stored transposed (n x m);  A_V = M^T Z_V
           first.push_back(gpp16(m, n, n, Mh, Ml, L.ldn, Vth, Vtl, L.ldn, Zvh, Zvl, x.zv_ld,
-                                kEpiStoreF16SplitT, kF16Inv, rinv, nullptr, none, none, bm));
+                                kEpiStoreF16SplitT, kF16Inv, rinv, nullptr, none, none, bzv));
           second.push_back(gpp16(n, n, m, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld, Avh, Avl, L.ldn,
-                                 kEpiStoreSplitT, 1.f, nullptr, nullptr, bm, bm, none));
+                                 kEpiStoreSplitT, 1.f, nullptr, nullptr, bmt, bzv, none));
         } else {
           // Gram M^T M (n x n, stored transposed);  A_V = Gram V
-          const Bound bg{rmax, (float)m, 1};
+          const Bound bg{amax, (float)m, 1};
           first.push_back(gpp16(n, n, m, MTh, MTl, L.ldm, MTh, MTl, L.ldm, Zvh, Zvl, x.zv_ld,
-                                kEpiStoreF16SplitT, 1.f, nullptr, nullptr, bm, bm, bg));
+                                kEpiStoreF16SplitT, 1.f, nullptr, nullptr, bmt, bmt, bg));
           second.push_back(gpp16(n, n, n, Zvh, Zvl, x.zv_ld, Vth, Vtl, L.ldn, Avh, Avl, L.ldn,
                                  kEpiStoreSplitT, kF16Inv, nullptr, nullptr, bg, none, none));
         }

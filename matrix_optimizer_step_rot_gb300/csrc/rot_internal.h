@@ -216,6 +216,7 @@ struct Momentum16Seg {
   float* m_hi;
   float* m_lo;
   int m_bf16 = 0;  // compact state: M is stored as bf16
+  float* m_amax = nullptr;  // refresh steps: grows to the largest |M_ij| (if set)
 };
 int launch_momentum16(const hvec<Momentum16Seg>& segs, float beta1, int* flag,
                       cudaStream_t stream);
@@ -283,7 +284,7 @@ int launch_transpose(const hvec<TransposeSeg>& segs, cudaStream_t stream);
 
 // M^T as a fp16 split with one power-of-two scale for the whole matrix:
 // d = split(M^T * pow2_below(*rmax)), *rmax a bound on every |M_ij| (the
-// largest row norm that the momentum kernel leaves).  m: the state's momentum
+// largest |M_ij| that the momentum kernel leaves).  m: the state's momentum
 // (rows x cols, float32 or bf16 when m_bf16, ld_src elements); d_hi / d_lo:
 // fp16 arrays, cols x rows, ld_dst elements.
 struct TransposeF16Seg {
