@@ -648,7 +648,7 @@ __device__ __forceinline__ void store_chunk_rows(const TcProblem& P, int row0, i
 // Measured relative error of a product with K = 6144 / 12288: 1.25e-7 with
 // this sum, 2.8e-7 / 3.8e-7 with a plain float32 sum of the blocks.
 // The four pieces are folded in turn (piece q after blocks q, q + 4, ...),
-// so each block costs one TMEM load and one add per element plus one
+// so each block costs one TMEM load and one add per element plus at most one
 // piece's fold, and no block stalls the MMAs behind a long fold.
 // TMEM: 2 K-block buffers x 128 columns, then the tile's 128 x 128 running
 // sums (columns 256..383) and their compensations (384..511).  Eight
@@ -852,8 +852,9 @@ __global__ void __launch_bounds__(kThreadsPrecise, 1)
       const int n0 = nt * BN;
       const int kblocks = kSub * ((P.K + BKE - 1) / BKE);
       // grp: per 16-column piece, the sum of the blocks since the piece's
-      // last fold.  Piece q is folded after blocks q, q + 4, q + 8, ... so
-      // that every block carries one piece's fold.
+      // last fold.  Folds come one per block (TF32 form) or one per stage of
+      // two blocks (fp16 form), piece q at folds q, q + 4, q + 8, ..., so that
+      // no block carries more than one piece's fold.
       float grp[kPreciseCols];
 #pragma unroll
       for (int c = 0; c < kPreciseCols; ++c) grp[c] = 0.f;
