@@ -48,6 +48,9 @@ TRAFFIC_PER_FLOP_PRECISE = {("3xtf32", "gemm_precise"): 1.556e-2,
                             ("3xf16", "gemm_precise"): 1.861e-2,
                             ("3xf16", "gemm_precise_f16"): 3.29e-3}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# the library's kernel classes (ROT_PROF_* in include/rot.h), in id order
+PROF_CLASSES = ["gemm", "elementwise", "qr_panel", "qr_apply", "qr_other", "gemm_precise",
+                "gemm_f16", "gemm_precise_f16"]
 
 
 def load_peaks():
@@ -246,9 +249,7 @@ def run_ours(args):
 
     prof = {}
     import ctypes
-    names = ["gemm", "elementwise", "qr_panel", "qr_apply", "qr_other", "gemm_precise", "gemm_f16",
-             "gemm_precise_f16"]
-    for c, nm in enumerate(names):
+    for c, nm in enumerate(PROF_CLASSES):
         n_, tot, mx, work = ctypes.c_uint64(), ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
         B.lib().rot_profile_read(c, ctypes.byref(n_), ctypes.byref(tot), ctypes.byref(mx),
                                  ctypes.byref(work))

@@ -2,6 +2,9 @@
 and its host planner matches the oracle's plan bit for bit."""
 
 import ctypes
+import importlib.util
+import os
+import re
 
 import numpy as np
 import pytest
@@ -219,3 +222,24 @@ def test_compact_state_bytes():
     assert B.lib().rot_plan_set_state_format(p.handle, B.ROT_STATE_FULL) == B.ROT_OK
     assert p.state_bytes()[0] == full
     assert B.lib().rot_plan_set_state_format(p.handle, 7) == B.ROT_EINVAL
+
+
+def test_profile_classes_match_the_header_and_the_bench():
+    """Every kernel class the header declares can be read, the next id is
+    refused, and the benchmark names exactly those classes."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "include", "rot.h")) as f:
+        header = f.read()
+    count = int(re.search(r"#define ROT_PROF_CLASSES (\d+)", header).group(1))
+    ids = sorted(int(v) for v in re.findall(r"#define ROT_PROF_\w+ (\d+)", header))
+    assert ids == list(range(count)) + [count]  # the classes, then ROT_PROF_CLASSES
+    L = B.lib()
+    n, tot, mx, work = ctypes.c_uint64(), ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    args = (ctypes.byref(n), ctypes.byref(tot), ctypes.byref(mx), ctypes.byref(work))
+    for c in range(count):
+        assert L.rot_profile_read(c, *args) == B.ROT_OK, c
+    assert L.rot_profile_read(count, *args) == B.ROT_EINVAL
+    spec = importlib.util.spec_from_file_location("bench_module", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    assert len(bench.PROF_CLASSES) == count
