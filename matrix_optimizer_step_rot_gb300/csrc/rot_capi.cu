@@ -128,18 +128,18 @@ int check_device() {
     return ROT_ECUDA;
   }
   const bool slot = dev >= 0 && dev < kMaxDevices;
-  int verdict = slot ? cached[dev].load(std::memory_order_acquire) : 0;
-  if (verdict == 0) {
+  int answer = slot ? cached[dev].load(std::memory_order_acquire) : 0;
+  if (answer == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
       cudaGetLastError();
       return ROT_ECUDA;
     }
-    verdict = (major == 10 && minor == 3) ? 1 : -1;
-    if (slot) cached[dev].store(verdict, std::memory_order_release);
+    answer = (major == 10 && minor == 3) ? 1 : -1;
+    if (slot) cached[dev].store(answer, std::memory_order_release);
   }
-  return verdict == 1 ? ROT_OK : ROT_ENOTSUP;
+  return answer == 1 ? ROT_OK : ROT_ENOTSUP;
 }
 
 // rot_step's host-side argument checks (no device access).
