@@ -174,6 +174,47 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=30)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def oracle_sample_one_thread(workload, steps, first_step=1):
+    """oracle_sample in a fresh process whose BLAS runs on one thread (the
+    thread count is fixed when numpy loads).  Returns (value, seconds) or
+    None if the child fails."""
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from matrix_optimizer_step_rot_gb300 import inputs; "
+            "v, s, _ = bench.oracle_sample(inputs.workload(%r), %d, first_step=%d); "
+            "print(json.dumps([v, s]))" % (ROOT, workload, steps, first_step))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                           timeout=600, env=dict(os.environ, **ONE_THREAD_ENV))
+        if r.returncode != 0:
+            return None
+        v, secs = json.loads(r.stdout.strip().splitlines()[-1])
+        return v, secs
+    except Exception:
+        return None
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -464,7 +505,12 @@ def run_ours(args):
         if world == 1 and not args.no_cpu_baseline:
             v, secs_cpu, desc = oracle_sample(wl, 5, first_step=1)
             out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_cores(),
-                                   "kind": "oracle", "sample": desc, "seconds": secs_cpu}
+                                   "kind": "oracle", "sample": desc, "seconds": secs_cpu,
+                                   "cpu_model": cpu_model()}
+            one = oracle_sample_one_thread(args.workload, 5, first_step=1)
+            if one is not None:
+                out["cpu_baseline"]["one_thread"] = {"value": one[0], "unit": UNIT,
+                                                     "cores": 1, "seconds": one[1]}
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -512,7 +558,7 @@ def run_reference(args):
         "data": "synthetic (seeded counter-based generator)",
         "config": workload_config(wl, args.precision),  # the GPU arm's config, unchanged
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)

@@ -24,6 +24,20 @@ def test_reference_arm_json_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"] == d["cpu_baseline"]["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["cpu_model"]
     # the GPU arm's config: same workload keys and the default precision mode
     assert d["config"]["precision"] == "3xf16"
     assert "full stack" in d["config"]["workload"]
+
+
+def test_one_thread_oracle_sample():
+    """The CPU baseline's one-thread leg: the oracle sample in a child process
+    with BLAS held to one thread (a small sample of the tiny workload here)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    out = bench.oracle_sample_one_thread("tiny", 2, first_step=1)
+    assert out is not None
+    value, secs = out
+    assert value > 0 and secs > 0
+    assert bench.cpu_model()
